@@ -1,0 +1,244 @@
+"""CPU oracle for absorbed MLA decode over a latent KV cache -- TEST INFRASTRUCTURE.
+
+Only the tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg
+may import this module.  The library (``mla_latent_kv_07_gb300``) never does,
+and the two share no code: this file wraps ``mla_oracle.c`` (plain C, fp64
+attention, fp32 where the cache-write step fixes it) through ctypes.
+
+Array conventions: bf16 values travel as ``np.uint16`` bit patterns, FP8 codes
+as ``np.uint8``, scales as ``np.float32``; results are ``np.float64``.
+
+Sources: "DeepSeek-V3.2-Exp . KV cache" (cache-write and MQA-decode excerpts),
+"DeepSeek MLA architecture: how Multi-Head Latent Attention cuts KV cache by
+93%" sections 3-4 (decoupled rotary term, matrix absorption).  The readings
+taken where the pages are silent are listed at the top of ``mla_oracle.c``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "mla_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+DC, DR, BLK = 512, 64, 128
+NBLK = DC // BLK
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (ISO C, no FMA contraction, OpenMP)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".{os.getpid()}.tmp"
+    cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fopenmp",
+           "-shared", "-fPIC", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P, I64, I32, D = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_double
+            lib.orc_e4m3_encode_array.argtypes = [P, I64, P]
+            lib.orc_e4m3_value_array.argtypes = [P, I64, P]
+            lib.orc_f32_to_bf16_array.argtypes = [P, I64, P]
+            lib.orc_quantize_rows.argtypes = [P, I64, P, P]
+            lib.orc_dequant_rows.argtypes = [P, P, I64, P]
+            lib.orc_sparse_gather_lists.argtypes = [P, I32, I32, P, P, P]
+            lib.orc_decode_absorbed.argtypes = [I32, I64, P, P, P, P, P, I32, P, P, I32, D,
+                                                P, I32, P, P, P, I64]
+            lib.orc_decode_absorbed.restype = I32
+            lib.orc_decode_naive.argtypes = [I32, I64, P, P, P, P, P, P, I32, I32, P, D, P, P]
+            lib.orc_decode_naive.restype = I32
+            lib.orc_num_threads.restype = I32
+            _lib = lib
+    return _lib
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---------------------------------------------------------------- formats
+
+def num_threads() -> int:
+    return int(_load().orc_num_threads())
+
+
+def e4m3_encode(y) -> np.ndarray:
+    """fp32 -> E4M3 code, nearest-even, saturating to +-448."""
+    y = _c(y, np.float32)
+    out = np.empty(y.shape, np.uint8)
+    _load().orc_e4m3_encode_array(_p(y), y.size, _p(out))
+    return out
+
+
+def e4m3_value(codes) -> np.ndarray:
+    codes = _c(codes, np.uint8)
+    out = np.empty(codes.shape, np.float64)
+    _load().orc_e4m3_value_array(_p(codes), codes.size, _p(out))
+    return out
+
+
+def bf16_round(f) -> np.ndarray:
+    """fp32 -> bf16 bit pattern, nearest-even."""
+    f = _c(f, np.float32)
+    out = np.empty(f.shape, np.uint16)
+    _load().orc_f32_to_bf16_array(_p(f), f.size, _p(out))
+    return out
+
+
+def bf16_bits_to_f64(bits) -> np.ndarray:
+    bits = np.asarray(bits, dtype=np.uint16)
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+# ------------------------------------------------------ cache-write step
+
+def quantize_rows(x_bits) -> tuple[np.ndarray, np.ndarray]:
+    """Latent rows [..., 512] (bf16 bits) -> (codes [..., 512] u8, scales [..., 4] f32)."""
+    x = _c(x_bits, np.uint16)
+    assert x.shape[-1] == DC
+    n = x.size // DC
+    q = np.empty(x.shape, np.uint8)
+    s = np.empty(x.shape[:-1] + (NBLK,), np.float32)
+    _load().orc_quantize_rows(_p(x), n, _p(q), _p(s))
+    return q, s
+
+
+def dequant_rows(q, scales) -> np.ndarray:
+    """(codes, scales) -> the bf16 latent the decode attends to (bits)."""
+    q = _c(q, np.uint8)
+    s = _c(scales, np.float32)
+    n = q.size // DC
+    assert s.size == n * NBLK
+    out = np.empty(q.shape, np.uint16)
+    _load().orc_dequant_rows(_p(q), _p(s), n, _p(out))
+    return out
+
+
+def cache_append(cache: dict, kv_new_bits, pe_new_bits, start_pos) -> None:
+    """Write row start_pos[b] of every sequence b < B, in place.
+
+    ``cache`` holds numpy arrays: 'fmt' (0 bf16, 1 fp8), 'kv', 'pe' and, for
+    fmt 1, 'kv_scale'.  bf16 rows are copied; FP8 rows are block-quantised.
+    A start_pos outside [0, max_seq_len) raises (the library refuses it too).
+    """
+    kv_new = _c(kv_new_bits, np.uint16).reshape(-1, DC)
+    pe_new = _c(pe_new_bits, np.uint16).reshape(-1, DR)
+    S = cache["kv"].shape[1]
+    for b, t in enumerate(np.asarray(start_pos).reshape(-1)):
+        if not 0 <= t < S:
+            raise IndexError(f"start_pos {t} outside [0, {S})")
+        if cache["fmt"] == 0:
+            cache["kv"][b, t] = kv_new[b]
+        else:
+            q, s = quantize_rows(kv_new[b:b + 1])
+            cache["kv"][b, t] = q[0]
+            cache["kv_scale"][b, t] = s[0]
+        cache["pe"][b, t] = pe_new[b]
+
+
+# ------------------------------------------------------ gather indices
+
+def sparse_gather_lists(topk, end_pos) -> tuple[np.ndarray, np.ndarray]:
+    """Per sequence: sorted unique top-k entries in [0, end_pos); -1 padded."""
+    topk = _c(topk, np.int32)
+    B, K = topk.shape
+    ep = _c(end_pos, np.int32)
+    gidx = np.empty((B, K), np.int32)
+    gcount = np.empty((B,), np.int32)
+    _load().orc_sparse_gather_lists(_p(topk), B, K, _p(ep), _p(gidx), _p(gcount))
+    return gidx, gcount
+
+
+# ------------------------------------------------------ absorbed decode
+
+def decode_absorbed(cache: dict, q_latent, q_pe, end_pos, softmax_scale: float,
+                    pairs=None, topk=None, weights_upto: int = 0):
+    """fp64 absorbed decode.
+
+    q_latent [B, H, 512] and q_pe [B, H, 64] are bf16 bits (uint16) or exact
+    floats; ``pairs`` is an [n, 2] array of (b, h) to evaluate (default all).
+    Returns (out [n, 512] f64, lse [n] f64) and, if ``weights_upto`` > 0, the
+    attention weights [n, weights_upto] of positions 0..weights_upto-1.
+    """
+    ql = np.asarray(q_latent)
+    qp = np.asarray(q_pe)
+    if ql.dtype == np.uint16:
+        ql = bf16_bits_to_f64(ql)
+    if qp.dtype == np.uint16:
+        qp = bf16_bits_to_f64(qp)
+    ql = _c(ql, np.float64)
+    qp = _c(qp, np.float64)
+    B, H, dc = ql.shape
+    assert dc == DC and qp.shape == (B, H, DR)
+    if pairs is None:
+        pairs = np.array([(b, h) for b in range(B) for h in range(H)], np.int32)
+    pairs = _c(pairs, np.int32).reshape(-1, 2)
+    n = pairs.shape[0]
+    kv = np.ascontiguousarray(cache["kv"])
+    pe = _c(cache["pe"], np.uint16)
+    S = kv.shape[1]
+    scale = None
+    if cache["fmt"] == 1:
+        scale = _c(cache["kv_scale"], np.float32)
+    ep = _c(end_pos, np.int32)
+    K = 0
+    if topk is not None:
+        topk = _c(topk, np.int32)
+        K = topk.shape[1]
+    out = np.empty((n, DC), np.float64)
+    lse = np.empty((n,), np.float64)
+    w = np.empty((n, weights_upto), np.float64) if weights_upto > 0 else None
+    err = _load().orc_decode_absorbed(int(cache["fmt"]), S, _p(kv), _p(scale), _p(pe),
+                                      _p(ql), _p(qp), H, _p(ep), _p(topk), K,
+                                      float(softmax_scale), _p(pairs), n, _p(out), _p(lse),
+                                      _p(w), weights_upto)
+    if err:
+        raise MemoryError("oracle allocation failed")
+    return (out, lse, w) if w is not None else (out, lse)
+
+
+def decode_naive(cache: dict, wkv_b, q_nope, q_pe, end_pos, softmax_scale: float):
+    """fp64 non-absorbed MHA: keys/values expanded through wkv_b [H, 256, 512].
+
+    Returns (o [B, H, 128], lse [B, H]).  Tiny inputs only.
+    """
+    w = _c(wkv_b, np.float64)
+    qn = _c(q_nope, np.float64)
+    qp = np.asarray(q_pe)
+    if qp.dtype == np.uint16:
+        qp = bf16_bits_to_f64(qp)
+    qp = _c(qp, np.float64)
+    B, H, _ = qn.shape
+    kv = np.ascontiguousarray(cache["kv"])
+    pe = _c(cache["pe"], np.uint16)
+    scale = _c(cache["kv_scale"], np.float32) if cache["fmt"] == 1 else None
+    ep = _c(end_pos, np.int32)
+    o = np.empty((B, H, 128), np.float64)
+    lse = np.empty((B, H), np.float64)
+    err = _load().orc_decode_naive(int(cache["fmt"]), kv.shape[1], _p(kv), _p(scale), _p(pe),
+                                   _p(w), _p(qn), _p(qp), B, H, _p(ep), float(softmax_scale),
+                                   _p(o), _p(lse))
+    if err:
+        raise MemoryError("oracle allocation failed")
+    return o, lse
