@@ -1,0 +1,191 @@
+/*
+ * mla.h -- C ABI of libmla: absorbed Multi-Head Latent Attention decode over a
+ * compressed latent KV cache on one NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes (sources are web pages, cited by title/section):
+ *   - "DeepSeek-V3.2-Exp . KV cache" (atlas.klimoza.dev), cache-write excerpt:
+ *     each call writes the new rows of every sequence at start_pos, after
+ *     rounding the 512-wide latent through FP8 with one scale per 128 values;
+ *     the 64-wide rotary key is stored as is.
+ *   - same page, MQA-decode excerpt: scores = (q_latent . c_KV + q_pe . k_R)
+ *     * softmax_scale over cached positions 0..end_pos-1, an optional top-k
+ *     index mask (positions outside the list get -inf), softmax, and the
+ *     weighted sum of c_KV, which stays in the 512-wide latent space.
+ *   - "DeepSeek MLA architecture: how Multi-Head Latent Attention cuts KV
+ *     cache by 93%", sections 3-4: the score splits into a content term and a
+ *     rotary term, and W_UK / W_UV are absorbed into the query and applied
+ *     after the weighted sum (both outside this library: q_latent arrives
+ *     already absorbed and the output is returned in latent space).
+ *
+ * Conventions shared by every call
+ *   - The caller owns every buffer.  Device pointers must be device memory of
+ *     the current CUDA device; "host" pointers are ordinary host memory.  The
+ *     library allocates no device memory and keeps no state except cached
+ *     device attributes and driver entry points.
+ *   - All work is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream).  Nothing synchronises unless stated.
+ *   - Host-checkable errors return an MLA_ERR_* code before anything is
+ *     launched.  A failed launch returns MLA_ERR_CUDA.
+ *   - Conditions only the device can see never trap: they are clamped or
+ *     skipped and recorded in the status word of the workspace (see
+ *     mla_workspace_status).
+ *   - Sizes: latent width 512, rotary width 64, FP8 block 128 are fixed.
+ *     H must be 16, 32, 64 or 128.  Device pointers must be 16-byte aligned.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned pointer      */
+  MLA_ERR_OUT_OF_RANGE = 2,  /* a position outside [0, max_seq_len)             */
+  MLA_ERR_UNSUPPORTED = 3,   /* H, format or device not supported               */
+  MLA_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required      */
+  MLA_ERR_CUDA = 5           /* a CUDA runtime/driver call failed               */
+} mla_status;
+
+typedef enum {
+  MLA_KV_BF16 = 0,           /* kv: bf16 [max_batch, max_seq_len, 512]          */
+  MLA_KV_FP8_E4M3_B128 = 1   /* kv: e4m3 bytes [max_batch, max_seq_len, 512] and
+                                kv_scale: fp32 [max_batch, max_seq_len, 4]      */
+} mla_kv_format;
+
+/* Cache descriptor (caller-owned device buffers, row-major, one slot per
+ * sequence, as the register_buffer calls of "DeepSeek-V3.2-Exp . KV cache"
+ * lay them out: [max_batch_size, max_seq_len, width]).
+ *   kv       latent c_KV: bf16 or e4m3 codes, see mla_kv_format
+ *   kv_scale fp32 block scales [max_batch, max_seq_len, 4] (FP8 only; NULL
+ *            for bf16).  Scale j covers latent columns 128j..128j+127 and the
+ *            stored value is bf16(fp32(e4m3(code) * scale)).
+ *   pe       rotary key k_R, bf16 [max_batch, max_seq_len, 64]            */
+typedef struct {
+  int32_t fmt;               /* mla_kv_format */
+  int32_t max_batch;
+  int32_t max_seq_len;
+  void* kv;
+  float* kv_scale;
+  void* pe;
+} mla_cache;
+
+/* Bit flags of the device status word (OR-ed, sticky until the workspace is
+ * cleared by the next mla_decode / mla_decode_sparse call). */
+#define MLA_DEV_END_POS_CLAMPED   0x1u  /* an end_pos was < 0 or > max_end_pos  */
+#define MLA_DEV_APPEND_SKIPPED    0x2u  /* fused append: end_pos-1 out of range */
+#define MLA_DEV_PIPELINE_TIMEOUT  0x4u  /* a bounded wait in a kernel gave up   */
+
+/*
+ * mla_cache_append -- the cache-write step of "DeepSeek-V3.2-Exp . KV cache"
+ * (cache-write excerpt) and of "KV Cache Eviction Strategy in MLA ...",
+ * section "Write-Back Logic and Position Tracking": for b in [0, B) write
+ * kv_new[b] into row start_pos[b] of sequence slot b, and pe_new[b] into the
+ * same row of pe.  bf16 caches store the row unchanged.  FP8 caches store
+ * e4m3 codes and 4 fp32 scales: per 128-wide block, amax = max |x|, scale =
+ * fp32(amax / 448), code = e4m3(fp32(x / scale)) with round-to-nearest-even
+ * and saturation to +-448; an all-zero block stores scale 0 and code 0.
+ *
+ *   kv_new     device bf16 [B, 512]
+ *   pe_new     device bf16 [B, 64]
+ *   start_pos  HOST int32 [B]; each must be in [0, max_seq_len), otherwise
+ *              MLA_ERR_OUT_OF_RANGE and nothing is written.  (The page's claim
+ *              that writes past max_seq_len evict old rows does not hold for
+ *              PyTorch slice assignment, which drops the new rows silently;
+ *              the library refuses instead.)
+ *   B          1 <= B <= min(max_batch, 2048)
+ */
+MLA_API mla_status mla_cache_append(const mla_cache* cache, const void* kv_new, const void* pe_new,
+                            const int32_t* start_pos, int32_t B, void* stream);
+
+/*
+ * mla_workspace_size -- bytes of device workspace mla_decode (topk == 0) or
+ * mla_decode_sparse (topk = K > 0) needs for B sequences and H heads.  The
+ * workspace holds the split schedule, the per-split partial outputs and
+ * log-sum-exps, the gather lists and the device status word.  max_end_pos is
+ * accepted for interface stability; the size does not depend on it.
+ * Returns 0 for unsupported arguments.
+ */
+MLA_API size_t mla_workspace_size(int32_t B, int32_t H, int32_t max_end_pos, int32_t topk);
+
+/*
+ * mla_decode -- absorbed MLA decode for one query token per sequence
+ * ("DeepSeek-V3.2-Exp . KV cache", MQA-decode excerpt, without the index
+ * mask; "DeepSeek MLA architecture ...", sections 3-4):
+ *   s[b,h,t] = softmax_scale * (q_latent[b,h,:] . c[b,t,:] + q_pe[b,h,:] . kR[b,t,:])
+ *   for t in [0, end_pos[b]);  p = softmax_t(s);  out[b,h,:] = sum_t p c[b,t,:]
+ *   lse[b,h] = log sum_t exp(s[b,h,t])   (natural log)
+ * where c is the bf16 latent or its FP8 round trip.  Work is split along t
+ * across the GPU and merged by log-sum-exp.
+ *
+ *   q_latent    device bf16 [B, H, 512] (absorbed queries)
+ *   q_pe        device bf16 [B, H, 64]  (rotated rotary queries)
+ *   end_pos     device int32 [B]; positions read are 0..end_pos[b]-1.
+ *               Values < 0 or > max_end_pos are clamped on the device and
+ *               flagged (MLA_DEV_END_POS_CLAMPED).  end_pos[b] == 0 gives
+ *               out = 0 and lse = -inf.
+ *   max_end_pos host bound on every end_pos[b]; 1 <= max_end_pos <= max_seq_len
+ *   out         device bf16 [B, H, 512] (round to nearest even)
+ *   lse         device fp32 [B, H] or NULL
+ *   workspace   device, >= mla_workspace_size(B, H, max_end_pos, 0) bytes,
+ *               16-byte aligned; overwritten by the call
+ */
+MLA_API mla_status mla_decode(const mla_cache* cache, const void* q_latent, const void* q_pe,
+                      const int32_t* end_pos, int32_t max_end_pos, int32_t B, int32_t H,
+                      float softmax_scale, void* out, float* lse, void* workspace,
+                      size_t ws_bytes, void* stream);
+
+/*
+ * mla_decode_sparse -- the same decode restricted by the DeepSeek-V3.2 top-k
+ * index mask ("DeepSeek-V3.2-Exp . KV cache", MQA-decode excerpt: a tensor of
+ * -inf with zeros scattered at the top-k positions is added to the scores,
+ * shared by all heads).  Entries < 0 or >= end_pos[b] are skipped, repeated
+ * entries count once, and only the listed rows are read.
+ *
+ *   topk_idx    device int32 [B, K], 1 <= K <= 8192
+ *   kv_new, pe_new  NULL, or device bf16 [B, 512] / [B, 64]: first append
+ *               them at row end_pos[b]-1 (the cache-write step, on the same
+ *               stream), so the decode sees the newly written row.  Rows with
+ *               end_pos[b]-1 outside [0, max_seq_len) are skipped and flagged
+ *               (MLA_DEV_APPEND_SKIPPED).
+ *   gidx_out    NULL, or device int32 [B, K]: the sorted, de-duplicated valid
+ *               positions actually attended, padded with -1
+ *   gcount_out  NULL, or device int32 [B]: their count
+ *   workspace   >= mla_workspace_size(B, H, max_end_pos, K) bytes
+ *   other arguments as for mla_decode
+ */
+MLA_API mla_status mla_decode_sparse(const mla_cache* cache, const void* q_latent, const void* q_pe,
+                             const int32_t* end_pos, int32_t max_end_pos, int32_t B, int32_t H,
+                             float softmax_scale, const int32_t* topk_idx, int32_t K,
+                             const void* kv_new, const void* pe_new, void* out, float* lse,
+                             int32_t* gidx_out, int32_t* gcount_out, void* workspace,
+                             size_t ws_bytes, void* stream);
+
+/*
+ * mla_workspace_status -- copy the device status word of a workspace used by
+ * the last decode call into *flags (MLA_DEV_* bits).  Synchronises `stream`.
+ */
+MLA_API mla_status mla_workspace_status(const void* workspace, uint32_t* flags, void* stream);
+
+/* Human-readable name of a status code (static string). */
+MLA_API const char* mla_status_string(mla_status status);
+
+/* Text of the last CUDA error seen by this thread's last failing call
+ * (static per-thread buffer; empty if none). */
+MLA_API const char* mla_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

@@ -1,0 +1,291 @@
+// aux_kernels.cu -- the small kernels around the decode:
+//   append   cache-write step with FP8 block quantisation
+//            ("DeepSeek-V3.2-Exp . KV cache", cache-write excerpt)
+//   prep     top-k list -> sorted, de-duplicated, valid gather list
+//            (same page, MQA-decode excerpt: the index mask is a scatter of
+//            zeros into -inf, so repeats act once and order does not matter)
+//   schedule split every sequence's positions into units of about equal size
+//   combine  log-sum-exp merge of the per-unit partial outputs
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "common.cuh"
+
+namespace mla {
+namespace {
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ---------------------------------------------------------------- append
+// One CTA (4 warps) per row.  Warp j owns latent block j (128 values, 4 per
+// lane): amax by shuffle, scale = amax / 448 (IEEE fp32 division), codes =
+// e4m3 of x / scale with round-to-nearest-even and saturation.
+template <bool kDevicePos>
+__global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
+  const int b = blockIdx.x;
+  int row;
+  if (kDevicePos) {
+    row = p.end_pos[b] - 1;
+    if (row < 0 || row >= p.max_seq_len) {
+      if (threadIdx.x == 0) atomicOr(p.status, kDevAppendSkipped);
+      return;
+    }
+  } else {
+    row = p.pos[b];
+  }
+  const size_t r = (size_t)b * p.max_seq_len + row;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int col = warp * kBlk + lane * 4;
+  const uint2 raw = *reinterpret_cast<const uint2*>(
+      static_cast<const __nv_bfloat16*>(p.kv_new) + (size_t)b * kDc + col);
+  if (p.fmt == 0) {
+    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.kv) + r * kDc + col) = raw;
+  } else {
+    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    float2 x01 = __bfloat1622float2(h2[0]);
+    float2 x23 = __bfloat1622float2(h2[1]);
+    float amax = fmaxf(fmaxf(fabsf(x01.x), fabsf(x01.y)), fmaxf(fabsf(x23.x), fabsf(x23.y)));
+    amax = warp_max(amax);
+    const float scale = __fdiv_rn(amax, 448.0f);
+    uint32_t packed = 0;
+    if (amax > 0.0f) {
+      float2 y01 = make_float2(__fdiv_rn(x01.x, scale), __fdiv_rn(x01.y, scale));
+      float2 y23 = make_float2(__fdiv_rn(x23.x, scale), __fdiv_rn(x23.y, scale));
+      uint32_t lo = __nv_cvt_float2_to_fp8x2(y01, __NV_SATFINITE, __NV_E4M3);
+      uint32_t hi = __nv_cvt_float2_to_fp8x2(y23, __NV_SATFINITE, __NV_E4M3);
+      packed = (lo & 0xffffu) | (hi << 16);
+    }
+    *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.kv) + r * kDc + col) = packed;
+    if (lane == 0) p.kv_scale[r * kNblk + warp] = scale;
+  }
+  if (threadIdx.x < 8) {  // rotary key: 64 bf16 = 8 x 16 bytes
+    const uint4 v = reinterpret_cast<const uint4*>(
+        static_cast<const __nv_bfloat16*>(p.pe_new) + (size_t)b * kDr)[threadIdx.x];
+    reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.pe) + r * kDr)[threadIdx.x] = v;
+  }
+}
+
+// ------------------------------------------------------------ block scan
+// Exclusive prefix sum over the block's threads; returns the block total.
+__device__ int block_exclusive_scan(int v, int* smem /* >= 33 ints */, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) smem[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nwarps ? smem[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nwarps) smem[lane] = w;   // inclusive warp totals
+    if (lane == 31) smem[32] = w;
+  }
+  __syncthreads();
+  int excl = x - v + (warp > 0 ? smem[warp - 1] : 0);
+  *total = smem[32];
+  __syncthreads();
+  return excl;
+}
+
+// ------------------------------------------------------------ sparse prep
+// One CTA per sequence: invalid entries become INT_MAX, a bitonic sort puts
+// the list in order, repeats are dropped and the survivors compacted.
+__global__ void __launch_bounds__(1024) sparse_prep_kernel(const int* __restrict__ topk, int K,
+                                                          int Kpad, const int* __restrict__ end_pos,
+                                                          int max_end_pos, Workspace ws,
+                                                          int* gidx_out, int* gcount_out) {
+  extern __shared__ int sv[];
+  __shared__ int scan_smem[33];
+  const int b = blockIdx.x;
+  int T = end_pos[b];
+  if (T < 0 || T > max_end_pos) {
+    if (threadIdx.x == 0) atomicOr(ws.status, kDevEndPosClamped);
+    T = T < 0 ? 0 : max_end_pos;
+  }
+  for (int k = threadIdx.x; k < Kpad; k += blockDim.x) {
+    int v = k < K ? topk[(size_t)b * K + k] : INT_MAX;
+    sv[k] = (v >= 0 && v < T) ? v : INT_MAX;
+  }
+  __syncthreads();
+  for (int size = 2; size <= Kpad; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < Kpad; i += blockDim.x) {
+        int j = i ^ stride;
+        if (j > i) {
+          bool up = (i & size) == 0;
+          int a = sv[i], c = sv[j];
+          if ((a > c) == up) { sv[i] = c; sv[j] = a; }
+        }
+      }
+      __syncthreads();
+    }
+  }
+  // each thread owns a contiguous run of the sorted list
+  const int per = (Kpad + blockDim.x - 1) / blockDim.x;
+  const int k0 = threadIdx.x * per;
+  int keep = 0;
+  for (int k = k0; k < k0 + per && k < Kpad; ++k)
+    keep += (sv[k] != INT_MAX && (k == 0 || sv[k] != sv[k - 1])) ? 1 : 0;
+  int total;
+  int dst = block_exclusive_scan(keep, scan_smem, &total);
+  int* g = ws.gidx + (size_t)b * K;
+  for (int k = k0; k < k0 + per && k < Kpad; ++k) {
+    if (sv[k] != INT_MAX && (k == 0 || sv[k] != sv[k - 1])) {
+      g[dst] = sv[k];
+      if (gidx_out) gidx_out[(size_t)b * K + dst] = sv[k];
+      ++dst;
+    }
+  }
+  for (int k = total + threadIdx.x; k < K; k += blockDim.x) {
+    g[k] = -1;
+    if (gidx_out) gidx_out[(size_t)b * K + k] = -1;
+  }
+  if (threadIdx.x == 0) {
+    ws.gcount[b] = total;
+    ws.lengths[b] = total;
+    if (gcount_out) gcount_out[b] = total;
+  }
+}
+
+// --------------------------------------------------------------- schedule
+// Single CTA.  lengths[b] (dense: clamped end_pos; sparse: gather count) is
+// cut into units of `chunk` positions, chunk = ceil(total / target) rounded up
+// to the kernel's tile granule, so sum_b ceil(len_b / chunk) <= target + B.
+__global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ end_pos,
+                                                       int max_end_pos, Workspace ws, int B,
+                                                       int target, int granule) {
+  __shared__ int scan_smem[33];
+  __shared__ unsigned long long total_len;
+  if (threadIdx.x == 0) total_len = 0;
+  __syncthreads();
+  const int per = (B + blockDim.x - 1) / blockDim.x;
+  const int b0 = threadIdx.x * per;
+  unsigned long long mine = 0;
+  for (int b = b0; b < b0 + per && b < B; ++b) {
+    int len;
+    if (end_pos) {
+      len = end_pos[b];
+      if (len < 0 || len > max_end_pos) {
+        atomicOr(ws.status, kDevEndPosClamped);
+        len = len < 0 ? 0 : max_end_pos;
+      }
+      ws.lengths[b] = len;
+    } else {
+      len = ws.lengths[b];
+    }
+    mine += (unsigned long long)len;
+  }
+  atomicAdd(&total_len, mine);
+  __syncthreads();
+  long long chunk = ((long long)total_len + target - 1) / target;
+  chunk = ((chunk + granule - 1) / granule) * granule;
+  if (chunk < granule) chunk = granule;
+  int nmine = 0;
+  for (int b = b0; b < b0 + per && b < B; ++b)
+    nmine += (int)((ws.lengths[b] + chunk - 1) / chunk);
+  int total_units;
+  int u = block_exclusive_scan(nmine, scan_smem, &total_units);
+  for (int b = b0; b < b0 + per && b < B; ++b) {
+    const int len = ws.lengths[b];
+    const int n = (int)((len + chunk - 1) / chunk);
+    ws.seq[b] = make_int2(u, n);
+    for (int i = 0; i < n; ++i) {
+      int t0 = (int)(i * chunk);
+      int t1 = (int)((i + 1) * chunk < len ? (i + 1) * chunk : len);
+      ws.units[u + i] = Unit{b, t0, t1, 0};
+    }
+    u += n;
+  }
+  for (int i = total_units + threadIdx.x; i < ws.max_units; i += blockDim.x)
+    ws.units[i] = Unit{-1, 0, 0, 0};
+  if (threadIdx.x == 0) *ws.n_units = total_units;
+}
+
+// ---------------------------------------------------------------- combine
+// One CTA per (h, b); 128 threads x 4 latent columns.  out = sum_i w_i O_i,
+// w_i = exp(lse_i - lse), lse = log sum_i exp(lse_i).
+__global__ void __launch_bounds__(128) combine_kernel(Workspace ws, int H,
+                                                     __nv_bfloat16* __restrict__ out,
+                                                     float* __restrict__ lse_out) {
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int2 sq = ws.seq[b];
+  const int c = threadIdx.x * 4;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float lse = -INFINITY;
+  if (sq.y > 0) {
+    float m = -INFINITY;
+    for (int i = 0; i < sq.y; ++i) m = fmaxf(m, ws.part_lse[(size_t)(sq.x + i) * H + h]);
+    float wsum = 0.f;
+    for (int i = 0; i < sq.y; ++i) {
+      const size_t u = (size_t)(sq.x + i);
+      const float w = expf(ws.part_lse[u * H + h] - m);
+      const float4 o = *reinterpret_cast<const float4*>(ws.part_o + (u * H + h) * kDc + c);
+      acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+      wsum += w;
+    }
+    const float inv = 1.0f / wsum;
+    acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
+    lse = m + logf(wsum);
+  }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  uint2 pk;
+  pk.x = *reinterpret_cast<uint32_t*>(&lo);
+  pk.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(out + ((size_t)b * H + h) * kDc + c) = pk;
+  if (lse_out && threadIdx.x == 0) lse_out[(size_t)b * H + h] = lse;
+}
+
+}  // namespace
+
+cudaError_t launch_append_host_pos(const AppendParams& p, cudaStream_t s) {
+  append_kernel<false><<<p.B, 128, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_append_device_pos(const AppendParams& p, cudaStream_t s) {
+  append_kernel<true><<<p.B, 128, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int max_end_pos,
+                               const Workspace& ws, int B, int* gidx_out, int* gcount_out,
+                               cudaStream_t s) {
+  int Kpad = 2;
+  while (Kpad < K) Kpad <<= 1;
+  size_t smem = sizeof(int) * (size_t)Kpad;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(sparse_prep_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  sparse_prep_kernel<<<B, 1024, smem, s>>>(topk, K, Kpad, end_pos, max_end_pos, ws, gidx_out,
+                                           gcount_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_schedule(const int* end_pos, int max_end_pos, const Workspace& ws, int B,
+                            int target, int granule, cudaStream_t s) {
+  schedule_kernel<<<1, 1024, 0, s>>>(end_pos, max_end_pos, ws, B, target, granule);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const Workspace& ws, int B, int H, void* out, float* lse,
+                           cudaStream_t s) {
+  combine_kernel<<<dim3(H, B), 128, 0, s>>>(ws, H, static_cast<__nv_bfloat16*>(out), lse);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -1,0 +1,125 @@
+// common.cuh -- constants, parameter blocks and the workspace layout shared by
+// the host API (mla_api.cu) and the kernels.  No kernel code lives here.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mla {
+
+constexpr int kDc = 512;          // latent width (kv_lora_rank)
+constexpr int kDr = 64;           // rotary key width (qk_rope_head_dim)
+constexpr int kDqk = kDc + kDr;   // 576: score contraction length
+constexpr int kBlk = 128;         // FP8 block width
+constexpr int kNblk = kDc / kBlk; // 4 scales per row
+constexpr int kMaxAppendB = 2048; // rows one append call may write
+constexpr int kMaxTopK = 8192;
+
+constexpr uint32_t kDevEndPosClamped = 0x1u;
+constexpr uint32_t kDevAppendSkipped = 0x2u;
+constexpr uint32_t kDevTimeout = 0x4u;
+
+// One unit of decode work: positions [t0, t1) of sequence b (dense), or
+// entries [t0, t1) of b's gather list (sparse).  b < 0: no work.
+struct Unit {
+  int b, t0, t1, pad;
+};
+
+// Workspace carve-up.  Every region starts on a 256-byte boundary.
+struct Workspace {
+  uint32_t* status;   // device status word (MLA_DEV_* bits)
+  int* n_units;       // units actually scheduled
+  int2* seq;          // [B] (first unit, unit count)
+  int* lengths;       // [B] clamped end_pos (dense) or gather count (sparse)
+  Unit* units;        // [max_units]
+  float* part_lse;    // [max_units, H]
+  float* part_o;      // [max_units, H, 512]
+  int* gidx;          // [B, K] sorted unique gather lists (sparse only)
+  int* gcount;        // [B]
+  size_t bytes;
+  int max_units;
+};
+
+inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Units the scheduler aims for: enough CTAs to fill every SM about twice.
+inline int target_units(int H, int num_sms) {
+  int per_unit = H / 16;                 // head-group CTAs per unit (mma.sync path)
+  int t1 = (2 * num_sms + per_unit - 1) / per_unit;
+  int t2 = num_sms / 2;                  // cluster-pair path: one pair per unit
+  return t1 > t2 ? t1 : t2;
+}
+
+inline Workspace carve_workspace(void* base, int B, int H, int K, int num_sms) {
+  Workspace w{};
+  w.max_units = target_units(H, num_sms) + B;
+  char* p = static_cast<char*>(base);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    char* r = p ? p + off : nullptr;
+    off += align256(bytes);
+    return r;
+  };
+  char* hdr = take(16);
+  w.status = reinterpret_cast<uint32_t*>(hdr);
+  w.n_units = hdr ? reinterpret_cast<int*>(hdr + 4) : nullptr;
+  w.seq = reinterpret_cast<int2*>(take(sizeof(int2) * (size_t)B));
+  w.lengths = reinterpret_cast<int*>(take(sizeof(int) * (size_t)B));
+  w.units = reinterpret_cast<Unit*>(take(sizeof(Unit) * (size_t)w.max_units));
+  w.part_lse = reinterpret_cast<float*>(take(sizeof(float) * (size_t)w.max_units * H));
+  w.part_o = reinterpret_cast<float*>(take(sizeof(float) * (size_t)w.max_units * H * kDc));
+  if (K > 0) {
+    w.gidx = reinterpret_cast<int*>(take(sizeof(int) * (size_t)B * K));
+    w.gcount = reinterpret_cast<int*>(take(sizeof(int) * (size_t)B));
+  }
+  w.bytes = off;
+  return w;
+}
+
+// Parameters of the append kernels.
+struct AppendParams {
+  int fmt;
+  int max_seq_len;
+  void* kv;
+  float* kv_scale;
+  void* pe;
+  const void* kv_new;     // bf16 [B, 512]
+  const void* pe_new;     // bf16 [B, 64]
+  const int* end_pos;     // device positions (fused path): row = end_pos[b] - 1
+  uint32_t* status;
+  int B;
+  int pos[kMaxAppendB];   // host positions (plain path)
+};
+
+// Parameters of the decode kernels.
+struct DecodeParams {
+  int fmt;
+  int max_seq_len;
+  const void* kv;
+  const float* kv_scale;
+  const void* pe;
+  const void* q_latent;   // bf16 [B, H, 512]
+  const void* q_pe;       // bf16 [B, H, 64]
+  int B, H;
+  float scale_log2;       // softmax_scale * log2(e)
+  Workspace ws;
+  int K;                  // sparse list length (0 = dense)
+};
+
+// Launchers (defined in the kernel translation units).
+cudaError_t launch_append_host_pos(const AppendParams& p, cudaStream_t s);
+cudaError_t launch_append_device_pos(const AppendParams& p, cudaStream_t s);
+cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int max_end_pos,
+                               const Workspace& ws, int B, int* gidx_out, int* gcount_out,
+                               cudaStream_t s);
+// end_pos != nullptr: dense (lengths = clamped end_pos); nullptr: the
+// lengths were already written (sparse prep).
+cudaError_t launch_schedule(const int* end_pos, int max_end_pos, const Workspace& ws, int B,
+                            int target_units, int granule, cudaStream_t s);
+cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s);
+int decode_mma_granule();
+cudaError_t launch_combine(const Workspace& ws, int B, int H, void* out, float* lse,
+                           cudaStream_t s);
+
+}  // namespace mla

@@ -1,0 +1,235 @@
+// mla_api.cu -- the C ABI declared in include/mla.h: argument checks, the
+// workspace carve-up and the launch sequence of each call.  Every check that
+// the host can make happens before the first launch.
+#include <mutex>
+#include <stdio.h>
+#include <string.h>
+
+#include "../../include/mla.h"
+#include "common.cuh"
+
+namespace {
+
+thread_local char g_last_error[256] = "";
+
+mla_status cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, cudaGetErrorString(e));
+  return MLA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// SM count of the current device, cached per device.
+int num_sms(int* out) {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return -1;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      return -1;
+    }
+    cache[dev] = n;
+  }
+  *out = cache[dev];
+  return 0;
+}
+
+bool supported_heads(int H) { return H == 16 || H == 32 || H == 64 || H == 128; }
+
+mla_status check_cache(const mla_cache* c) {
+  if (!c || !c->kv || !c->pe) return MLA_ERR_INVALID_ARG;
+  if (c->fmt != MLA_KV_BF16 && c->fmt != MLA_KV_FP8_E4M3_B128) return MLA_ERR_UNSUPPORTED;
+  if (c->max_batch <= 0 || c->max_seq_len <= 0) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(c->kv) || !aligned16(c->pe)) return MLA_ERR_INVALID_ARG;
+  if (c->fmt == MLA_KV_FP8_E4M3_B128 && (!c->kv_scale || !aligned16(c->kv_scale)))
+    return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+struct DecodeArgs {
+  const mla_cache* cache;
+  const void* q_latent;
+  const void* q_pe;
+  const int32_t* end_pos;
+  int32_t max_end_pos, B, H;
+  float softmax_scale;
+  void* out;
+  float* lse;
+  void* workspace;
+  size_t ws_bytes;
+};
+
+mla_status check_decode(const DecodeArgs& a, int K, mla::Workspace* ws) {
+  mla_status st = check_cache(a.cache);
+  if (st != MLA_OK) return st;
+  if (!supported_heads(a.H)) return MLA_ERR_UNSUPPORTED;
+  if (a.B <= 0 || a.B > a.cache->max_batch) return MLA_ERR_INVALID_ARG;
+  if (a.max_end_pos <= 0 || a.max_end_pos > a.cache->max_seq_len) return MLA_ERR_OUT_OF_RANGE;
+  if (!a.q_latent || !a.q_pe || !a.end_pos || !a.out) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(a.q_latent) || !aligned16(a.q_pe) || !aligned16(a.out) || !aligned4(a.end_pos))
+    return MLA_ERR_INVALID_ARG;
+  if (a.lse && !aligned4(a.lse)) return MLA_ERR_INVALID_ARG;
+  if (!(a.softmax_scale == a.softmax_scale)) return MLA_ERR_INVALID_ARG;  // NaN
+  int sms = 0;
+  if (num_sms(&sms) != 0) return MLA_ERR_UNSUPPORTED;
+  mla::Workspace need = mla::carve_workspace(nullptr, a.B, a.H, K, sms);
+  if (!a.workspace || !aligned16(a.workspace) || a.ws_bytes < need.bytes) return MLA_ERR_WORKSPACE;
+  *ws = mla::carve_workspace(a.workspace, a.B, a.H, K, sms);
+  return MLA_OK;
+}
+
+mla::DecodeParams make_params(const DecodeArgs& a, const mla::Workspace& ws, int K) {
+  mla::DecodeParams p{};
+  p.fmt = a.cache->fmt;
+  p.max_seq_len = a.cache->max_seq_len;
+  p.kv = a.cache->kv;
+  p.kv_scale = a.cache->kv_scale;
+  p.pe = a.cache->pe;
+  p.q_latent = a.q_latent;
+  p.q_pe = a.q_pe;
+  p.B = a.B;
+  p.H = a.H;
+  p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
+  p.ws = ws;
+  p.K = K;
+  return p;
+}
+
+// schedule -> decode -> combine, after the lengths are known on the device.
+mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cudaStream_t s) {
+  int sms = 0;
+  num_sms(&sms);
+  cudaError_t e = mla::launch_schedule(K ? nullptr : a.end_pos, a.max_end_pos, ws, a.B,
+                                       mla::target_units(a.H, sms), mla::decode_mma_granule(), s);
+  if (e != cudaSuccess) return cuda_fail(e, "schedule");
+  e = mla::launch_decode_mma(make_params(a, ws, K), s);
+  if (e != cudaSuccess) return cuda_fail(e, "decode");
+  e = mla::launch_combine(ws, a.B, a.H, a.out, a.lse, s);
+  if (e != cudaSuccess) return cuda_fail(e, "combine");
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+mla_status mla_cache_append(const mla_cache* cache, const void* kv_new, const void* pe_new,
+                            const int32_t* start_pos, int32_t B, void* stream) {
+  g_last_error[0] = 0;
+  mla_status st = check_cache(cache);
+  if (st != MLA_OK) return st;
+  if (!kv_new || !pe_new || !start_pos) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(kv_new) || !aligned16(pe_new)) return MLA_ERR_INVALID_ARG;
+  if (B <= 0 || B > cache->max_batch || B > mla::kMaxAppendB) return MLA_ERR_INVALID_ARG;
+  for (int b = 0; b < B; ++b)
+    if (start_pos[b] < 0 || start_pos[b] >= cache->max_seq_len) return MLA_ERR_OUT_OF_RANGE;
+  mla::AppendParams p{};
+  p.fmt = cache->fmt;
+  p.max_seq_len = cache->max_seq_len;
+  p.kv = cache->kv;
+  p.kv_scale = cache->kv_scale;
+  p.pe = cache->pe;
+  p.kv_new = kv_new;
+  p.pe_new = pe_new;
+  p.B = B;
+  memcpy(p.pos, start_pos, sizeof(int32_t) * (size_t)B);
+  cudaError_t e = mla::launch_append_host_pos(p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "append");
+}
+
+size_t mla_workspace_size(int32_t B, int32_t H, int32_t max_end_pos, int32_t topk) {
+  (void)max_end_pos;
+  if (B <= 0 || !supported_heads(H) || topk < 0 || topk > mla::kMaxTopK) return 0;
+  int sms = 0;
+  if (num_sms(&sms) != 0) return 0;
+  return mla::carve_workspace(nullptr, B, H, topk, sms).bytes;
+}
+
+mla_status mla_decode(const mla_cache* cache, const void* q_latent, const void* q_pe,
+                      const int32_t* end_pos, int32_t max_end_pos, int32_t B, int32_t H,
+                      float softmax_scale, void* out, float* lse, void* workspace,
+                      size_t ws_bytes, void* stream) {
+  g_last_error[0] = 0;
+  DecodeArgs a{cache, q_latent, q_pe, end_pos, max_end_pos, B, H, softmax_scale, out, lse,
+               workspace, ws_bytes};
+  mla::Workspace ws;
+  mla_status st = check_decode(a, 0, &ws);
+  if (st != MLA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws.status, 0, 16, s);
+  if (e != cudaSuccess) return cuda_fail(e, "memset");
+  return run_decode(a, ws, 0, s);
+}
+
+mla_status mla_decode_sparse(const mla_cache* cache, const void* q_latent, const void* q_pe,
+                             const int32_t* end_pos, int32_t max_end_pos, int32_t B, int32_t H,
+                             float softmax_scale, const int32_t* topk_idx, int32_t K,
+                             const void* kv_new, const void* pe_new, void* out, float* lse,
+                             int32_t* gidx_out, int32_t* gcount_out, void* workspace,
+                             size_t ws_bytes, void* stream) {
+  g_last_error[0] = 0;
+  if (!topk_idx || K <= 0 || K > mla::kMaxTopK || !aligned4(topk_idx)) return MLA_ERR_INVALID_ARG;
+  if ((kv_new == nullptr) != (pe_new == nullptr)) return MLA_ERR_INVALID_ARG;
+  if (kv_new && (!aligned16(kv_new) || !aligned16(pe_new) || B > mla::kMaxAppendB))
+    return MLA_ERR_INVALID_ARG;
+  if ((gidx_out && !aligned4(gidx_out)) || (gcount_out && !aligned4(gcount_out)))
+    return MLA_ERR_INVALID_ARG;
+  DecodeArgs a{cache, q_latent, q_pe, end_pos, max_end_pos, B, H, softmax_scale, out, lse,
+               workspace, ws_bytes};
+  mla::Workspace ws;
+  mla_status st = check_decode(a, K, &ws);
+  if (st != MLA_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws.status, 0, 16, s);
+  if (e != cudaSuccess) return cuda_fail(e, "memset");
+  if (kv_new) {
+    mla::AppendParams p{};
+    p.fmt = cache->fmt;
+    p.max_seq_len = cache->max_seq_len;
+    p.kv = cache->kv;
+    p.kv_scale = cache->kv_scale;
+    p.pe = cache->pe;
+    p.kv_new = kv_new;
+    p.pe_new = pe_new;
+    p.end_pos = end_pos;
+    p.status = ws.status;
+    p.B = B;
+    e = mla::launch_append_device_pos(p, s);
+    if (e != cudaSuccess) return cuda_fail(e, "append");
+  }
+  e = mla::launch_sparse_prep(topk_idx, K, end_pos, max_end_pos, ws, B, gidx_out, gcount_out, s);
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_prep");
+  return run_decode(a, ws, K, s);
+}
+
+mla_status mla_workspace_status(const void* workspace, uint32_t* flags, void* stream) {
+  if (!workspace || !flags) return MLA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "status");
+}
+
+const char* mla_status_string(mla_status status) {
+  switch (status) {
+    case MLA_OK: return "MLA_OK";
+    case MLA_ERR_INVALID_ARG: return "MLA_ERR_INVALID_ARG";
+    case MLA_ERR_OUT_OF_RANGE: return "MLA_ERR_OUT_OF_RANGE";
+    case MLA_ERR_UNSUPPORTED: return "MLA_ERR_UNSUPPORTED";
+    case MLA_ERR_WORKSPACE: return "MLA_ERR_WORKSPACE";
+    case MLA_ERR_CUDA: return "MLA_ERR_CUDA";
+  }
+  return "MLA_ERR_UNKNOWN";
+}
+
+const char* mla_last_error(void) { return g_last_error; }
+
+}  // extern "C"
