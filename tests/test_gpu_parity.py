@@ -1,0 +1,254 @@
+"""GPU parity: the CUDA library against the CPU oracle on the same seeded
+inputs, called through the C ABI (ctypes binding).  Small cases compare every
+output and span several tiles with ragged tails; the five workloads run at
+their full sizes in the launch configuration the benchmark times and compare
+sampled (sequence, head) outputs the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mla_latent_kv_07_gb300 as mla
+from mla_latent_kv_07_gb300 import inputs
+from oracle import oracle as orc
+
+from mla_cases import (bits, check_close, device_cache, f64, oracle_cache, sample_pairs,
+                       workload_cache)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from mla_latent_kv_07_gb300 import build
+    build.build()
+    mla.lib()
+
+
+def _rand_bf16(shape, seed):
+    return inputs.randn_bf16(shape, seed)
+
+
+# ------------------------------------------------------------------ append
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_append_bit_exact(fmt):
+    B, S = 64, 300
+    g = torch.Generator().manual_seed(7)
+    kv_new = (torch.randn(B, 512, generator=g) * torch.exp(torch.randn(B, 1, generator=g) * 4)).to(torch.bfloat16)
+    kv_new[0, :128] = 0.0                         # an all-zero block
+    kv_new[1, 128:256] = 448.0                    # scale exactly 1
+    kv_new[2, 256:384] = torch.tensor([2.0 ** -9, -2.0 ** -10] * 64)
+    pe_new = _rand_bf16((B, 64), 8)
+    start = np.random.default_rng(9).integers(0, S, B).astype(np.int32)
+    start[3] = S - 1
+    oc = oracle_cache(_rand_bf16((B, S, 512), 10), _rand_bf16((B, S, 64), 11), fmt)
+    dc = device_cache(oc)
+    mla.cache_append(dc, kv_new.cuda(), pe_new.cuda(), start)
+    orc.cache_append(oc, bits(kv_new), bits(pe_new), start)
+    torch.cuda.synchronize()
+    if fmt == 0:
+        assert np.array_equal(bits(dc.kv.cpu()), oc["kv"])
+    else:
+        assert np.array_equal(dc.kv.cpu().numpy(), oc["kv"])
+        assert np.array_equal(dc.kv_scale.cpu().numpy().view(np.uint32), oc["kv_scale"].view(np.uint32))
+    assert np.array_equal(bits(dc.pe.cpu()), oc["pe"])
+
+
+def test_append_refuses_positions_past_the_cache():
+    oc = oracle_cache(_rand_bf16((2, 8, 512), 1), _rand_bf16((2, 8, 64), 2), 1)
+    dc = device_cache(oc)
+    before = dc.kv.clone()
+    with pytest.raises(mla.MLAError) as e:
+        mla.cache_append(dc, _rand_bf16((2, 512), 3).cuda(), _rand_bf16((2, 64), 4).cuda(), [1, 8])
+    assert e.value.code == 2
+    torch.cuda.synchronize()
+    assert torch.equal(before, dc.kv)
+
+
+# ------------------------------------------------------------ small dense
+
+SMALL = [  # (fmt, H, end_pos per sequence, S)
+    (0, 16, [1, 31, 32, 33], 64),
+    (1, 16, [100, 257, 5], 300),
+    (0, 32, [64, 1, 200], 256),
+    (1, 64, [129, 77], 160),
+    (0, 128, [300, 33, 1], 320),
+    (1, 128, [1000, 513, 2, 64], 1024),
+]
+
+
+@pytest.mark.parametrize("fmt,H,ends,S", SMALL)
+def test_decode_small_all_outputs(fmt, H, ends, S):
+    B = len(ends)
+    seed = 100 * H + S + fmt
+    oc = oracle_cache(_rand_bf16((B, S, 512), seed), _rand_bf16((B, S, 64), seed + 1), fmt)
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((B, H, 512), seed + 2), _rand_bf16((B, H, 64), seed + 3)
+    end_pos = np.array(ends, np.int32)
+    sm = 0.1352
+    out, lse = mla.decode(dc, ql.cuda(), qp.cuda(), torch.from_numpy(end_pos).cuda(), S, sm)
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), end_pos, sm)
+    check_close(f64(out).reshape(-1, 512), ref, "out")
+    check_close(f64(lse).reshape(-1), ref_lse, "lse")
+
+
+def test_rows_past_end_pos_are_never_used():
+    # NaN codes, infinite scales and NaN rotary keys beyond end_pos
+    B, S, H = 2, 200, 128
+    oc = oracle_cache(_rand_bf16((B, S, 512), 21), _rand_bf16((B, S, 64), 22), 1)
+    ends = np.array([77, 130], np.int32)
+    for b, T in enumerate(ends):
+        oc["kv"][b, T:] = 0x7F
+        oc["kv_scale"][b, T:] = np.inf
+        oc["pe"][b, T:] = 0x7FC0
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((B, H, 512), 23), _rand_bf16((B, H, 64), 24)
+    out, lse = mla.decode(dc, ql.cuda(), qp.cuda(), torch.from_numpy(ends).cuda(), S, 0.2)
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), ends, 0.2)
+    check_close(f64(out).reshape(-1, 512), ref, "out")
+    check_close(f64(lse).reshape(-1), ref_lse, "lse")
+
+
+def test_empty_and_clamped_sequences():
+    B, S, H = 3, 64, 16
+    oc = oracle_cache(_rand_bf16((B, S, 512), 31), _rand_bf16((B, S, 64), 32), 0)
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((B, H, 512), 33), _rand_bf16((B, H, 64), 34)
+    ends = torch.tensor([0, 40, 50], dtype=torch.int32).cuda()
+    ws = mla.alloc_workspace(B, H, 48)
+    out, lse = mla.decode(dc, ql.cuda(), qp.cuda(), ends, 48, 0.3, workspace=ws)
+    flags = mla.workspace_status(ws)
+    assert flags == mla.DEV_END_POS_CLAMPED           # 50 > max_end_pos 48
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), np.array([0, 40, 48], np.int32), 0.3)
+    o = f64(out).reshape(-1, 512)
+    assert (o[:H] == 0).all() and np.isneginf(f64(lse)[0]).all()
+    check_close(o, ref, "out")
+    check_close(f64(lse).reshape(-1), ref_lse, "lse")
+    ends_ok = torch.tensor([0, 40, 48], dtype=torch.int32).cuda()
+    mla.decode(dc, ql.cuda(), qp.cuda(), ends_ok, 48, 0.3, workspace=ws)
+    assert mla.workspace_status(ws) == 0
+
+
+def test_workspace_too_small_is_refused():
+    oc = oracle_cache(_rand_bf16((1, 32, 512), 41), _rand_bf16((1, 32, 64), 42), 0)
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((1, 16, 512), 43).cuda(), _rand_bf16((1, 16, 64), 44).cuda()
+    ws = torch.empty(mla.workspace_size(1, 16, 32) - 256, dtype=torch.uint8, device="cuda")
+    with pytest.raises(mla.MLAError) as e:
+        mla.decode(dc, ql, qp, torch.tensor([32], dtype=torch.int32).cuda(), 32, 0.1, workspace=ws)
+    assert e.value.code == 4
+
+
+# ---------------------------------------------------------- small sparse
+
+def test_sparse_small_lists_and_outputs():
+    B, S, H, K = 4, 400, 128, 96
+    oc = oracle_cache(_rand_bf16((B, S, 512), 51), _rand_bf16((B, S, 64), 52), 1)
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((B, H, 512), 53), _rand_bf16((B, H, 64), 54)
+    ends = np.array([400, 37, 1, 250], np.int32)
+    rng = np.random.default_rng(55)
+    topk = rng.integers(-2, 420, (B, K)).astype(np.int32)
+    topk[1, :40] = np.arange(40)                    # covers all of a short sequence (with extras)
+    topk[3, 10:20] = topk[3, 0]                     # repeats
+    gidx = torch.empty((B, K), dtype=torch.int32, device="cuda")
+    gcnt = torch.empty((B,), dtype=torch.int32, device="cuda")
+    out, lse = mla.decode_sparse(dc, ql.cuda(), qp.cuda(), torch.from_numpy(ends).cuda(), S, 0.15,
+                                 torch.from_numpy(topk).cuda(), gidx=gidx, gcount=gcnt)
+    ref_g, ref_c = orc.sparse_gather_lists(topk, ends)
+    assert np.array_equal(gidx.cpu().numpy(), ref_g) and np.array_equal(gcnt.cpu().numpy(), ref_c)
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), ends, 0.15, topk=topk)
+    check_close(f64(out).reshape(-1, 512), ref, "out")
+    check_close(f64(lse).reshape(-1), ref_lse, "lse")
+
+
+def test_sparse_fused_append_sees_the_new_row():
+    B, S, H, K = 3, 128, 128, 64
+    oc = oracle_cache(_rand_bf16((B, S, 512), 61), _rand_bf16((B, S, 64), 62), 1)
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((B, H, 512), 63), _rand_bf16((B, H, 64), 64)
+    ends = np.array([128, 50, 7], np.int32)
+    topk = inputs.topk_indices(B, K, ends, 65).numpy()
+    kv_new, pe_new = _rand_bf16((B, 512), 66), _rand_bf16((B, 64), 67)
+    out, lse = mla.decode_sparse(dc, ql.cuda(), qp.cuda(), torch.from_numpy(ends).cuda(), S, 0.2,
+                                 torch.from_numpy(topk).cuda(), kv_new=kv_new.cuda(), pe_new=pe_new.cuda())
+    orc.cache_append(oc, bits(kv_new), bits(pe_new), ends - 1)
+    torch.cuda.synchronize()
+    assert np.array_equal(dc.kv.cpu().numpy(), oc["kv"])
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), ends, 0.2, topk=topk)
+    check_close(f64(out).reshape(-1, 512), ref, "out")
+    check_close(f64(lse).reshape(-1), ref_lse, "lse")
+
+
+# ------------------------------------------------------ full-size workloads
+
+def _run_dense_workload(w, per_seq):
+    oc, dc = workload_cache(w)
+    ql, qp = inputs.queries(w)
+    ends = inputs.end_positions(w)
+    out, lse = mla.decode(dc, ql.cuda(), qp.cuda(), ends.cuda(), w.S, w.softmax_scale)
+    pairs = None if per_seq is None else sample_pairs(w.B, w.H, per_seq, w.index)
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), ends.numpy(), w.softmax_scale,
+                                       pairs=pairs)
+    o = f64(out)
+    l = f64(lse)
+    if pairs is None:
+        got, got_l = o.reshape(-1, 512), l.reshape(-1)
+    else:
+        got = np.stack([o[b, h] for b, h in pairs])
+        got_l = np.array([l[b, h] for b, h in pairs])
+    check_close(got, ref, f"{w.name} out")
+    check_close(got_l, ref_lse, f"{w.name} lse")
+
+
+def test_workload1_tiny_all_outputs():
+    _run_dense_workload(inputs.WORKLOADS[1], None)
+
+
+def test_workload1_fp8_append_row():
+    # the tiny workload's one-row FP8 append: row 255 of a 1 x 256 FP8 cache
+    w = inputs.WORKLOADS[1]
+    oc = oracle_cache(inputs.latent_rows(w), inputs.rotary_rows(w), 1)
+    dc = device_cache(oc)
+    kv_new, pe_new = inputs.new_rows(w)
+    mla.cache_append(dc, kv_new.cuda(), pe_new.cuda(), [255])
+    orc.cache_append(oc, bits(kv_new), bits(pe_new), [255])
+    torch.cuda.synchronize()
+    assert np.array_equal(dc.kv.cpu().numpy(), oc["kv"])
+    assert np.array_equal(dc.kv_scale.cpu().numpy(), oc["kv_scale"])
+
+
+def test_workload2_v3_decode():
+    _run_dense_workload(inputs.WORKLOADS[2], 6)
+
+
+def test_workload3_serving_variable_lengths():
+    _run_dense_workload(inputs.WORKLOADS[3], 2)
+
+
+def test_workload4_long_context():
+    _run_dense_workload(inputs.WORKLOADS[4], 4)
+
+
+def test_workload5_sparse_with_fused_append():
+    w = inputs.WORKLOADS[5]
+    oc, dc = workload_cache(w)
+    ql, qp = inputs.queries(w)
+    ends = inputs.end_positions(w)
+    topk = inputs.topk_indices(w.B, w.topk, ends, 1000 * w.index + inputs.T_TOPK)
+    kv_new, pe_new = inputs.new_rows(w)
+    gidx = torch.empty((w.B, w.topk), dtype=torch.int32, device="cuda")
+    gcnt = torch.empty((w.B,), dtype=torch.int32, device="cuda")
+    out, lse = mla.decode_sparse(dc, ql.cuda(), qp.cuda(), ends.cuda(), w.S, w.softmax_scale,
+                                 topk.cuda(), kv_new=kv_new.cuda(), pe_new=pe_new.cuda(),
+                                 gidx=gidx, gcount=gcnt)
+    orc.cache_append(oc, bits(kv_new), bits(pe_new), ends.numpy() - 1)
+    ref_g, ref_c = orc.sparse_gather_lists(topk.numpy(), ends.numpy())
+    assert np.array_equal(gidx.cpu().numpy(), ref_g) and np.array_equal(gcnt.cpu().numpy(), ref_c)
+    pairs = sample_pairs(w.B, w.H, 3, w.index)
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), ends.numpy(), w.softmax_scale,
+                                       pairs=pairs, topk=topk.numpy())
+    o, l = f64(out), f64(lse)
+    check_close(np.stack([o[b, h] for b, h in pairs]), ref, "out")
+    check_close(np.array([l[b, h] for b, h in pairs]), ref_lse, "lse")
