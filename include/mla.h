@@ -177,6 +177,22 @@ MLA_API mla_status mla_decode_sparse(const mla_cache* cache, const void* q_laten
  */
 MLA_API mla_status mla_workspace_status(const void* workspace, uint32_t* flags, void* stream);
 
+/*
+ * Tracing (no counterpart on the pages; a measurement aid).  Between
+ * mla_trace_begin and mla_trace_end, on the calling host thread, every decode
+ * call records a CUDA event pair around its main decode kernel on the call's
+ * stream (up to max_records pairs; further calls are counted but not timed),
+ * and every kernel the library launches is counted.  Calls may be captured
+ * into a CUDA graph; the events then become graph nodes and are read after
+ * the graph ran.  mla_trace_end synchronises on the last event and returns
+ * the summed kernel time in milliseconds, the number of timed launches and
+ * the number of kernel launches.  Events are created by begin and destroyed
+ * by end.
+ */
+MLA_API mla_status mla_trace_begin(int32_t max_records);
+MLA_API mla_status mla_trace_end(float* main_kernel_ms, int32_t* timed_launches,
+                                 int32_t* kernel_launches);
+
 /* Human-readable name of a status code (static string). */
 MLA_API const char* mla_status_string(mla_status status);
 

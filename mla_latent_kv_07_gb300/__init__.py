@@ -69,6 +69,10 @@ def lib() -> ctypes.CDLL:
             L.mla_status_string.argtypes = [I32]
             L.mla_status_string.restype = ctypes.c_char_p
             L.mla_last_error.restype = ctypes.c_char_p
+            L.mla_trace_begin.argtypes = [I32]
+            L.mla_trace_begin.restype = I32
+            L.mla_trace_end.argtypes = [P, P, P]
+            L.mla_trace_end.restype = I32
             _lib = L
     return _lib
 
@@ -196,3 +200,17 @@ def workspace_status(workspace, stream=None) -> int:
     _check(lib().mla_workspace_status(_ptr(workspace), ctypes.byref(flags), _stream(stream)),
            "mla_workspace_status")
     return int(flags.value)
+
+
+def trace_begin(max_records: int) -> None:
+    """Start timing the main decode kernel of every call on this thread."""
+    _check(lib().mla_trace_begin(int(max_records)), "mla_trace_begin")
+
+
+def trace_end():
+    """Stop tracing; returns (summed main-kernel ms, timed launches, kernel launches)."""
+    ms = ctypes.c_float(0)
+    n = ctypes.c_int32(0)
+    k = ctypes.c_int32(0)
+    _check(lib().mla_trace_end(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(k)), "mla_trace_end")
+    return float(ms.value), int(n.value), int(k.value)

@@ -2,6 +2,7 @@
 // workspace carve-up and the launch sequence of each call.  Every check that
 // the host can make happens before the first launch.
 #include <mutex>
+#include <new>
 #include <stdio.h>
 #include <string.h>
 
@@ -15,6 +16,28 @@ thread_local char g_last_error[256] = "";
 mla_status cuda_fail(cudaError_t e, const char* where) {
   snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, cudaGetErrorString(e));
   return MLA_ERR_CUDA;
+}
+
+// Per-thread trace of the main decode kernel (see mla_trace_begin).
+struct Trace {
+  bool on = false;
+  int cap = 0, n = 0, launches = 0;
+  cudaEvent_t* ev = nullptr;  // [2 * cap]: start, stop pairs
+};
+thread_local Trace g_trace;
+
+void trace_launches(int k) {
+  if (g_trace.on) g_trace.launches += k;
+}
+
+bool trace_start(cudaStream_t s) {
+  if (!g_trace.on || g_trace.n >= g_trace.cap) return false;
+  return cudaEventRecord(g_trace.ev[2 * g_trace.n], s) == cudaSuccess;
+}
+
+void trace_stop(cudaStream_t s, bool started) {
+  if (!started) return;
+  if (cudaEventRecord(g_trace.ev[2 * g_trace.n + 1], s) == cudaSuccess) ++g_trace.n;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -110,10 +133,13 @@ mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cuda
   cudaError_t e = mla::launch_schedule(K ? nullptr : a.end_pos, a.max_end_pos, ws, a.B,
                                        mla::target_units(a.H, sms), mla::decode_mma_granule(), s);
   if (e != cudaSuccess) return cuda_fail(e, "schedule");
+  const bool traced = trace_start(s);
   e = mla::launch_decode_mma(make_params(a, ws, K), s);
+  trace_stop(s, traced);
   if (e != cudaSuccess) return cuda_fail(e, "decode");
   e = mla::launch_combine(ws, a.B, a.H, a.out, a.lse, s);
   if (e != cudaSuccess) return cuda_fail(e, "combine");
+  trace_launches(3);
   return MLA_OK;
 }
 
@@ -142,7 +168,9 @@ mla_status mla_cache_append(const mla_cache* cache, const void* kv_new, const vo
   p.B = B;
   memcpy(p.pos, start_pos, sizeof(int32_t) * (size_t)B);
   cudaError_t e = mla::launch_append_host_pos(p, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? MLA_OK : cuda_fail(e, "append");
+  if (e != cudaSuccess) return cuda_fail(e, "append");
+  trace_launches(1);
+  return MLA_OK;
 }
 
 size_t mla_workspace_size(int32_t B, int32_t H, int32_t max_end_pos, int32_t topk) {
@@ -204,9 +232,11 @@ mla_status mla_decode_sparse(const mla_cache* cache, const void* q_latent, const
     p.B = B;
     e = mla::launch_append_device_pos(p, s);
     if (e != cudaSuccess) return cuda_fail(e, "append");
+    trace_launches(1);
   }
   e = mla::launch_sparse_prep(topk_idx, K, end_pos, max_end_pos, ws, B, gidx_out, gcount_out, s);
   if (e != cudaSuccess) return cuda_fail(e, "sparse_prep");
+  trace_launches(1);
   return run_decode(a, ws, K, s);
 }
 
@@ -231,5 +261,47 @@ const char* mla_status_string(mla_status status) {
 }
 
 const char* mla_last_error(void) { return g_last_error; }
+
+mla_status mla_trace_begin(int32_t max_records) {
+  if (g_trace.on || max_records <= 0 || max_records > (1 << 20)) return MLA_ERR_INVALID_ARG;
+  Trace t;
+  t.cap = max_records;
+  t.ev = new (std::nothrow) cudaEvent_t[2 * (size_t)max_records];
+  if (!t.ev) return MLA_ERR_INVALID_ARG;
+  for (int i = 0; i < 2 * max_records; ++i) {
+    cudaError_t e = cudaEventCreate(&t.ev[i]);
+    if (e != cudaSuccess) {
+      for (int j = 0; j < i; ++j) cudaEventDestroy(t.ev[j]);
+      delete[] t.ev;
+      return cuda_fail(e, "trace_begin");
+    }
+  }
+  t.on = true;
+  g_trace = t;
+  return MLA_OK;
+}
+
+mla_status mla_trace_end(float* main_kernel_ms, int32_t* timed_launches, int32_t* kernel_launches) {
+  if (!g_trace.on) return MLA_ERR_INVALID_ARG;
+  Trace t = g_trace;
+  g_trace = Trace();
+  mla_status st = MLA_OK;
+  double total = 0.0;
+  if (t.n > 0) {
+    cudaError_t e = cudaEventSynchronize(t.ev[2 * t.n - 1]);
+    for (int i = 0; e == cudaSuccess && i < t.n; ++i) {
+      float ms = 0.f;
+      e = cudaEventElapsedTime(&ms, t.ev[2 * i], t.ev[2 * i + 1]);
+      total += ms;
+    }
+    if (e != cudaSuccess) st = cuda_fail(e, "trace_end");
+  }
+  for (int i = 0; i < 2 * t.cap; ++i) cudaEventDestroy(t.ev[i]);
+  delete[] t.ev;
+  if (main_kernel_ms) *main_kernel_ms = (float)total;
+  if (timed_launches) *timed_launches = t.n;
+  if (kernel_launches) *kernel_launches = t.launches;
+  return st;
+}
 
 }  // extern "C"
