@@ -1,0 +1,461 @@
+"""Benchmark of the MLA latent-cache decode step on GB300.
+
+One step = the cache-write of this step's new row (row end_pos-1 of every
+sequence) followed by the absorbed decode over positions 0..end_pos-1 -- or,
+for the sparse workload, the fused append + top-k gather decode.  Inputs are
+seeded synthetic tensors of the workload's shapes, resident in HBM before the
+timed region.  The timed region is one CUDA-graph launch holding exactly K
+steps; successive steps rotate over cache copies (or top-k lists) so that each
+step's working set is not served from L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
+    python bench.py --impl reference ...     # the CPU oracle, same metric
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own
+replica on its own GPU (independent sequences, no data-path collective);
+the timing is bracketed by barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import mla_latent_kv_07_gb300 as mla  # noqa: E402
+from mla_latent_kv_07_gb300 import inputs, layout  # noqa: E402
+
+DEFAULT_WORKLOAD = 2
+METRIC = "MLA decode: cache HBM TB/s (algorithmic cache bytes / step time)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in ("decode_mma.cu", "common.cuh"):
+        with open(os.path.join(ROOT, "mla_latent_kv_07_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "decode_kernel_traffic.txt")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    src = re.search(r"^kernel_source_sha256_16:\s*(\S+)", text, re.M)
+    if not src or src.group(1) != kernel_source_hash():
+        return None
+    m = re.search(rf"^{re.escape(workload)}:\s*([0-9.eE+]+)", text, re.M)
+    return float(m.group(1)) if m else None
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 20 ms."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu=timestamp,{self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def mark(self, start: bool):
+        if start:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for ln in out.strip().splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 10:   # timestamp + the 9 queried fields
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10], parts[5]))
+            except (ValueError, IndexError):
+                continue
+        window = [r for r in rows if self.t0 - 0.05 <= r[0] <= self.t1 + 0.05]
+        where = "timed region"
+        if not window:
+            window, where = rows, "around the timed region (region shorter than the sampling period)"
+        if not window:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in window for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in window), "sm_max_mhz": max(r[2] for r in window),
+                "reasons": reasons, "samples": len(window), "window": where}
+
+
+# ------------------------------------------------------------ workload set-up
+
+class Setup:
+    """Device-resident inputs of one workload, with rotation for L2."""
+
+    def __init__(self, w: inputs.Workload, device, seed_offset: int = 0):
+        self.w = w
+        self.device = device
+        g = lambda shape, tid: inputs.randn_bf16(shape, 1000 * w.index + tid + seed_offset, device)
+        self.ends = inputs.end_positions(w).to(device)
+        self.ends_host = self.ends.cpu().tolist()
+        self.tokens = sum(min(t, w.topk) if w.topk else t for t in self.ends_host)
+        self.ql, self.qp = g((w.B, w.H, 512), inputs.T_QL), g((w.B, w.H, 64), inputs.T_QP)
+        self.kv_new, self.pe_new = g((w.B, 512), inputs.T_KVNEW), g((w.B, 64), inputs.T_PENEW)
+        step_bytes = layout.step_bytes(self.tokens, w.B, w.H, w.fmt)
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.rot = max(1, math.ceil(2 * l2 / step_bytes))
+        base = self._make_cache(g)
+        if w.topk:
+            # rotate the top-k lists (different gathered rows each step), one cache
+            self.caches = [base]
+            self.topks = [inputs.topk_indices(w.B, w.topk, self.ends_host,
+                                              1000 * w.index + inputs.T_TOPK + 17 * r).to(device)
+                          for r in range(self.rot)]
+            self.rotation = f"{self.rot} top-k lists ({self.rot * step_bytes / 1e6:.0f} MB gathered)"
+        else:
+            self.caches = [base] + [self._clone(base) for _ in range(self.rot - 1)]
+            self.topks = None
+            self.rotation = f"{self.rot} cache copies ({self.rot * step_bytes / 1e6:.0f} MB read)"
+        self.l2_bytes = l2
+        self.out = torch.empty((w.B, w.H, 512), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty((w.B, w.H), dtype=torch.float32, device=device)
+        self.ws = mla.alloc_workspace(w.B, w.H, w.S, w.topk, device)
+        self.start_pos = [t - 1 for t in self.ends_host]
+
+    def _make_cache(self, g):
+        w = self.w
+        kv = g((w.B, w.S, 512), inputs.T_KV)
+        pe = g((w.B, w.S, 64), inputs.T_PE)
+        if w.fmt == 0:
+            return mla.Cache(w.B, w.S, 0, kv=kv, pe=pe, device=self.device)
+        cache = mla.Cache(w.B, w.S, 1, pe=pe, device=self.device)
+        # quantise every row with the library's cache-write kernel: view the
+        # [B, S] rows as B*S one-row slots and append them in chunks
+        flat = mla.Cache(w.B * w.S, 1, 1, kv=cache.kv.view(w.B * w.S, 1, 512),
+                         kv_scale=cache.kv_scale.view(w.B * w.S, 1, 4),
+                         pe=cache.pe.view(w.B * w.S, 1, 64))
+        rows = kv.view(w.B * w.S, 512)
+        pe_rows = pe.view(w.B * w.S, 64)
+        zeros = [0] * 2048
+        for r0 in range(0, w.B * w.S, 2048):
+            n = min(2048, w.B * w.S - r0)
+            sub = mla.Cache(n, 1, 1, kv=flat.kv[r0:r0 + n], kv_scale=flat.kv_scale[r0:r0 + n],
+                            pe=flat.pe[r0:r0 + n])
+            mla.cache_append(sub, rows[r0:r0 + n], pe_rows[r0:r0 + n], zeros[:n])
+        torch.cuda.synchronize()
+        del kv
+        return cache
+
+    def _clone(self, c):
+        return mla.Cache(c.max_batch, c.max_seq_len, c.fmt, kv=c.kv.clone(),
+                         kv_scale=None if c.kv_scale is None else c.kv_scale.clone(), pe=c.pe.clone())
+
+    def step(self, i: int):
+        w = self.w
+        if w.topk:
+            mla.decode_sparse(self.caches[0], self.ql, self.qp, self.ends, w.S, w.softmax_scale,
+                              self.topks[i % self.rot], kv_new=self.kv_new, pe_new=self.pe_new,
+                              out=self.out, lse=self.lse, workspace=self.ws)
+        else:
+            c = self.caches[i % self.rot]
+            mla.cache_append(c, self.kv_new, self.pe_new, self.start_pos)
+            mla.decode(c, self.ql, self.qp, self.ends, w.S, w.softmax_scale, out=self.out,
+                       lse=self.lse, workspace=self.ws)
+
+
+# --------------------------------------------------------------- GPU arm
+
+def run_gpu(args, rank, world, local_rank):
+    import torch.distributed as dist
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    mla.lib()
+    w = inputs.WORKLOADS[args.workload]
+    st = Setup(w, device, seed_offset=0)
+    K, W = args.steps, args.warmup
+    for i in range(W):
+        st.step(i)
+    torch.cuda.synchronize()
+
+    # capture exactly K steps, each with its decode kernel bracketed by events
+    stream = torch.cuda.Stream(device)
+    graph = torch.cuda.CUDAGraph()
+    mla.trace_begin(K)
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(K):
+            st.step(W + i)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    if sampler:
+        sampler.mark(True)
+    t_wall = time.perf_counter()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if sampler:
+        sampler.mark(False)
+    if world > 1:
+        dist.barrier()
+    ms = e0.elapsed_time(e1)
+    kern_ms, timed, launches = mla.trace_end()
+    clocks = sampler.stop() if sampler else None
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    step_s = ms / 1e3 / K
+    cache_bytes = st.tokens * layout.cache_bytes_per_token(w.fmt)
+    value = world * cache_bytes / step_s / 1e12
+    tokens_per_s = world * w.B / step_s
+
+    # dominant kernel: the decode kernel, timed by its own events
+    kern_s = kern_ms / 1e3 / max(timed, 1)
+    pk, pk_src = peaks()
+    flops = layout.step_flops(st.tokens, w.H)
+    t_hbm = cache_bytes / (pk["hbm_gbs"] * 1e9)
+    t_tc = flops / (pk["bf16_tflops"] * 1e12)
+    if t_hbm >= t_tc:
+        achieved, peak, unit, bound = cache_bytes / kern_s / 1e9, pk["hbm_gbs"], "GB/s", "hbm"
+    else:
+        achieved, peak, unit, bound = flops / kern_s / 1e12, pk["bf16_tflops"], "TFLOP/s", "tensor"
+    roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
+                "peak_source": f"of {pk_src}", "kernel": "decode_mma_kernel",
+                "kernel_us": round(kern_s * 1e6, 3),
+                "hbm_frac_of_step": round(cache_bytes / step_s / 1e9 / pk["hbm_gbs"], 4),
+                "roofline_time_us": round(max(t_hbm, t_tc) * 1e6, 3)}
+
+    e2e = run_e2e(st, K, W) if not args.no_e2e else None
+    cpu = run_cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu) else None
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": "TB/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(ms / K, 6), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.fmt == 0 else "fp8-e4m3 cache, bf16 MMA",
+        "data": "synthetic (seeded N(0,1) bf16; FP8 cache quantised by the library's append)",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "end_pos": w.T or f"U[{w.T_lo},{w.T_hi}]",
+                   "attended_positions": st.tokens, "cache": "bf16" if w.fmt == 0 else "fp8-e4m3/128",
+                   "topk": w.topk or None, "step": "append new row + decode" if not w.topk
+                   else "fused append + top-k gather decode",
+                   "l2": f"inputs larger than L2: rotating {st.rotation}; L2 {st.l2_bytes / 1e6:.0f} MB",
+                   "timing": "CUDA graph of exactly K steps, CUDA events on its stream",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tokens_per_s": round(tokens_per_s, 1),
+        "wall_ms_per_step": round(t_wall * 1e3 / K, 6),
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(st: Setup, K: int, W: int):
+    """Public API per step with host buffers: H2D of the step's inputs from
+    pinned memory, the calls, D2H of the outputs, all inside the timing."""
+    w = st.w
+    host_in = {"ql": st.ql.cpu().pin_memory(), "qp": st.qp.cpu().pin_memory(),
+               "ends": st.ends.cpu().pin_memory(), "kv_new": st.kv_new.cpu().pin_memory(),
+               "pe_new": st.pe_new.cpu().pin_memory()}
+    if w.topk:
+        host_in["topk"] = st.topks[0].cpu().pin_memory()
+    dev = {k: torch.empty_like(v, device=st.device) for k, v in host_in.items()}
+    out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    lse_h = torch.empty(st.lse.shape, dtype=st.lse.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    n = min(K, 2000)
+
+    def one(i):
+        for k, v in host_in.items():
+            dev[k].copy_(v, non_blocking=True)
+        if w.topk:
+            mla.decode_sparse(st.caches[0], dev["ql"], dev["qp"], dev["ends"], w.S, w.softmax_scale,
+                              dev["topk"], kv_new=dev["kv_new"], pe_new=dev["pe_new"], out=st.out,
+                              lse=st.lse, workspace=st.ws)
+        else:
+            c = st.caches[i % st.rot]
+            mla.cache_append(c, dev["kv_new"], dev["pe_new"], st.start_pos)
+            mla.decode(c, dev["ql"], dev["qp"], dev["ends"], w.S, w.softmax_scale, out=st.out,
+                       lse=st.lse, workspace=st.ws)
+        out_h.copy_(st.out, non_blocking=True)
+        lse_h.copy_(st.lse, non_blocking=True)
+
+    for i in range(min(W, 10)):
+        one(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(n):
+        one(i)
+    e1.record()
+    torch.cuda.synchronize()
+    step_s = e0.elapsed_time(e1) / 1e3 / n
+    cache_bytes = st.tokens * layout.cache_bytes_per_token(w.fmt)
+    return {"value": round(cache_bytes / step_s / 1e12, 4), "unit": "TB/s", "steps": n,
+            "ms_per_step": round(step_s * 1e3, 6), "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "path": "python binding -> C ABI, pinned host buffers, per-step H2D inputs and D2H outputs"}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def oracle_sample(w: inputs.Workload, budget_s: float):
+    """Bounded sample of the workload for the CPU oracle: whole sequences (all
+    heads), drawn with the same recipe on the CPU, until the time budget."""
+    from oracle import oracle as orc
+    ends = inputs.end_positions(w)
+    S = int(ends.max())
+    kv = inputs.randn_bf16((1, S, 512), 1000 * w.index + inputs.T_KV)
+    pe = inputs.randn_bf16((1, S, 64), 1000 * w.index + inputs.T_PE)
+    cache = {"fmt": w.fmt, "pe": inputs.bf16_bits(pe)}
+    if w.fmt == 0:
+        cache["kv"] = inputs.bf16_bits(kv)
+    else:
+        cache["kv"], cache["kv_scale"] = orc.quantize_rows(inputs.bf16_bits(kv))
+    ql = inputs.randn_bf16((1, w.H, 512), 1000 * w.index + inputs.T_QL)
+    qp = inputs.randn_bf16((1, w.H, 64), 1000 * w.index + inputs.T_QP)
+    topk = None
+    if w.topk:
+        topk = inputs.topk_indices(1, w.topk, [int(ends[0])], 1000 * w.index + inputs.T_TOPK).numpy()
+    T = int(ends[0])
+    tokens = min(T, w.topk) if w.topk else T
+    return orc, cache, inputs.bf16_bits(ql), inputs.bf16_bits(qp), T, topk, tokens
+
+
+def time_oracle_step(sample, w):
+    orc, cache, ql, qp, T, topk, tokens = sample
+    t0 = time.perf_counter()
+    orc.decode_absorbed(cache, ql, qp, [T], w.softmax_scale, topk=topk)
+    return time.perf_counter() - t0, tokens
+
+
+def run_cpu_baseline(w):
+    from oracle import oracle as orc
+    sample = oracle_sample(w, 10.0)
+    dt, tokens = time_oracle_step(sample, w)
+    bytes_ = tokens * layout.cache_bytes_per_token(w.fmt)
+    return {"value": round(bytes_ / dt / 1e12, 8), "unit": "TB/s", "cores": orc.num_threads(),
+            "kind": "oracle", "seconds": round(dt, 3),
+            "sample": f"one sequence of the workload (end_pos {sample[4]}, all {w.H} heads, "
+                      f"{tokens} attended positions), fp64 oracle, OpenMP over heads"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    from oracle import oracle as orc
+    w = inputs.WORKLOADS[args.workload]
+    sample = oracle_sample(w, 10.0)
+    for _ in range(min(args.warmup, 1)):
+        time_oracle_step(sample, w)
+    K = args.steps if args.steps <= 5 else 5
+    t0 = time.perf_counter()
+    for _ in range(K):
+        _, tokens = time_oracle_step(sample, w)
+    dt = (time.perf_counter() - t0) / K
+    value = tokens * layout.cache_bytes_per_token(w.fmt) / dt / 1e12
+    desc = (f"one sequence of {w.name} per step (end_pos {sample[4]}, all {w.H} heads, "
+            f"{tokens} attended positions)")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 8), "unit": "TB/s",
+        "n_gpus": world, "steps": K, "warmup": min(args.warmup, 1), "ms_per_step": round(dt * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": w.name, "sample": desc},
+        "cpu_baseline": {"value": round(value, 8), "unit": "TB/s", "cores": orc.num_threads(),
+                         "kind": "oracle", "sample": desc},
+        "e2e": {"value": round(value, 8), "unit": "TB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", type=int, default=DEFAULT_WORKLOAD, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_gpu(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

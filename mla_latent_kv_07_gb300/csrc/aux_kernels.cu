@@ -266,11 +266,8 @@ cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int m
   int Kpad = 2;
   while (Kpad < K) Kpad <<= 1;
   size_t smem = sizeof(int) * (size_t)Kpad;
-  if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(sparse_prep_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-  }
+  cudaError_t e = ensure_smem(sparse_prep_kernel, sizeof(int) * (size_t)mla::kMaxTopK);
+  if (e != cudaSuccess) return e;
   sparse_prep_kernel<<<B, 1024, smem, s>>>(topk, K, Kpad, end_pos, max_end_pos, ws, gidx_out,
                                            gcount_out);
   return cudaGetLastError();

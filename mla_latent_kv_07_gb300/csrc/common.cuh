@@ -107,6 +107,19 @@ struct DecodeParams {
   int K;                  // sparse list length (0 = dense)
 };
 
+// Raise a kernel's dynamic shared memory limit once per device.
+template <typename Kernel>
+cudaError_t ensure_smem(Kernel k, size_t bytes) {
+  static int done[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
+  return e;
+}
+
 // Launchers (defined in the kernel translation units).
 cudaError_t launch_append_host_pos(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_append_device_pos(const AppendParams& p, cudaStream_t s);

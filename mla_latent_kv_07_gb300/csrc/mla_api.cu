@@ -32,12 +32,16 @@ void trace_launches(int k) {
 
 bool trace_start(cudaStream_t s) {
   if (!g_trace.on || g_trace.n >= g_trace.cap) return false;
-  return cudaEventRecord(g_trace.ev[2 * g_trace.n], s) == cudaSuccess;
+  // External records become real event nodes when the stream is being captured
+  // into a graph (a plain record would only mark a dependency); outside
+  // capture they behave as ordinary records.
+  return cudaEventRecordWithFlags(g_trace.ev[2 * g_trace.n], s, cudaEventRecordExternal) == cudaSuccess;
 }
 
 void trace_stop(cudaStream_t s, bool started) {
   if (!started) return;
-  if (cudaEventRecord(g_trace.ev[2 * g_trace.n + 1], s) == cudaSuccess) ++g_trace.n;
+  if (cudaEventRecordWithFlags(g_trace.ev[2 * g_trace.n + 1], s, cudaEventRecordExternal) == cudaSuccess)
+    ++g_trace.n;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
