@@ -189,12 +189,28 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
   }
   atomicAdd(&total_len, mine);
   __syncthreads();
+  // smallest granule multiple with sum_b ceil(len_b / chunk) <= target, so
+  // the units fit the launch (and, on the pair path, one wave of the GPU)
   long long chunk = ((long long)total_len + target - 1) / target;
   chunk = ((chunk + granule - 1) / granule) * granule;
   if (chunk < granule) chunk = granule;
+  __shared__ int count_smem;
   int nmine = 0;
-  for (int b = b0; b < b0 + per && b < B; ++b)
-    nmine += (int)((ws.lengths[b] + chunk - 1) / chunk);
+  for (int iter = 0; iter < 64; ++iter) {
+    nmine = 0;
+    for (int b = b0; b < b0 + per && b < B; ++b)
+      nmine += (int)((ws.lengths[b] + chunk - 1) / chunk);
+    if (threadIdx.x == 0) count_smem = 0;
+    __syncthreads();
+    atomicAdd(&count_smem, nmine);
+    __syncthreads();
+    const int n = count_smem;
+    __syncthreads();
+    if (n <= target) break;
+    long long grown = (chunk * n + target - 1) / target;
+    grown = ((grown + granule - 1) / granule) * granule;
+    chunk = grown > chunk + granule ? grown : chunk + granule;
+  }
   int total_units;
   int u = block_exclusive_scan(nmine, scan_smem, &total_units);
   for (int b = b0; b < b0 + per && b < B; ++b) {
@@ -266,7 +282,7 @@ cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int m
   int Kpad = 2;
   while (Kpad < K) Kpad <<= 1;
   size_t smem = sizeof(int) * (size_t)Kpad;
-  cudaError_t e = ensure_smem(sparse_prep_kernel, sizeof(int) * (size_t)mla::kMaxTopK);
+  cudaError_t e = ensure_smem<sparse_prep_kernel>(sizeof(int) * (size_t)mla::kMaxTopK);
   if (e != cudaSuccess) return e;
   sparse_prep_kernel<<<B, 1024, smem, s>>>(topk, K, Kpad, end_pos, max_end_pos, ws, gidx_out,
                                            gcount_out);

@@ -43,12 +43,16 @@ struct Workspace {
 
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Units the scheduler aims for: enough CTAs to fill every SM about twice.
+// Units the scheduler aims for.  mma.sync path: H/16 CTAs per unit, about
+// two per SM.  Tensor-memory path: one CTA pair per unit, one wave.
+inline int target_units_mma(int H, int num_sms) {
+  int per_unit = H / 16;
+  return (2 * num_sms + per_unit - 1) / per_unit;
+}
+inline int target_units_tc(int num_sms) { return num_sms / 2; }
 inline int target_units(int H, int num_sms) {
-  int per_unit = H / 16;                 // head-group CTAs per unit (mma.sync path)
-  int t1 = (2 * num_sms + per_unit - 1) / per_unit;
-  int t2 = num_sms / 2;                  // cluster-pair path: one pair per unit
-  return t1 > t2 ? t1 : t2;
+  int a = target_units_mma(H, num_sms), b = target_units_tc(num_sms);
+  return a > b ? a : b;
 }
 
 inline Workspace carve_workspace(void* base, int B, int H, int K, int num_sms) {
@@ -107,15 +111,17 @@ struct DecodeParams {
   int K;                  // sparse list length (0 = dense)
 };
 
-// Raise a kernel's dynamic shared memory limit once per device.
-template <typename Kernel>
-cudaError_t ensure_smem(Kernel k, size_t bytes) {
+// Raise a kernel's dynamic shared memory limit once per device.  The kernel
+// is a template argument, so every kernel (and every instantiation of a
+// kernel template) has its own flags.
+template <auto kKernel>
+cudaError_t ensure_smem(size_t bytes) {
   static int done[64] = {0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  e = cudaFuncSetAttribute(kKernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
   if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev] = 1;
   return e;
 }
@@ -132,6 +138,10 @@ cudaError_t launch_schedule(const int* end_pos, int max_end_pos, const Workspace
                             int target_units, int granule, cudaStream_t s);
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s);
 int decode_mma_granule();
+// tensor-memory path (H = 128): one CTA pair per unit
+cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s);
+int decode_tc_granule();
+bool decode_tc_supported(int H);
 cudaError_t launch_combine(const Workspace& ws, int B, int H, void* out, float* lse,
                            cudaStream_t s);
 

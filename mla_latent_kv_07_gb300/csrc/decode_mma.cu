@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const DecodeParams
 template <int kFmt, bool kSparse>
 cudaError_t launch_variant(const DecodeParams& p, cudaStream_t s) {
   const size_t smem = sizeof(Smem);
-  cudaError_t e = ensure_smem(decode_mma_kernel<kFmt, kSparse>, smem);
+  cudaError_t e = ensure_smem<decode_mma_kernel<kFmt, kSparse>>(smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.ws.max_units, p.H / kHeads);
   decode_mma_kernel<kFmt, kSparse><<<grid, kThreads, smem, s>>>(p);

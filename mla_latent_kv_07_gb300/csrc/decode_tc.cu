@@ -1,0 +1,688 @@
+// decode_tc.cu -- absorbed MLA decode for H = 128 heads on the 5th-generation
+// tensor cores (tcgen05 + TMEM), TMA-staged, one CTA pair (cluster of 2) per
+// unit of positions.
+//
+// What is computed ("DeepSeek-V3.2-Exp . KV cache", MQA-decode excerpt;
+// "DeepSeek MLA architecture ...", sections 3-4), per unit of positions:
+//   S[h, t] = q_latent[h] . c[t] + q_pe[h] . kR[t]            (128 heads)
+//   online softmax of S * softmax_scale over the unit's positions
+//   O[h, :] = sum_t p[h, t] c[t, :]                           (512 latent)
+// followed by the log-sum-exp combine across units (combine kernel).
+//
+// Why a pair: an fp32 accumulator for 128 heads x 512 latent columns fills all
+// of one SM's tensor memory (512 columns x 128 lanes x 4 B), leaving no room
+// for the scores.  So CTA r of the pair owns latent columns [256r, 256r+256)
+// and rotary columns [32r, 32r+32):
+//   * QK: each CTA contracts its 288-wide half (Q half as the A operand held in
+//     tensor memory, K half from shared memory) into a partial S; the two
+//     partials are exchanged through distributed shared memory and summed.
+//     fp32 addition commutes, so both CTAs hold bit-identical S and take the
+//     same softmax decisions.
+//   * PV: each CTA multiplies P (shared memory) by its latent half V (the same
+//     shared-memory tile, read as an MN-major operand) into its own O half.
+// Every cache byte is fetched by exactly one CTA and there is no redundant
+// tensor-core work.
+//
+// Tensor memory (512 columns): O half [0,256) fp32; Q half [256,400) bf16 (2
+// per column); S double buffer [400,448) and [448,496) fp32.
+//
+// Warp roles (256 threads; 384 when a converter is needed):
+//   warp 0  producer: TMA tiles (dense) or per-row bulk copies (gather)
+//   warp 1  MMA issuer (one thread) and tensor-memory owner
+//   warps 4-7  softmax: thread h <-> head h <-> TMEM lane h; partial-score
+//              exchange, online softmax (lazy rescale), P, epilogue
+//   warps 8-11 converter (FP8 caches and gathers): raw rows -> bf16 operand
+//              tile bf16(fp32(e4m3 * scale)) in the 128-byte swizzled layout
+//
+// Every wait is bounded; on expiry the kernel raises a status bit, stops
+// issuing work, and still runs its teardown (cluster barrier, TMEM release).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include <mutex>
+#include <string.h>
+
+#include "common.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kN = 48;                     // positions per tile (MMA N for QK, K for PV)
+constexpr int kHalf = kDc / 2;             // 256 latent columns per CTA
+constexpr int kPeHalf = kDr / 2;           // 32 rotary columns per CTA
+constexpr int kBlkBytes = kN * 128;        // one 64-column swizzled block of a tile: 6 KB
+constexpr int kOplBytes = 4 * kBlkBytes;   // latent half operand: 24 KB
+constexpr int kOpeBytes = kBlkBytes;       // rotary operand (full 64 columns): 6 KB
+constexpr int kPBytes = 128 * 128;         // P: 128 heads x 64 (48 used) bf16, swizzled
+constexpr int kXStride = kN + 4;           // exchange row stride (floats), bank spread
+constexpr int kXBytes = 128 * kXStride * 4;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
+constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemS0 = 400, kTmemS1 = 448;
+constexpr long kSpinLimit = 1L << 22;
+
+template <int kFmt, bool kSparse>
+struct Cfg {
+  static constexpr bool kConv = kFmt == 1 || kSparse;       // converter warps present
+  static constexpr int kThreads = kConv ? 384 : 256;
+  static constexpr int kRawRow = kFmt == 1 ? kHalf : kHalf * 2;  // bytes of a raw latent half row
+  static constexpr int kRawBytes = kConv ? kN * kRawRow : 0;
+  static constexpr int kScBytes = kFmt == 1 ? 1024 : 0;          // 48 x 16 B, padded
+  static constexpr int kRpeBytes = kSparse ? kN * 128 : 0;
+  static constexpr int kStage = kOplBytes + kOpeBytes + kRawBytes + kScBytes + kRpeBytes;
+  static constexpr int kStages = kSparse ? 2 : (kFmt == 1 ? 3 : 4);
+  static constexpr int kStagesBytes = kStages * kStage;
+  static constexpr int kPOff = kStagesBytes;
+  static constexpr int kXOff = kPOff + 2 * kPBytes;
+  static constexpr int kBarOff = kXOff + 2 * kXBytes;
+  static constexpr int kSmem = kBarOff + 1024 + 1024;      // barriers/flags + base alignment slack
+  static_assert(kSmem <= 232448, "shared memory budget");
+  static_assert(kStage % 1024 == 0 && kOplBytes % 1024 == 0, "1 KB alignment of swizzled tiles");
+};
+
+struct TcParams {
+  DecodeParams p;
+  CUtensorMap m_kv;   // bf16: latent (box 64 x 48), FP8: codes (box 256 x 48)
+  CUtensorMap m_pe;   // rotary (box 64 x 48, 128-byte swizzle)
+  CUtensorMap m_sc;   // FP8 scales (box 4 x 48)
+};
+
+// ------------------------------------------------------------------ PTX
+__device__ __forceinline__ uint32_t sa(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void bar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(b)), "r"(count));
+}
+__device__ __forceinline__ void bar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(sa(b)) : "memory");
+}
+__device__ __forceinline__ void bar_arrive_remote(uint32_t remote_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_addr)
+               : "memory");
+}
+__device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa(b)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
+      "selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(sa(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint32_t mapa(const void* p, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(sa(p)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned; barrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// smem matrix descriptor: 128-byte swizzle, version 1
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
+}
+// instruction descriptor, kind::f16: bf16 x bf16 -> fp32
+__host__ __device__ constexpr uint32_t idesc(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_ss(uint32_t d, uint64_t a, uint64_t b, uint32_t id, int acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d),
+      "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint32_t id, int acc) {
+  asm volatile(
+      "{ .reg .pred p; setp.ne.b32 p, %4, 0; "
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d),
+      "r"(a), "l"(b), "r"(id), "r"(acc));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* b) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   sa(b))
+               : "memory");
+}
+#define TC_LD16(taddr, r)                                                                       \
+  asm volatile(                                                                                 \
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13," \
+      "%14,%15}, [%16];"                                                                        \
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),     \
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), \
+        "=r"(r[14]), "=r"(r[15])                                                                \
+      : "r"(taddr))
+#define TC_ST16(taddr, r)                                                                     \
+  asm volatile(                                                                               \
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12," \
+      "%13,%14,%15,%16};" ::"r"(taddr),                                                       \
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), \
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),       \
+      "r"(r[15])                                                                              \
+      : "memory")
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+__device__ __forceinline__ void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma3(void* dst, const CUtensorMap* m, int c0, int c1, int c2,
+                                     uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4}], [%5];" ::"r"(sa(dst)),
+      "l"(m), "r"(c0), "r"(c1), "r"(c2), "r"(sa(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          sa(dst)),
+      "l"(src), "r"(bytes), "r"(sa(bar))
+      : "memory");
+}
+
+// byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled block
+__device__ __forceinline__ uint32_t swz_chunk(int row, int chunk) {
+  return (row >> 3) * 1024 + (row & 7) * 128 + (((chunk ^ row) & 7) << 4);
+}
+
+// Shared state of the CTA (barriers, flags) at the tail of shared memory.
+struct Bars {
+  uint64_t full[4], deq[4], empty[4];
+  uint64_t sfull[2], sfree[2], pfull[2], pfree[2], xfull[2], xempty[2];
+  uint64_t drain;   // final commit of the MMA issuer
+  uint32_t tmem;
+  volatile int abort;
+};
+
+struct Waiter {
+  Bars* bars;
+  uint32_t* status;
+  __device__ __forceinline__ bool wait(uint64_t* b, uint32_t parity) {
+    for (long it = 0; it < kSpinLimit; ++it) {
+      if (bar_try(b, parity)) return true;
+      if (bars->abort) return false;
+    }
+    bars->abort = 1;
+    atomicOr(status, kDevTimeout);
+    return false;
+  }
+  // teardown variant: ignores the abort flag (the awaited operation was
+  // issued by this thread and completes on its own), still bounded
+  __device__ __forceinline__ void drain(uint64_t* b, uint32_t parity) {
+    for (long it = 0; it < kSpinLimit; ++it)
+      if (bar_try(b, parity)) return;
+    atomicOr(status, kDevTimeout);
+  }
+};
+
+// FP8 codes (16) x scale -> 16 bf16 values bf16(fp32(e4m3) * scale)
+__device__ __forceinline__ void dequant16(uint4 v, float sc, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((w[i >> 1] >> ((i & 1) * 16)) & 0xffffu);
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+    const __nv_bfloat162 bb = __floats2bfloat162_rn(__fmul_rn(f.x, sc), __fmul_rn(f.y, sc));
+    o[i] = *reinterpret_cast<const uint32_t*>(&bb);
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+template <int kFmt, bool kSparse>
+__global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ TcParams tp) {
+  using C = Cfg<kFmt, kSparse>;
+  const DecodeParams& p = tp.p;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Bars* bars = reinterpret_cast<Bars*>(sm + C::kBarOff);
+
+  const int unit_id = blockIdx.x >> 1;
+  const Unit u = p.ws.units[unit_id];
+  if (u.b < 0) return;  // both CTAs of the cluster read the same unit
+  uint32_t rank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const uint32_t peer = rank ^ 1u;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ntiles = (u.t1 - u.t0 + kN - 1) / kN;
+  Waiter wt{bars, p.ws.status};
+
+  auto stage_base = [&](int j) { return sm + j * C::kStage; };
+  auto opl = [&](int j) { return stage_base(j); };
+  auto ope = [&](int j) { return stage_base(j) + kOplBytes; };
+  auto raw = [&](int j) { return stage_base(j) + kOplBytes + kOpeBytes; };
+  auto rsc = [&](int j) { return stage_base(j) + kOplBytes + kOpeBytes + C::kRawBytes; };
+  auto rpe = [&](int j) { return stage_base(j) + kOplBytes + kOpeBytes + C::kRawBytes + C::kScBytes; };
+  auto pbuf = [&](int b) { return sm + C::kPOff + b * kPBytes; };
+  auto xbuf = [&](int b) { return reinterpret_cast<float*>(sm + C::kXOff + b * kXBytes); };
+
+  // ---------------------------------------------------------------- set-up
+  if (threadIdx.x == 0) {
+    for (int j = 0; j < C::kStages; ++j) {
+      bar_init(&bars->full[j], 1);
+      bar_init(&bars->deq[j], 128);
+      bar_init(&bars->empty[j], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      bar_init(&bars->sfull[b], 1);
+      bar_init(&bars->sfree[b], 128);
+      bar_init(&bars->pfull[b], 128);
+      bar_init(&bars->pfree[b], 1);
+      bar_init(&bars->xfull[b], 128);
+      bar_init(&bars->xempty[b], 128);
+    }
+    bar_init(&bars->drain, 1);
+    bars->abort = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+        sa(&bars->tmem)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_before();
+  __syncthreads();
+  tc_after();
+  const uint32_t tmem = bars->tmem;
+  cluster_sync();  // the peer's barriers are initialised before any remote arrive
+
+  // Q half -> tensor memory (A operand of QK): lane h, 2 bf16 per column
+  if (warp >= 4 && warp < 8) {
+    const int h = threadIdx.x - 128;
+    const size_t qrow = (size_t)u.b * p.H + h;
+    const uint4* ql = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q_latent) +
+                                                     qrow * kDc + rank * kHalf);
+    const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q_pe) +
+                                                     qrow * kDr + rank * kPeHalf);
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+#pragma unroll
+    for (int c = 0; c < 9; ++c) {  // 144 columns = 9 x 16
+      uint32_t r[16];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint4 v = c < 8 ? ql[c * 4 + k] : qp[k];
+        r[4 * k] = v.x; r[4 * k + 1] = v.y; r[4 * k + 2] = v.z; r[4 * k + 3] = v.w;
+      }
+      TC_ST16(lane_base + kTmemQ + 16 * c, r);
+    }
+    tc_wait_st();
+  }
+  tc_before();
+  __syncthreads();
+  tc_after();
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    int issued = 0;
+    for (int i = 0; i < ntiles && !bars->abort; ++i) {
+      const int j = i % C::kStages;
+      const uint32_t use = i / C::kStages;
+      if (!wt.wait(&bars->empty[j], (use & 1) ^ 1)) break;
+      const int e0 = u.t0 + i * kN;
+      if (!kSparse) {
+        if (lane == 0) {
+          if (kFmt == 0) {
+            bar_expect_tx(&bars->full[j], kOplBytes + kOpeBytes);
+            for (int blk = 0; blk < 4; ++blk)
+              tma3(opl(j) + blk * kBlkBytes, &tp.m_kv, rank * kHalf + blk * 64, e0, u.b, &bars->full[j]);
+          } else {
+            bar_expect_tx(&bars->full[j], kN * kHalf + kN * 16 + kOpeBytes);
+            tma3(raw(j), &tp.m_kv, rank * kHalf, e0, u.b, &bars->full[j]);
+            tma3(rsc(j), &tp.m_sc, 0, e0, u.b, &bars->full[j]);
+          }
+          tma3(ope(j), &tp.m_pe, 0, e0, u.b, &bars->full[j]);
+        }
+      } else {
+        const int v = min(kN, u.t1 - e0);
+        const uint32_t row_bytes = C::kRawRow + (kFmt == 1 ? 16 : 0) + 128;
+        if (lane == 0) bar_expect_tx(&bars->full[j], (uint32_t)v * row_bytes);
+        __syncwarp();
+        for (int c = lane; c < v; c += 32) {
+          const int pos = p.ws.gidx[(size_t)u.b * p.K + e0 + c];
+          const size_t row = (size_t)u.b * p.max_seq_len + pos;
+          const uint8_t* kvb = static_cast<const uint8_t*>(p.kv);
+          if (kFmt == 1) {
+            bulk_copy(raw(j) + c * C::kRawRow, kvb + row * kDc + rank * kHalf, C::kRawRow, &bars->full[j]);
+            bulk_copy(rsc(j) + c * 16, p.kv_scale + row * kNblk, 16, &bars->full[j]);
+          } else {
+            bulk_copy(raw(j) + c * C::kRawRow, kvb + (row * kDc + rank * kHalf) * 2, C::kRawRow,
+                      &bars->full[j]);
+          }
+          bulk_copy(rpe(j) + c * 128, static_cast<const uint8_t*>(p.pe) + row * kDr * 2, 128,
+                    &bars->full[j]);
+        }
+      }
+      issued = i + 1;
+    }
+    // copies still in flight must land before this CTA's shared memory goes
+    // away; on the normal path every stage was already consumed
+    if (lane == 0 && bars->abort) {
+      for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
+        wt.drain(&bars->full[i % C::kStages], (i / C::kStages) & 1);
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc(128, kN, false);
+      constexpr uint32_t id_pv = idesc(128, kHalf, true);
+      auto issue_pv = [&](int i) -> bool {
+        const int j = i % C::kStages, b = i & 1;
+        if (!wt.wait(&bars->pfull[b], (i >> 1) & 1)) return false;
+        tc_after();
+        const uint32_t pa = sa(pbuf(b)), va = sa(opl(j));
+#pragma unroll
+        for (int k = 0; k < kN / 16; ++k)
+          mma_ss(tmem + kTmemO, sdesc(pa + 32 * k, 16, 1024), sdesc(va + 2048 * k, kBlkBytes, 1024),
+                 id_pv, (i > 0 || k > 0) ? 1 : 0);
+        mma_commit(&bars->pfree[b]);
+        mma_commit(&bars->empty[j]);
+        return true;
+      };
+      bool ok = true;
+      for (int i = 0; i < ntiles && ok; ++i) {
+        const int j = i % C::kStages, b = i & 1;
+        const uint32_t use = i / C::kStages;
+        ok = wt.wait(&bars->full[j], use & 1);
+        if (ok && C::kConv) ok = wt.wait(&bars->deq[j], use & 1);
+        if (ok) ok = wt.wait(&bars->sfree[b], ((i >> 1) & 1) ^ 1);
+        if (!ok) break;
+        tc_after();
+        const uint32_t sd = tmem + (b ? kTmemS1 : kTmemS0);
+        const uint32_t la = sa(opl(j)), pe = sa(ope(j)) + rank * (kPeHalf * 2);
+#pragma unroll
+        for (int k = 0; k < kHalf / 16; ++k)
+          mma_ts(sd, tmem + kTmemQ + 8 * k, sdesc(la + (k >> 2) * kBlkBytes + (k & 3) * 32, 16, 1024),
+                 id_qk, k > 0 ? 1 : 0);
+#pragma unroll
+        for (int k = 0; k < kPeHalf / 16; ++k)
+          mma_ts(sd, tmem + kTmemQ + kHalf / 2 + 8 * k, sdesc(pe + 32 * k, 16, 1024), id_qk, 1);
+        mma_commit(&bars->sfull[b]);
+        if (i > 0) ok = issue_pv(i - 1);
+      }
+      if (ok && ntiles > 0) issue_pv(ntiles - 1);
+      // every MMA issued by this thread completes before tensor memory is freed
+      mma_commit(&bars->drain);
+      wt.drain(&bars->drain, 0);
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ softmax
+    const int h = threadIdx.x - 128;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const float sl2 = p.scale_log2;
+    float m_ref = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int i = 0; i < ntiles; ++i) {
+      const int j = i % C::kStages, b = i & 1;
+      const uint32_t use2 = (i >> 1) & 1;
+      ok = ok && wt.wait(&bars->sfull[b], use2);
+      float s[kN];
+      if (ok) {
+        tc_after();
+        uint32_t r[16];
+#pragma unroll
+        for (int c = 0; c < kN / 16; ++c) {
+          TC_LD16(lane_base + (b ? kTmemS1 : kTmemS0) + 16 * c, r);
+          tc_wait_ld();
+#pragma unroll
+          for (int k = 0; k < 16; ++k) s[16 * c + k] = __uint_as_float(r[k]);
+        }
+        tc_before();
+        bar_arrive(&bars->sfree[b]);
+        // exchange partial scores with the peer
+        ok = wt.wait(&bars->xempty[b], use2 ^ 1);
+      }
+      if (ok) {
+        const uint32_t dst = mapa(xbuf(b) + h * kXStride, peer);
+#pragma unroll
+        for (int c = 0; c < kN / 4; ++c)
+          asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16 * c),
+                       "f"(s[4 * c]), "f"(s[4 * c + 1]), "f"(s[4 * c + 2]), "f"(s[4 * c + 3])
+                       : "memory");
+        bar_arrive_remote(mapa(&bars->xfull[b], peer));
+        ok = wt.wait(&bars->xfull[b], use2);
+      }
+      if (ok) {
+        const float4* xr = reinterpret_cast<const float4*>(xbuf(b) + h * kXStride);
+#pragma unroll
+        for (int c = 0; c < kN / 4; ++c) {
+          const float4 v = xr[c];
+          s[4 * c] += v.x; s[4 * c + 1] += v.y; s[4 * c + 2] += v.z; s[4 * c + 3] += v.w;
+        }
+        bar_arrive_remote(mapa(&bars->xempty[b], peer));
+      }
+      // masked, scaled scores; lazy rescale of the running reference max
+      const int valid = min(kN, u.t1 - (u.t0 + i * kN));
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kN; ++c) {
+        s[c] = c < valid ? s[c] * sl2 : -INFINITY;
+        mt = fmaxf(mt, s[c]);
+      }
+      const bool need = ok && mt > m_ref + kRescaleThreshold;
+      if (__any_sync(0xffffffffu, need)) {
+        const float m_new = need ? mt : m_ref;
+        const float alpha = exp2f(m_ref - m_new);   // 0 when m_ref = -inf
+        if (i > 0) {
+          // O holds tiles < i: wait for PV of tile i-1 (its P buffer's release;
+          // the previous use of that buffer is known complete, so the parity
+          // wait cannot be fooled by a phase two steps back), then scale this
+          // lane's row
+          ok = ok && wt.wait(&bars->pfree[(i - 1) & 1], ((i - 1) >> 1) & 1);
+          tc_after();
+#pragma unroll 1
+          for (int c = 0; c < kHalf / 16; ++c) {
+            uint32_t r[16];
+            TC_LD16(lane_base + kTmemO + 16 * c, r);
+            tc_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
+            TC_ST16(lane_base + kTmemO + 16 * c, r);
+          }
+          tc_wait_st();
+        }
+        l *= alpha;
+        m_ref = m_new;
+      }
+      // P row of head h (bf16), summed as rounded
+      ok = ok && wt.wait(&bars->pfree[b], use2 ^ 1);
+      uint8_t* prow = pbuf(b);
+#pragma unroll
+      for (int c = 0; c < kN / 8; ++c) {
+        uint32_t pk[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const __nv_bfloat162 two = __floats2bfloat162_rn(exp2f(s[8 * c + 2 * k] - m_ref),
+                                                           exp2f(s[8 * c + 2 * k + 1] - m_ref));
+          const float2 back = __bfloat1622float2(two);
+          l += back.x + back.y;
+          pk[k] = *reinterpret_cast<const uint32_t*>(&two);
+        }
+        *reinterpret_cast<uint4*>(prow + swz_chunk(h, c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      }
+      if (!C::kConv && valid < kN) {
+        // dense bf16 tail: rows past the unit hold whatever the cache holds
+        // there; zero them so P = 0 never meets a non-finite value
+        uint8_t* v = opl(j);
+        for (int idx = h; idx < (kN - valid) * 32; idx += 128) {
+          const int row = valid + idx / 32, blk = (idx / 8) & 3, ch = idx & 7;
+          *reinterpret_cast<uint4*>(v + blk * kBlkBytes + swz_chunk(row, ch)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_async_smem();
+      tc_before();
+      bar_arrive(&bars->pfull[b]);
+    }
+    // ------------------------------------------------------------ epilogue
+    if (ntiles > 0) ok = ok && wt.wait(&bars->pfree[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1);
+    tc_after();
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    float* po = p.ws.part_o + ((size_t)unit_id * p.H + h) * kDc + rank * kHalf;
+#pragma unroll 1
+    for (int c = 0; c < kHalf / 16; ++c) {
+      uint32_t r[16];
+      TC_LD16(lane_base + kTmemO + 16 * c, r);
+      tc_wait_ld();
+#pragma unroll
+      for (int k = 0; k < 16; k += 4)
+        *reinterpret_cast<float4*>(po + 16 * c + k) =
+            make_float4(__uint_as_float(r[k]) * inv, __uint_as_float(r[k + 1]) * inv,
+                        __uint_as_float(r[k + 2]) * inv, __uint_as_float(r[k + 3]) * inv);
+    }
+    if (rank == 0)
+      p.ws.part_lse[(size_t)unit_id * p.H + h] =
+          (ok && l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+  } else if (C::kConv && warp >= 8) {
+    // ------------------------------------------------------------ converter
+    const int t = threadIdx.x - 256;
+    for (int i = 0; i < ntiles; ++i) {
+      const int j = i % C::kStages;
+      const uint32_t use = i / C::kStages;
+      if (!wt.wait(&bars->full[j], use & 1)) break;
+      const int valid = min(kN, u.t1 - (u.t0 + i * kN));
+      uint8_t* dst = opl(j);
+      if (kFmt == 1) {
+        // 48 rows x 16 chunks of 16 codes -> 2 swizzled 16-byte chunks each
+        for (int idx = t; idx < kN * 16; idx += 128) {
+          const int row = idx >> 4, q = idx & 15;  // codes [16q, 16q + 16) of the half row
+          uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+          if (row < valid) {
+            const uint4 v = *reinterpret_cast<const uint4*>(raw(j) + row * kHalf + q * 16);
+            const float sc = reinterpret_cast<const float*>(rsc(j) + row * 16)[rank * 2 + (q >> 3)];
+            dequant16(v, sc, lo, hi);
+          }
+          const int blk = q >> 2, ch = (q & 3) * 2;
+          *reinterpret_cast<uint4*>(dst + blk * kBlkBytes + swz_chunk(row, ch)) = lo;
+          *reinterpret_cast<uint4*>(dst + blk * kBlkBytes + swz_chunk(row, ch + 1)) = hi;
+        }
+      } else {
+        // gathered bf16 rows: 48 rows x 32 chunks of 8 values
+        for (int idx = t; idx < kN * 32; idx += 128) {
+          const int row = idx >> 5, q = idx & 31;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (row < valid) v = *reinterpret_cast<const uint4*>(raw(j) + row * C::kRawRow + q * 16);
+          *reinterpret_cast<uint4*>(dst + (q >> 3) * kBlkBytes + swz_chunk(row, q & 7)) = v;
+        }
+      }
+      if (kSparse) {
+        // rotary rows -> swizzled operand
+        for (int idx = t; idx < kN * 8; idx += 128) {
+          const int row = idx >> 3, q = idx & 7;
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (row < valid) v = *reinterpret_cast<const uint4*>(rpe(j) + row * 128 + q * 16);
+          *reinterpret_cast<uint4*>(ope(j) + swz_chunk(row, q)) = v;
+        }
+      }
+      fence_async_smem();
+      bar_arrive(&bars->deq[j]);
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_before();
+  __syncthreads();
+  cluster_sync();  // no remote access into this CTA's shared memory remains
+  if (warp == 1) {
+    tc_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+  }
+}
+
+// ------------------------------------------------------------------ host
+PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+bool encode3(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
+             uint64_t S, uint64_t B, uint32_t box0, CUtensorMapSwizzle sw) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {inner, S, B};
+  cuuint64_t strides[2] = {inner * esize, inner * esize * S};
+  cuuint32_t box[3] = {box0, (cuuint32_t)kN, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int kFmt, bool kSparse>
+cudaError_t launch_tc_variant(const TcParams& tp, cudaStream_t s) {
+  using C = Cfg<kFmt, kSparse>;
+  cudaError_t e = ensure_smem<decode_tc_kernel<kFmt, kSparse>>(C::kSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * tp.p.ws.max_units);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_tc_kernel<kFmt, kSparse>, tp);
+}
+
+}  // namespace
+
+int decode_tc_granule() { return kN; }
+
+bool decode_tc_supported(int H) { return H == 128 && get_encoder() != nullptr; }
+
+cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s) {
+  TcParams tp;
+  memset(&tp, 0, sizeof(tp));
+  tp.p = p;
+  const uint64_t S = (uint64_t)p.max_seq_len, B = (uint64_t)p.B;
+  bool ok = true;
+  if (!p.K) {
+    if (p.fmt == 0) {
+      ok = encode3(&tp.m_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.kv, kDc, S, B, 64,
+                   CU_TENSOR_MAP_SWIZZLE_128B);
+    } else {
+      ok = encode3(&tp.m_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.kv, kDc, S, B, kHalf,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) &&
+           encode3(&tp.m_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.kv_scale, kNblk, S, B, kNblk,
+                   CU_TENSOR_MAP_SWIZZLE_NONE);
+    }
+    ok = ok && encode3(&tp.m_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.pe, kDr, S, B, 64,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
+  }
+  if (!ok) return cudaErrorInvalidValue;
+  if (p.fmt == 0) return p.K ? launch_tc_variant<0, true>(tp, s) : launch_tc_variant<0, false>(tp, s);
+  return p.K ? launch_tc_variant<1, true>(tp, s) : launch_tc_variant<1, false>(tp, s);
+}
+
+}  // namespace mla

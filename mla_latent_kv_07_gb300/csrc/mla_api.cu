@@ -4,6 +4,7 @@
 #include <mutex>
 #include <new>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include "../../include/mla.h"
@@ -130,15 +131,31 @@ mla::DecodeParams make_params(const DecodeArgs& a, const mla::Workspace& ws, int
   return p;
 }
 
+// Decode path: the tensor-memory kernel for H = 128 unless MLA_DECODE_PATH=mma
+// (read once per process) selects the warp-MMA kernel.
+bool use_tc_path(int H) {
+  static int forced = -1;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    const char* v = getenv("MLA_DECODE_PATH");
+    forced = (v && strcmp(v, "mma") == 0) ? 0 : 1;
+  });
+  return forced && mla::decode_tc_supported(H);
+}
+
 // schedule -> decode -> combine, after the lengths are known on the device.
 mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cudaStream_t s) {
   int sms = 0;
   num_sms(&sms);
-  cudaError_t e = mla::launch_schedule(K ? nullptr : a.end_pos, a.max_end_pos, ws, a.B,
-                                       mla::target_units(a.H, sms), mla::decode_mma_granule(), s);
+  const bool tc = use_tc_path(a.H);
+  cudaError_t e = mla::launch_schedule(
+      K ? nullptr : a.end_pos, a.max_end_pos, ws, a.B,
+      tc ? mla::target_units_tc(sms) : mla::target_units_mma(a.H, sms),
+      tc ? mla::decode_tc_granule() : mla::decode_mma_granule(), s);
   if (e != cudaSuccess) return cuda_fail(e, "schedule");
   const bool traced = trace_start(s);
-  e = mla::launch_decode_mma(make_params(a, ws, K), s);
+  e = tc ? mla::launch_decode_tc(make_params(a, ws, K), s)
+         : mla::launch_decode_mma(make_params(a, ws, K), s);
   trace_stop(s, traced);
   if (e != cudaSuccess) return cuda_fail(e, "decode");
   e = mla::launch_combine(ws, a.B, a.H, a.out, a.lse, s);
