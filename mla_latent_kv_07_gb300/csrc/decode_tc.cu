@@ -26,12 +26,17 @@
 // Tensor memory (512 columns): O half [0,256) fp32; Q half [256,400) bf16 (2
 // per column); S double buffer [400,448) and [448,496) fp32.
 //
-// Warp roles (256 threads; 384 when a converter is needed):
+// Warp roles (384 threads; 512 when a converter is needed):
 //   warp 0  producer: TMA tiles (dense) or per-row bulk copies (gather)
 //   warp 1  MMA issuer (one thread) and tensor-memory owner
-//   warps 4-7  softmax: thread h <-> head h <-> TMEM lane h; partial-score
-//              exchange, online softmax (lazy rescale), P, epilogue
-//   warps 8-11 converter (FP8 caches and gathers): raw rows -> bf16 operand
+//   warps 4-7  softmax: thread h <-> head h <-> TMEM lane h; online softmax
+//              (lazy rescale), P, epilogue
+//   warps 8-11 exchange: partial S from TMEM -> peer (DSMEM), peer partial +
+//              own partial -> full S written back to the same TMEM columns.
+//              Distributed shared memory moves ~40 GB/s per SM with ~0.3 us
+//              latency on this part, so this runs as its own pipeline stage,
+//              overlapping the softmax of the previous tile.
+//   warps 12-15 converter (FP8 caches and gathers): raw rows -> bf16 operand
 //              tile bf16(fp32(e4m3 * scale)) in the 128-byte swizzled layout
 //
 // Every wait is bounded; on expiry the kernel raises a status bit, stops
@@ -57,16 +62,19 @@ constexpr int kBlkBytes = kN * 128;        // one 64-column swizzled block of a 
 constexpr int kOplBytes = 4 * kBlkBytes;   // latent half operand: 24 KB
 constexpr int kOpeBytes = kBlkBytes;       // rotary operand (full 64 columns): 6 KB
 constexpr int kPBytes = 128 * 128;         // P: 128 heads x 64 (48 used) bf16, swizzled
-constexpr int kXStride = kN + 4;           // exchange row stride (floats), bank spread
-constexpr int kXBytes = 128 * kXStride * 4;
+// exchange buffer: float4 chunk c (positions 4c..4c+3) of head h at index
+// c * 128 + h, so a warp's remote store is one contiguous 512-byte run
+constexpr int kXBytes = (kN / 4) * 128 * 16;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
 constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemS0 = 400, kTmemS1 = 448;
-constexpr long kSpinLimit = 1L << 22;
+constexpr long kSpinLimit = 1L << 26;   // polls (~seconds) before giving up
+constexpr int kQRow = 576 + 16;   // staged query row (bytes), padded against bank conflicts
+constexpr int kORow = 512 + 16;   // staged half-output row (128 fp32), padded
 
 template <int kFmt, bool kSparse>
 struct Cfg {
   static constexpr bool kConv = kFmt == 1 || kSparse;       // converter warps present
-  static constexpr int kThreads = kConv ? 384 : 256;
+  static constexpr int kThreads = kConv ? 512 : 384;
   static constexpr int kRawRow = kFmt == 1 ? kHalf : kHalf * 2;  // bytes of a raw latent half row
   static constexpr int kRawBytes = kConv ? kN * kRawRow : 0;
   static constexpr int kScBytes = kFmt == 1 ? 1024 : 0;          // 48 x 16 B, padded
@@ -80,6 +88,7 @@ struct Cfg {
   static constexpr int kSmem = kBarOff + 1024 + 1024;      // barriers/flags + base alignment slack
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kStage % 1024 == 0 && kOplBytes % 1024 == 0, "1 KB alignment of swizzled tiles");
+  static_assert(kStagesBytes >= 128 * kQRow && kStagesBytes >= 128 * kORow, "staging fits the stages");
 };
 
 struct TcParams {
@@ -107,10 +116,14 @@ __device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa(b)), "r"(bytes)
                : "memory");
 }
+// Non-suspending probe of a barrier phase.  (A suspending try_wait was seen to
+// return up to microseconds after phases completed by tcgen05.commit or by
+// remote arrivals, which serialised the pipeline; a polling test_wait notices
+// them at once.)
 __device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
+      "{ .reg .pred p; mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
       "selp.u32 %0, 1, 0, p; }"
       : "=r"(ok)
       : "r"(sa(b)), "r"(parity)
@@ -198,6 +211,20 @@ __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+__device__ __forceinline__ void bulk_store(void* gdst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(sa(src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// named barrier 1 among the 128 softmax threads
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+
 // byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled block
 __device__ __forceinline__ uint32_t swz_chunk(int row, int chunk) {
   return (row >> 3) * 1024 + (row & 7) * 128 + (((chunk ^ row) & 7) << 4);
@@ -206,8 +233,9 @@ __device__ __forceinline__ uint32_t swz_chunk(int row, int chunk) {
 // Shared state of the CTA (barriers, flags) at the tail of shared memory.
 struct Bars {
   uint64_t full[4], deq[4], empty[4];
-  uint64_t sfull[2], sfree[2], pfull[2], pfree[2], xfull[2], xempty[2];
+  uint64_t sfull[2], sready[2], sfree[2], pfull[2], pfree[2], xfull[2], xempty[2];
   uint64_t drain;   // final commit of the MMA issuer
+  uint64_t qbar;    // query rows staged in shared memory
   uint32_t tmem;
   volatile int abort;
 };
@@ -281,18 +309,20 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int j = 0; j < C::kStages; ++j) {
       bar_init(&bars->full[j], 1);
-      bar_init(&bars->deq[j], 128);
+      bar_init(&bars->deq[j], 4);
       bar_init(&bars->empty[j], 1);
     }
     for (int b = 0; b < 2; ++b) {
       bar_init(&bars->sfull[b], 1);
-      bar_init(&bars->sfree[b], 128);
-      bar_init(&bars->pfull[b], 128);
+      bar_init(&bars->sready[b], 4);
+      bar_init(&bars->sfree[b], 4);
+      bar_init(&bars->pfull[b], 4);
       bar_init(&bars->pfree[b], 1);
-      bar_init(&bars->xfull[b], 128);
-      bar_init(&bars->xempty[b], 128);
+      bar_init(&bars->xfull[b], 4);
+      bar_init(&bars->xempty[b], 4);
     }
     bar_init(&bars->drain, 1);
+    bar_init(&bars->qbar, 1);
     bars->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -307,21 +337,28 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   const uint32_t tmem = bars->tmem;
   cluster_sync();  // the peer's barriers are initialised before any remote arrive
 
-  // Q half -> tensor memory (A operand of QK): lane h, 2 bf16 per column
+  // Q half -> tensor memory (A operand of QK): lane h, 2 bf16 per column.
+  // All 128 rows are bulk-copied into (still unused) stage memory at once,
+  // then each thread moves its row to its TMEM lane.
   if (warp >= 4 && warp < 8) {
     const int h = threadIdx.x - 128;
     const size_t qrow = (size_t)u.b * p.H + h;
-    const uint4* ql = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q_latent) +
-                                                     qrow * kDc + rank * kHalf);
-    const uint4* qp = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q_pe) +
-                                                     qrow * kDr + rank * kPeHalf);
+    uint8_t* qs = sm + h * kQRow;
+    if (h == 0) bar_expect_tx(&bars->qbar, 128 * (kHalf * 2 + kPeHalf * 2));
+    softmax_sync();
+    bulk_copy(qs, static_cast<const __nv_bfloat16*>(p.q_latent) + qrow * kDc + rank * kHalf,
+              kHalf * 2, &bars->qbar);
+    bulk_copy(qs + kHalf * 2, static_cast<const __nv_bfloat16*>(p.q_pe) + qrow * kDr + rank * kPeHalf,
+              kPeHalf * 2, &bars->qbar);
+    wt.drain(&bars->qbar, 0);
+    const uint4* qv = reinterpret_cast<const uint4*>(qs);
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
 #pragma unroll
     for (int c = 0; c < 9; ++c) {  // 144 columns = 9 x 16
       uint32_t r[16];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint4 v = c < 8 ? ql[c * 4 + k] : qp[k];
+        const uint4 v = qv[c * 4 + k];
         r[4 * k] = v.x; r[4 * k + 1] = v.y; r[4 * k + 2] = v.z; r[4 * k + 3] = v.w;
       }
       TC_ST16(lane_base + kTmemQ + 16 * c, r);
@@ -383,47 +420,134 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer
+    // Event-driven: QK of the next tile is issued as soon as its stage, its
+    // converted operand and its S buffer are ready (at most two tiles ahead
+    // of PV: the S buffers are double); PV of the next tile as soon as its P
+    // is written.  Neither waits behind the other's inputs.
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc(128, kN, false);
       constexpr uint32_t id_pv = idesc(128, kHalf, true);
-      auto issue_pv = [&](int i) -> bool {
-        const int j = i % C::kStages, b = i & 1;
-        if (!wt.wait(&bars->pfull[b], (i >> 1) & 1)) return false;
-        tc_after();
-        const uint32_t pa = sa(pbuf(b)), va = sa(opl(j));
+      int nq = 0, np = 0;
+      long idle = 0;
+      while (np < ntiles && !bars->abort) {
+        bool did = false;
+        if (nq < ntiles && nq < np + 3) {
+          const int k = nq, j = k % C::kStages, b = k & 1;
+          const uint32_t use = k / C::kStages;
+          if (bar_try(&bars->full[j], use & 1) && (!C::kConv || bar_try(&bars->deq[j], use & 1)) &&
+              bar_try(&bars->sfree[b], ((k >> 1) & 1) ^ 1)) {
+            tc_after();
+            const uint32_t sd = tmem + (b ? kTmemS1 : kTmemS0);
+            const uint32_t la = sa(opl(j)), pe = sa(ope(j)) + rank * (kPeHalf * 2);
 #pragma unroll
-        for (int k = 0; k < kN / 16; ++k)
-          mma_ss(tmem + kTmemO, sdesc(pa + 32 * k, 16, 1024), sdesc(va + 2048 * k, kBlkBytes, 1024),
-                 id_pv, (i > 0 || k > 0) ? 1 : 0);
-        mma_commit(&bars->pfree[b]);
-        mma_commit(&bars->empty[j]);
-        return true;
-      };
-      bool ok = true;
-      for (int i = 0; i < ntiles && ok; ++i) {
-        const int j = i % C::kStages, b = i & 1;
-        const uint32_t use = i / C::kStages;
-        ok = wt.wait(&bars->full[j], use & 1);
-        if (ok && C::kConv) ok = wt.wait(&bars->deq[j], use & 1);
-        if (ok) ok = wt.wait(&bars->sfree[b], ((i >> 1) & 1) ^ 1);
-        if (!ok) break;
-        tc_after();
-        const uint32_t sd = tmem + (b ? kTmemS1 : kTmemS0);
-        const uint32_t la = sa(opl(j)), pe = sa(ope(j)) + rank * (kPeHalf * 2);
+            for (int kk = 0; kk < kHalf / 16; ++kk)
+              mma_ts(sd, tmem + kTmemQ + 8 * kk,
+                     sdesc(la + (kk >> 2) * kBlkBytes + (kk & 3) * 32, 16, 1024), id_qk, kk > 0 ? 1 : 0);
 #pragma unroll
-        for (int k = 0; k < kHalf / 16; ++k)
-          mma_ts(sd, tmem + kTmemQ + 8 * k, sdesc(la + (k >> 2) * kBlkBytes + (k & 3) * 32, 16, 1024),
-                 id_qk, k > 0 ? 1 : 0);
+            for (int kk = 0; kk < kPeHalf / 16; ++kk)
+              mma_ts(sd, tmem + kTmemQ + kHalf / 2 + 8 * kk, sdesc(pe + 32 * kk, 16, 1024), id_qk, 1);
+            mma_commit(&bars->sfull[b]);
+            ++nq;
+            did = true;
+          }
+        }
+        if (np < nq) {
+          const int i = np, j = i % C::kStages, b = i & 1;
+          if (bar_try(&bars->pfull[b], (i >> 1) & 1)) {
+            tc_after();
+            const uint32_t pa = sa(pbuf(b)), va = sa(opl(j));
 #pragma unroll
-        for (int k = 0; k < kPeHalf / 16; ++k)
-          mma_ts(sd, tmem + kTmemQ + kHalf / 2 + 8 * k, sdesc(pe + 32 * k, 16, 1024), id_qk, 1);
-        mma_commit(&bars->sfull[b]);
-        if (i > 0) ok = issue_pv(i - 1);
+            for (int kk = 0; kk < kN / 16; ++kk)
+              mma_ss(tmem + kTmemO, sdesc(pa + 32 * kk, 16, 1024),
+                     sdesc(va + 2048 * kk, kBlkBytes, 1024), id_pv, (i > 0 || kk > 0) ? 1 : 0);
+            mma_commit(&bars->pfree[b]);
+            mma_commit(&bars->empty[j]);
+            ++np;
+            did = true;
+          }
+        }
+        if (did) {
+          idle = 0;
+        } else if (++idle > kSpinLimit) {
+          bars->abort = 1;
+          atomicOr(p.ws.status, kDevTimeout);
+        }
       }
-      if (ok && ntiles > 0) issue_pv(ntiles - 1);
       // every MMA issued by this thread completes before tensor memory is freed
       mma_commit(&bars->drain);
       wt.drain(&bars->drain, 0);
+    }
+  } else if (warp >= 8 && warp < 12) {
+    // ------------------------------------------------------------ exchange
+    // The own partial is re-read from TMEM when finishing (it stays there
+    // until the softmax has read the full sum), so no registers are held
+    // across the transfer.
+    const int h = threadIdx.x - 256;
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    auto send = [&](int k) -> bool {
+      const int b = k & 1;
+      const uint32_t use2 = (k >> 1) & 1;
+      if (!wt.wait(&bars->sfull[b], use2)) return false;
+      tc_after();
+      const uint32_t sb = lane_base + (b ? kTmemS1 : kTmemS0);
+      uint32_t r0[16], r1[16], r2[16];
+      TC_LD16(sb, r0);
+      TC_LD16(sb + 16, r1);
+      TC_LD16(sb + 32, r2);
+      tc_wait_ld();
+      if (!wt.wait(&bars->xempty[b], use2 ^ 1)) return false;
+      const uint32_t xd = mapa(xbuf(b) + 4 * h, peer);
+#pragma unroll
+      for (int c = 0; c < kN / 4; ++c) {
+        const uint32_t* src = c < 4 ? r0 + 4 * c : (c < 8 ? r1 + 4 * (c - 4) : r2 + 4 * (c - 8));
+        asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(xd + 16 * 128 * c),
+                     "r"(src[0]), "r"(src[1]), "r"(src[2]), "r"(src[3])
+                     : "memory");
+      }
+      __syncwarp();
+      if (lane == 0) bar_arrive_remote(mapa(&bars->xfull[b], peer));
+      return true;
+    };
+    auto finish = [&](int k) -> bool {
+      const int b = k & 1;
+      const uint32_t use2 = (k >> 1) & 1;
+      if (!wt.wait(&bars->xfull[b], use2)) return false;
+      tc_after();
+      const uint32_t sb = lane_base + (b ? kTmemS1 : kTmemS0);
+      uint32_t r0[16], r1[16], r2[16];
+      TC_LD16(sb, r0);
+      TC_LD16(sb + 16, r1);
+      TC_LD16(sb + 32, r2);
+      tc_wait_ld();
+      const float4* xr = reinterpret_cast<const float4*>(xbuf(b)) + h;
+#pragma unroll
+      for (int c = 0; c < kN / 4; ++c) {
+        const float4 v = xr[128 * c];
+        uint32_t* d = c < 4 ? r0 + 4 * c : (c < 8 ? r1 + 4 * (c - 4) : r2 + 4 * (c - 8));
+        d[0] = __float_as_uint(__uint_as_float(d[0]) + v.x);
+        d[1] = __float_as_uint(__uint_as_float(d[1]) + v.y);
+        d[2] = __float_as_uint(__uint_as_float(d[2]) + v.z);
+        d[3] = __float_as_uint(__uint_as_float(d[3]) + v.w);
+      }
+      TC_ST16(sb, r0);
+      TC_ST16(sb + 16, r1);
+      TC_ST16(sb + 32, r2);
+      tc_wait_st();
+      tc_before();
+      __syncwarp();
+      if (lane == 0) {
+        bar_arrive_remote(mapa(&bars->xempty[b], peer));   // my buffer b may be refilled
+        bar_arrive(&bars->sready[b]);
+      }
+      return true;
+    };
+    // One tile at a time: sending tile i+1 before finishing tile i would make
+    // the finish wait for QK of tile i+1, which itself waits for the softmax
+    // of tile i-1 (two score buffers), lengthening the critical cycle.
+    bool ok = true;
+    for (int i = 0; i < ntiles && ok; ++i) {
+      ok = send(i);
+      if (ok) ok = finish(i);
     }
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ softmax
@@ -435,50 +559,37 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     for (int i = 0; i < ntiles; ++i) {
       const int j = i % C::kStages, b = i & 1;
       const uint32_t use2 = (i >> 1) & 1;
-      ok = ok && wt.wait(&bars->sfull[b], use2);
-      float s[kN];
-      if (ok) {
+      float sc[kN];
+      ok = ok && wt.wait(&bars->sready[b], use2);
+      {
         tc_after();
-        uint32_t r[16];
+        const uint32_t sb = lane_base + (b ? kTmemS1 : kTmemS0);
+        uint32_t r0[16], r1[16], r2[16];
+        TC_LD16(sb, r0);
+        TC_LD16(sb + 16, r1);
+        TC_LD16(sb + 32, r2);
+        tc_wait_ld();
 #pragma unroll
-        for (int c = 0; c < kN / 16; ++c) {
-          TC_LD16(lane_base + (b ? kTmemS1 : kTmemS0) + 16 * c, r);
-          tc_wait_ld();
-#pragma unroll
-          for (int k = 0; k < 16; ++k) s[16 * c + k] = __uint_as_float(r[k]);
+        for (int c = 0; c < 16; ++c) {
+          sc[c] = __uint_as_float(r0[c]);
+          sc[16 + c] = __uint_as_float(r1[c]);
+          sc[32 + c] = __uint_as_float(r2[c]);
         }
         tc_before();
-        bar_arrive(&bars->sfree[b]);
-        // exchange partial scores with the peer
-        ok = wt.wait(&bars->xempty[b], use2 ^ 1);
-      }
-      if (ok) {
-        const uint32_t dst = mapa(xbuf(b) + h * kXStride, peer);
-#pragma unroll
-        for (int c = 0; c < kN / 4; ++c)
-          asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16 * c),
-                       "f"(s[4 * c]), "f"(s[4 * c + 1]), "f"(s[4 * c + 2]), "f"(s[4 * c + 3])
-                       : "memory");
-        bar_arrive_remote(mapa(&bars->xfull[b], peer));
-        ok = wt.wait(&bars->xfull[b], use2);
-      }
-      if (ok) {
-        const float4* xr = reinterpret_cast<const float4*>(xbuf(b) + h * kXStride);
-#pragma unroll
-        for (int c = 0; c < kN / 4; ++c) {
-          const float4 v = xr[c];
-          s[4 * c] += v.x; s[4 * c + 1] += v.y; s[4 * c + 2] += v.z; s[4 * c + 3] += v.w;
-        }
-        bar_arrive_remote(mapa(&bars->xempty[b], peer));
+        __syncwarp();
+        if (lane == 0) bar_arrive(&bars->sfree[b]);   // QK of tile i+2 may overwrite
       }
       // masked, scaled scores; lazy rescale of the running reference max
       const int valid = min(kN, u.t1 - (u.t0 + i * kN));
-      float mt = -INFINITY;
+      float mx[8];
 #pragma unroll
-      for (int c = 0; c < kN; ++c) {
-        s[c] = c < valid ? s[c] * sl2 : -INFINITY;
-        mt = fmaxf(mt, s[c]);
-      }
+      for (int c = 0; c < kN; ++c) sc[c] = c < valid ? sc[c] * sl2 : -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+        mx[c] = fmaxf(fmaxf(fmaxf(sc[c], sc[c + 8]), fmaxf(sc[c + 16], sc[c + 24])),
+                      fmaxf(sc[c + 32], sc[c + 40]));
+      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const bool need = ok && mt > m_ref + kRescaleThreshold;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? mt : m_ref;
@@ -491,35 +602,44 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           ok = ok && wt.wait(&bars->pfree[(i - 1) & 1], ((i - 1) >> 1) & 1);
           tc_after();
 #pragma unroll 1
-          for (int c = 0; c < kHalf / 16; ++c) {
-            uint32_t r[16];
-            TC_LD16(lane_base + kTmemO + 16 * c, r);
+          for (int c = 0; c < kHalf / 32; ++c) {
+            uint32_t r[16], q[16];
+            TC_LD16(lane_base + kTmemO + 32 * c, r);
+            TC_LD16(lane_base + kTmemO + 32 * c + 16, q);
             tc_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-            TC_ST16(lane_base + kTmemO + 16 * c, r);
+            for (int k = 0; k < 16; ++k) {
+              r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
+              q[k] = __float_as_uint(__uint_as_float(q[k]) * alpha);
+            }
+            TC_ST16(lane_base + kTmemO + 32 * c, r);
+            TC_ST16(lane_base + kTmemO + 32 * c + 16, q);
           }
           tc_wait_st();
         }
         l *= alpha;
         m_ref = m_new;
       }
-      // P row of head h (bf16), summed as rounded
+      // P row of head h (bf16); l sums the rounded values
       ok = ok && wt.wait(&bars->pfree[b], use2 ^ 1);
       uint8_t* prow = pbuf(b);
+      float ls[kN / 8];
 #pragma unroll
       for (int c = 0; c < kN / 8; ++c) {
         uint32_t pk[4];
+        float part = 0.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const __nv_bfloat162 two = __floats2bfloat162_rn(exp2f(s[8 * c + 2 * k] - m_ref),
-                                                           exp2f(s[8 * c + 2 * k + 1] - m_ref));
+          const __nv_bfloat162 two = __floats2bfloat162_rn(exp2f(sc[8 * c + 2 * k] - m_ref),
+                                                           exp2f(sc[8 * c + 2 * k + 1] - m_ref));
           const float2 back = __bfloat1622float2(two);
-          l += back.x + back.y;
+          part += back.x + back.y;
           pk[k] = *reinterpret_cast<const uint32_t*>(&two);
         }
+        ls[c] = part;
         *reinterpret_cast<uint4*>(prow + swz_chunk(h, c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
+      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + (ls[4] + ls[5]);
       if (!C::kConv && valid < kN) {
         // dense bf16 tail: rows past the unit hold whatever the cache holds
         // there; zero them so P = 0 never meets a non-finite value
@@ -531,30 +651,48 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       }
       fence_async_smem();
       tc_before();
-      bar_arrive(&bars->pfull[b]);
+      __syncwarp();
+      if (lane == 0) bar_arrive(&bars->pfull[b]);
     }
     // ------------------------------------------------------------ epilogue
     if (ntiles > 0) ok = ok && wt.wait(&bars->pfree[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1);
     tc_after();
+    // O half (128 heads x 256) -> workspace, normalised by l: staged through
+    // the (now idle) stage memory in two 128-column halves, one bulk store
+    // of 512 bytes per head row
     const float inv = l > 0.f ? 1.f / l : 0.f;
     float* po = p.ws.part_o + ((size_t)unit_id * p.H + h) * kDc + rank * kHalf;
+    uint8_t* orow = sm + h * kORow;
 #pragma unroll 1
-    for (int c = 0; c < kHalf / 16; ++c) {
-      uint32_t r[16];
-      TC_LD16(lane_base + kTmemO + 16 * c, r);
-      tc_wait_ld();
+    for (int half = 0; half < 2; ++half) {
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[16], q[16];
+        const uint32_t col = kTmemO + 128 * half + 32 * c;
+        TC_LD16(lane_base + col, r);
+        TC_LD16(lane_base + col + 16, q);
+        tc_wait_ld();
+        float4* dst = reinterpret_cast<float4*>(orow + 128 * c);
 #pragma unroll
-      for (int k = 0; k < 16; k += 4)
-        *reinterpret_cast<float4*>(po + 16 * c + k) =
-            make_float4(__uint_as_float(r[k]) * inv, __uint_as_float(r[k + 1]) * inv,
-                        __uint_as_float(r[k + 2]) * inv, __uint_as_float(r[k + 3]) * inv);
+        for (int k = 0; k < 4; ++k) {
+          dst[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
+                               __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
+          dst[4 + k] = make_float4(__uint_as_float(q[4 * k]) * inv, __uint_as_float(q[4 * k + 1]) * inv,
+                                   __uint_as_float(q[4 * k + 2]) * inv, __uint_as_float(q[4 * k + 3]) * inv);
+        }
+      }
+      fence_async_smem();
+      bulk_store(po + 128 * half, orow, 512);
+      bulk_commit();
+      bulk_wait_read();   // the staging row is reused by the second half
     }
+    bulk_wait_all();
     if (rank == 0)
       p.ws.part_lse[(size_t)unit_id * p.H + h] =
           (ok && l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
-  } else if (C::kConv && warp >= 8) {
+  } else if (C::kConv && warp >= 12) {
     // ------------------------------------------------------------ converter
-    const int t = threadIdx.x - 256;
+    const int t = threadIdx.x - 384;
     for (int i = 0; i < ntiles; ++i) {
       const int j = i % C::kStages;
       const uint32_t use = i / C::kStages;
@@ -594,7 +732,8 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         }
       }
       fence_async_smem();
-      bar_arrive(&bars->deq[j]);
+      __syncwarp();
+      if (lane == 0) bar_arrive(&bars->deq[j]);
     }
   }
 
