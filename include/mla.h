@@ -178,6 +178,35 @@ MLA_API mla_status mla_decode_sparse(const mla_cache* cache, const void* q_laten
 MLA_API mla_status mla_workspace_status(const void* workspace, uint32_t* flags, void* stream);
 
 /*
+ * mla_decode_noalloc -- the dense decode of mla_decode, for callers that
+ * cannot allocate device memory where they decode (for example a serving loop
+ * that forbids allocations after warm-up, or a host interface that hands in
+ * only the input and output buffers), and so cannot provide a workspace.  The
+ * pages have no counterpart of this call.
+ *
+ * Instead of a caller workspace it uses one file-scope device array of
+ * 32 MiB, reserved on every GPU that loads the library until the process
+ * exits.  The first call on a device looks up that array's device address and
+ * caches it: make that first call before starting any stream capture.  It
+ * allocates nothing (no cudaMalloc, cudaFree or allocating routine).
+ *
+ *   arguments   as for mla_decode, without workspace and ws_bytes
+ *   returns     MLA_ERR_WORKSPACE if this B and H (on this GPU's SM count)
+ *               need more scratch than the 32 MiB array holds -- at H = 128 on
+ *               152 SMs that is B > about 50 -- and the other MLA_ERR_* codes
+ *               as mla_decode does.
+ *
+ * All calls share the array and leave their contents in it; each call clears
+ * what must start at zero.  Calls whose GPU work overlaps (other streams, or
+ * other host threads without ordering) race on it: order them.  The device
+ * status word (MLA_DEV_*) of this call lives in that array and is not exposed.
+ */
+MLA_API mla_status mla_decode_noalloc(const mla_cache* cache, const void* q_latent,
+                                      const void* q_pe, const int32_t* end_pos,
+                                      int32_t max_end_pos, int32_t B, int32_t H,
+                                      float softmax_scale, void* out, float* lse, void* stream);
+
+/*
  * Tracing (no counterpart on the pages; a measurement aid).  Between
  * mla_trace_begin and mla_trace_end, on the calling host thread, every decode
  * call records a CUDA event pair around its main decode kernel on the call's

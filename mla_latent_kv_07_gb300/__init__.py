@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
             L.mla_status_string.argtypes = [I32]
             L.mla_status_string.restype = ctypes.c_char_p
             L.mla_last_error.restype = ctypes.c_char_p
+            L.mla_decode_noalloc.argtypes = [P, P, P, P, I32, I32, I32, F, P, P, P]
+            L.mla_decode_noalloc.restype = I32
             L.mla_trace_begin.argtypes = [I32]
             L.mla_trace_begin.restype = I32
             L.mla_trace_end.argtypes = [P, P, P]
@@ -167,6 +169,22 @@ def decode(cache: Cache, q_latent, q_pe, end_pos, max_end_pos: int, softmax_scal
     _check(lib().mla_decode(cache.ref, _ptr(q_latent), _ptr(q_pe), _ptr(end_pos), int(max_end_pos),
                             B, H, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
                             workspace.numel(), _stream(stream)), "mla_decode")
+    return out, lse
+
+
+def decode_noalloc(cache: Cache, q_latent, q_pe, end_pos, max_end_pos: int, softmax_scale: float,
+                   out=None, lse=None, want_lse: bool = True, stream=None):
+    """Dense decode through mla_decode_noalloc: no workspace is passed; the
+    library uses its own static device scratch (for callers that cannot
+    allocate).  Returns (out, lse)."""
+    B, H, _ = q_latent.shape
+    _need(q_latent, torch.bfloat16, (B, H, 512), "q_latent")
+    _need(q_pe, torch.bfloat16, (B, H, 64), "q_pe")
+    _need(end_pos, torch.int32, (B,), "end_pos")
+    out, lse = _outputs(B, H, q_latent.device, out, lse, want_lse)
+    _check(lib().mla_decode_noalloc(cache.ref, _ptr(q_latent), _ptr(q_pe), _ptr(end_pos),
+                                    int(max_end_pos), B, H, float(softmax_scale), _ptr(out),
+                                    _ptr(lse), _stream(stream)), "mla_decode_noalloc")
     return out, lse
 
 
