@@ -53,15 +53,23 @@ def peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kernel_source_hash() -> str:
+def decode_path(H: int) -> str:
+    """Which decode kernel the library runs for H heads (mirrors its choice)."""
+    if H == 128 and os.environ.get("MLA_DECODE_PATH", "") != "mma":
+        return "decode_tc_kernel"
+    return "decode_mma_kernel"
+
+
+def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
-    for name in ("decode_mma.cu", "common.cuh"):
+    src = "decode_tc.cu" if kernel == "decode_tc_kernel" else "decode_mma.cu"
+    for name in (src, "common.cuh"):
         with open(os.path.join(ROOT, "mla_latent_kv_07_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
+def recorded_traffic(workload: str, kernel: str):
     """DRAM bytes per launch of the decode kernel from the committed ncu
     summary, if it was taken on the current kernel source; else None."""
     path = os.path.join(ROOT, "profiles", "decode_kernel_traffic.txt")
@@ -70,7 +78,7 @@ def recorded_traffic(workload: str):
     except OSError:
         return None
     src = re.search(r"^kernel_source_sha256_16:\s*(\S+)", text, re.M)
-    if not src or src.group(1) != kernel_source_hash():
+    if not src or src.group(1) != kernel_source_hash(kernel):
         return None
     m = re.search(rf"^{re.escape(workload)}:\s*([0-9.eE+]+)", text, re.M)
     return float(m.group(1)) if m else None
@@ -131,6 +139,21 @@ class ClockSampler:
         reasons = sorted({names[i] for r in window for i, v in enumerate(r[3]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[1] for r in window), "sm_max_mhz": max(r[2] for r in window),
                 "reasons": reasons, "samples": len(window), "window": where}
+
+
+def slowest(ms: float, device) -> float:
+    """Largest time over all ranks (identity without a process group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, slowest_s: float) -> float:
+    """Units all ranks processed / the slowest rank's time (weak scaling)."""
+    return world * units_per_rank / slowest_s
 
 
 # ------------------------------------------------------------ workload set-up
@@ -255,15 +278,11 @@ def run_gpu(args, rank, world, local_rank):
     ms = e0.elapsed_time(e1)
     kern_ms, timed, launches = mla.trace_end()
     clocks = sampler.stop() if sampler else None
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-
+    ms = slowest(ms, device)
     step_s = ms / 1e3 / K
     cache_bytes = st.tokens * layout.cache_bytes_per_token(w.fmt)
-    value = world * cache_bytes / step_s / 1e12
-    tokens_per_s = world * w.B / step_s
+    value = whole_job_rate(cache_bytes, world, step_s) / 1e12
+    tokens_per_s = whole_job_rate(w.B, world, step_s)
 
     # dominant kernel: the decode kernel, timed by its own events
     kern_s = kern_ms / 1e3 / max(timed, 1)
@@ -275,9 +294,10 @@ def run_gpu(args, rank, world, local_rank):
         achieved, peak, unit, bound = cache_bytes / kern_s / 1e9, pk["hbm_gbs"], "GB/s", "hbm"
     else:
         achieved, peak, unit, bound = flops / kern_s / 1e12, pk["bf16_tflops"], "TFLOP/s", "tensor"
+    kernel = decode_path(w.H)
     roofline = {"bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name),
-                "peak_source": f"of {pk_src}", "kernel": "decode_mma_kernel",
+                "frac": round(achieved / peak, 4), "traffic": recorded_traffic(w.name, kernel),
+                "peak_source": f"of {pk_src}", "kernel": kernel,
                 "kernel_us": round(kern_s * 1e6, 3),
                 "hbm_frac_of_step": round(cache_bytes / step_s / 1e9 / pk["hbm_gbs"], 4),
                 "roofline_time_us": round(max(t_hbm, t_tc) * 1e6, 3)}
@@ -389,14 +409,20 @@ def time_oracle_step(sample, w):
     return time.perf_counter() - t0, tokens
 
 
-def run_cpu_baseline(w):
+def run_cpu_baseline(w, min_seconds: float = 1.0):
+    """The oracle on one sequence of the workload, repeated until about
+    `min_seconds` of wall time (x the cores it uses: ~10-30 s of CPU work)."""
     from oracle import oracle as orc
     sample = oracle_sample(w, 10.0)
-    dt, tokens = time_oracle_step(sample, w)
-    bytes_ = tokens * layout.cache_bytes_per_token(w.fmt)
-    return {"value": round(bytes_ / dt / 1e12, 8), "unit": "TB/s", "cores": orc.num_threads(),
-            "kind": "oracle", "seconds": round(dt, 3),
-            "sample": f"one sequence of the workload (end_pos {sample[4]}, all {w.H} heads, "
+    total, reps, tokens = 0.0, 0, 0
+    while total < min_seconds or reps == 0:
+        dt, tokens = time_oracle_step(sample, w)
+        total += dt
+        reps += 1
+    bytes_ = reps * tokens * layout.cache_bytes_per_token(w.fmt)
+    return {"value": round(bytes_ / total / 1e12, 8), "unit": "TB/s", "cores": orc.num_threads(),
+            "kind": "oracle", "seconds": round(total, 3),
+            "sample": f"{reps} x one sequence of the workload (end_pos {sample[4]}, all {w.H} heads, "
                       f"{tokens} attended positions), fp64 oracle, OpenMP over heads"}
 
 

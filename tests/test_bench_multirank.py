@@ -1,0 +1,51 @@
+"""The benchmark's multi-rank harness logic on CPU: two gloo ranks, each with
+its own timing; every rank must see the slowest rank's time, and the
+whole-job rate must count the units of all ranks (weak scaling)."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank(rank, world, port, results):
+    import torch.distributed as dist
+    import bench
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    ms = [3.0, 7.5][rank]
+    slow = bench.slowest(ms, "cpu")
+    rate = bench.whole_job_rate(100.0, world, slow / 1e3)
+    results[rank] = (slow, rate)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_take_the_slowest_time():
+    world = 2
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as mgr:
+        results = mgr.dict()
+        port = _free_port()
+        procs = [ctx.Process(target=_rank, args=(r, world, port, results)) for r in range(world)]
+        for p in procs:
+            p.start()
+        for p in procs:
+            p.join(120)
+            assert p.exitcode == 0
+        assert results[0] == results[1]
+        slow, rate = results[0]
+        assert slow == 7.5
+        assert rate == pytest.approx(2 * 100.0 / 7.5e-3)
+
+
+def test_single_process_is_identity():
+    import bench
+    assert bench.slowest(4.25, "cpu") == 4.25
+    assert bench.whole_job_rate(10.0, 1, 2.0) == 5.0
