@@ -31,11 +31,11 @@
 //   warp 1  MMA issuer (one thread) and tensor-memory owner
 //   warps 4-7  softmax: thread h <-> head h <-> TMEM lane h; online softmax
 //              (lazy rescale), P, epilogue
-//   warps 8-11 exchange: partial S from TMEM -> peer (DSMEM), peer partial +
-//              own partial -> full S written back to the same TMEM columns.
-//              Distributed shared memory moves ~40 GB/s per SM with ~0.3 us
-//              latency on this part, so this runs as its own pipeline stage,
-//              overlapping the softmax of the previous tile.
+//   warps 8-11 exchange: partial S of each tile from TMEM -> peer (DSMEM),
+//              as soon as it is computed.  Distributed shared memory moves
+//              ~40 GB/s per SM with ~0.3 us latency on this part, so sending
+//              runs as its own pipeline stage, ahead of the softmax; the
+//              softmax adds the peer's partial when it reads its own.
 //   warps 12-15 converter (FP8 caches and gathers): raw rows -> bf16 operand
 //              tile bf16(fp32(e4m3 * scale)) in the 128-byte swizzled layout
 //
@@ -110,6 +110,12 @@ __device__ __forceinline__ void bar_arrive(uint64_t* b) {
 }
 __device__ __forceinline__ void bar_arrive_remote(uint32_t remote_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_addr)
+               : "memory");
+}
+// Remote arrive without release semantics: for signals whose only ordering
+// requirement is on loads whose values are already consumed in registers.
+__device__ __forceinline__ void bar_arrive_remote_relaxed(uint32_t remote_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_addr)
                : "memory");
 }
 __device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes) {
@@ -233,7 +239,7 @@ __device__ __forceinline__ uint32_t swz_chunk(int row, int chunk) {
 // Shared state of the CTA (barriers, flags) at the tail of shared memory.
 struct Bars {
   uint64_t full[4], deq[4], empty[4];
-  uint64_t sfull[2], sready[2], sfree[2], pfull[2], pfree[2], xfull[2], xempty[2];
+  uint64_t sfull[2], sfree[2], pfull[2], pfree[2], xfull[2], xempty[2];
   uint64_t drain;   // final commit of the MMA issuer
   uint64_t qbar;    // query rows staged in shared memory
   uint32_t tmem;
@@ -314,8 +320,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       bar_init(&bars->sfull[b], 1);
-      bar_init(&bars->sready[b], 4);
-      bar_init(&bars->sfree[b], 4);
+      bar_init(&bars->sfree[b], 8);   // softmax and exchange warps both read S
       bar_init(&bars->pfull[b], 4);
       bar_init(&bars->pfree[b], 1);
       bar_init(&bars->xfull[b], 4);
@@ -431,6 +436,23 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       long idle = 0;
       while (np < ntiles && !bars->abort) {
         bool did = false;
+        // PV first: it is on the critical path (the softmax waits for it), and
+        // issuing the 18 QK instructions takes about as long as running them
+        if (np < nq) {
+          const int i = np, j = i % C::kStages, b = i & 1;
+          if (bar_try(&bars->pfull[b], (i >> 1) & 1)) {
+            tc_after();
+            const uint32_t pa = sa(pbuf(b)), va = sa(opl(j));
+#pragma unroll
+            for (int kk = 0; kk < kN / 16; ++kk)
+              mma_ss(tmem + kTmemO, sdesc(pa + 32 * kk, 16, 1024),
+                     sdesc(va + 2048 * kk, kBlkBytes, 1024), id_pv, (i > 0 || kk > 0) ? 1 : 0);
+            mma_commit(&bars->pfree[b]);
+            mma_commit(&bars->empty[j]);
+            ++np;
+            did = true;
+          }
+        }
         if (nq < ntiles && nq < np + 3) {
           const int k = nq, j = k % C::kStages, b = k & 1;
           const uint32_t use = k / C::kStages;
@@ -451,21 +473,6 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
             did = true;
           }
         }
-        if (np < nq) {
-          const int i = np, j = i % C::kStages, b = i & 1;
-          if (bar_try(&bars->pfull[b], (i >> 1) & 1)) {
-            tc_after();
-            const uint32_t pa = sa(pbuf(b)), va = sa(opl(j));
-#pragma unroll
-            for (int kk = 0; kk < kN / 16; ++kk)
-              mma_ss(tmem + kTmemO, sdesc(pa + 32 * kk, 16, 1024),
-                     sdesc(va + 2048 * kk, kBlkBytes, 1024), id_pv, (i > 0 || kk > 0) ? 1 : 0);
-            mma_commit(&bars->pfree[b]);
-            mma_commit(&bars->empty[j]);
-            ++np;
-            did = true;
-          }
-        }
         if (did) {
           idle = 0;
         } else if (++idle > kSpinLimit) {
@@ -479,15 +486,14 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     }
   } else if (warp >= 8 && warp < 12) {
     // ------------------------------------------------------------ exchange
-    // The own partial is re-read from TMEM when finishing (it stays there
-    // until the softmax has read the full sum), so no registers are held
-    // across the transfer.
+    // Send only: partial S of tile i -> peer's exchange buffer i&1 (a warp
+    // writes 512 contiguous bytes per store), then release the S buffer.
     const int h = threadIdx.x - 256;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    auto send = [&](int k) -> bool {
-      const int b = k & 1;
-      const uint32_t use2 = (k >> 1) & 1;
-      if (!wt.wait(&bars->sfull[b], use2)) return false;
+    for (int i = 0; i < ntiles; ++i) {
+      const int b = i & 1;
+      const uint32_t use2 = (i >> 1) & 1;
+      if (!wt.wait(&bars->sfull[b], use2)) break;
       tc_after();
       const uint32_t sb = lane_base + (b ? kTmemS1 : kTmemS0);
       uint32_t r0[16], r1[16], r2[16];
@@ -495,7 +501,10 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       TC_LD16(sb + 16, r1);
       TC_LD16(sb + 32, r2);
       tc_wait_ld();
-      if (!wt.wait(&bars->xempty[b], use2 ^ 1)) return false;
+      tc_before();
+      __syncwarp();
+      if (lane == 0) bar_arrive(&bars->sfree[b]);
+      if (!wt.wait(&bars->xempty[b], use2 ^ 1)) break;
       const uint32_t xd = mapa(xbuf(b) + 4 * h, peer);
 #pragma unroll
       for (int c = 0; c < kN / 4; ++c) {
@@ -506,48 +515,6 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) bar_arrive_remote(mapa(&bars->xfull[b], peer));
-      return true;
-    };
-    auto finish = [&](int k) -> bool {
-      const int b = k & 1;
-      const uint32_t use2 = (k >> 1) & 1;
-      if (!wt.wait(&bars->xfull[b], use2)) return false;
-      tc_after();
-      const uint32_t sb = lane_base + (b ? kTmemS1 : kTmemS0);
-      uint32_t r0[16], r1[16], r2[16];
-      TC_LD16(sb, r0);
-      TC_LD16(sb + 16, r1);
-      TC_LD16(sb + 32, r2);
-      tc_wait_ld();
-      const float4* xr = reinterpret_cast<const float4*>(xbuf(b)) + h;
-#pragma unroll
-      for (int c = 0; c < kN / 4; ++c) {
-        const float4 v = xr[128 * c];
-        uint32_t* d = c < 4 ? r0 + 4 * c : (c < 8 ? r1 + 4 * (c - 4) : r2 + 4 * (c - 8));
-        d[0] = __float_as_uint(__uint_as_float(d[0]) + v.x);
-        d[1] = __float_as_uint(__uint_as_float(d[1]) + v.y);
-        d[2] = __float_as_uint(__uint_as_float(d[2]) + v.z);
-        d[3] = __float_as_uint(__uint_as_float(d[3]) + v.w);
-      }
-      TC_ST16(sb, r0);
-      TC_ST16(sb + 16, r1);
-      TC_ST16(sb + 32, r2);
-      tc_wait_st();
-      tc_before();
-      __syncwarp();
-      if (lane == 0) {
-        bar_arrive_remote(mapa(&bars->xempty[b], peer));   // my buffer b may be refilled
-        bar_arrive(&bars->sready[b]);
-      }
-      return true;
-    };
-    // One tile at a time: sending tile i+1 before finishing tile i would make
-    // the finish wait for QK of tile i+1, which itself waits for the softmax
-    // of tile i-1 (two score buffers), lengthening the critical cycle.
-    bool ok = true;
-    for (int i = 0; i < ntiles && ok; ++i) {
-      ok = send(i);
-      if (ok) ok = finish(i);
     }
   } else if (warp >= 4 && warp < 8) {
     // ------------------------------------------------------------ softmax
@@ -560,7 +527,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       const int j = i % C::kStages, b = i & 1;
       const uint32_t use2 = (i >> 1) & 1;
       float sc[kN];
-      ok = ok && wt.wait(&bars->sready[b], use2);
+      ok = ok && wt.wait(&bars->sfull[b], use2);
       {
         tc_after();
         const uint32_t sb = lane_base + (b ? kTmemS1 : kTmemS0);
@@ -578,6 +545,20 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         tc_before();
         __syncwarp();
         if (lane == 0) bar_arrive(&bars->sfree[b]);   // QK of tile i+2 may overwrite
+      }
+      // + the peer's partial (fp32 addition commutes: both CTAs get the same S)
+      ok = ok && wt.wait(&bars->xfull[b], use2);
+      {
+        const float4* xr = reinterpret_cast<const float4*>(xbuf(b)) + h;
+#pragma unroll
+        for (int c = 0; c < kN / 4; ++c) {
+          const float4 v = xr[128 * c];
+          sc[4 * c] += v.x; sc[4 * c + 1] += v.y; sc[4 * c + 2] += v.z; sc[4 * c + 3] += v.w;
+        }
+        __syncwarp();
+        // my buffer b may be refilled: the values read above are already in
+        // registers, so no release ordering is needed
+        if (lane == 0) bar_arrive_remote_relaxed(mapa(&bars->xempty[b], peer));
       }
       // masked, scaled scores; lazy rescale of the running reference max
       const int valid = min(kN, u.t1 - (u.t0 + i * kN));
