@@ -216,7 +216,11 @@ MLA_API mla_status mla_decode_noalloc(const mla_cache* cache, const void* q_late
  * the graph ran.  mla_trace_end synchronises on the last event and returns
  * the summed kernel time in milliseconds, the number of timed launches and
  * the number of kernel launches.  Events are created by begin and destroyed
- * by end.
+ * by end.  max_records = 0 counts launches without recording events (an
+ * event between two kernels also ends their programmatic launch overlap, so
+ * a launch count of a timed run is best taken this way).  Returns
+ * MLA_ERR_INVALID_ARG if tracing is already on or max_records is outside
+ * [0, 2^20].
  */
 MLA_API mla_status mla_trace_begin(int32_t max_records);
 MLA_API mla_status mla_trace_end(float* main_kernel_ms, int32_t* timed_launches,

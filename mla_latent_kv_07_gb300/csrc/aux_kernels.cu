@@ -26,6 +26,8 @@ __device__ __forceinline__ float warp_max(float v) {
 // e4m3 of x / scale with round-to-nearest-even and saturation.
 template <bool kDevicePos>
 __global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
+  pdl_wait();   // earlier kernels may still read the cache rows written here
+  pdl_trigger();
   const int b = blockIdx.x;
   int row;
   if (kDevicePos) {
@@ -108,6 +110,8 @@ __global__ void __launch_bounds__(1024) sparse_prep_kernel(const int* __restrict
                                                           int* gidx_out, int* gcount_out) {
   extern __shared__ int sv[];
   __shared__ int scan_smem[33];
+  pdl_wait();
+  pdl_trigger();
   const int b = blockIdx.x;
   int T = end_pos[b];
   if (T < 0 || T > max_end_pos) {
@@ -160,16 +164,23 @@ __global__ void __launch_bounds__(1024) sparse_prep_kernel(const int* __restrict
 }
 
 // --------------------------------------------------------------- schedule
-// Single CTA.  lengths[b] (dense: clamped end_pos; sparse: gather count) is
-// cut into units of `chunk` positions, chunk = ceil(total / target) rounded up
-// to the kernel's tile granule, so sum_b ceil(len_b / chunk) <= target + B.
+// Single CTA of 32 x ceil(B / 32) threads (at most 1024).  lengths[b] (dense:
+// clamped end_pos; sparse: gather count) is cut into units of `chunk`
+// positions, chunk = ceil(total / target) rounded up to the kernel's tile
+// granule and grown until sum_b ceil(len_b / chunk) <= target.
 __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ end_pos,
                                                        int max_end_pos, Workspace ws, int B,
                                                        int target, int granule) {
   __shared__ int scan_smem[33];
   __shared__ unsigned long long total_len;
-  if (threadIdx.x == 0) total_len = 0;
+  __shared__ int count_smem;
+  pdl_wait();   // the previous call's kernels may still read this workspace
+  if (threadIdx.x == 0) {
+    total_len = 0;
+    if (end_pos) *ws.status = 0u;   // dense: first kernel of the call
+  }
   __syncthreads();
+  pdl_trigger();
   const int per = (B + blockDim.x - 1) / blockDim.x;
   const int b0 = threadIdx.x * per;
   unsigned long long mine = 0;
@@ -194,7 +205,6 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
   long long chunk = ((long long)total_len + target - 1) / target;
   chunk = ((chunk + granule - 1) / granule) * granule;
   if (chunk < granule) chunk = granule;
-  __shared__ int count_smem;
   int nmine = 0;
   for (int iter = 0; iter < 64; ++iter) {
     nmine = 0;
@@ -231,26 +241,48 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
 
 // ---------------------------------------------------------------- combine
 // One CTA per (h, b); 128 threads x 4 latent columns.  out = sum_i w_i O_i,
-// w_i = exp(lse_i - lse), lse = log sum_i exp(lse_i).
+// w_i = exp(lse_i - lse), lse = log sum_i exp(lse_i).  The partial rows are
+// fetched eight units at a time, loads first, so their latencies overlap.
 __global__ void __launch_bounds__(128) combine_kernel(Workspace ws, int H,
                                                      __nv_bfloat16* __restrict__ out,
                                                      float* __restrict__ lse_out) {
+  pdl_wait();
+  pdl_trigger();
   const int h = blockIdx.x, b = blockIdx.y;
   const int2 sq = ws.seq[b];
+  const int n = sq.y;
   const int c = threadIdx.x * 4;
+  const float* pl = ws.part_lse + (size_t)sq.x * H + h;            // unit stride H
+  const float* po = ws.part_o + ((size_t)sq.x * H + h) * kDc + c;  // unit stride H * 512
+  const size_t ostride = (size_t)H * kDc;
+  float m = -INFINITY;
+  for (int i = threadIdx.x & 31; i < n; i += 32) m = fmaxf(m, pl[(size_t)i * H]);
+  m = warp_max(m);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lse = -INFINITY;
-  if (sq.y > 0) {
-    float m = -INFINITY;
-    for (int i = 0; i < sq.y; ++i) m = fmaxf(m, ws.part_lse[(size_t)(sq.x + i) * H + h]);
-    float wsum = 0.f;
-    for (int i = 0; i < sq.y; ++i) {
-      const size_t u = (size_t)(sq.x + i);
-      const float w = expf(ws.part_lse[u * H + h] - m);
-      const float4 o = *reinterpret_cast<const float4*>(ws.part_o + (u * H + h) * kDc + c);
-      acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
-      wsum += w;
+  float wsum = 0.f;
+  if (m > -INFINITY) {
+    for (int i0 = 0; i0 < n; i0 += 8) {
+      float4 o[8];
+      float l[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (i0 + k < n) {
+          o[k] = *reinterpret_cast<const float4*>(po + (size_t)(i0 + k) * ostride);
+          l[k] = pl[(size_t)(i0 + k) * H];
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        if (i0 + k < n) {
+          const float w = expf(l[k] - m);
+          acc.x += w * o[k].x; acc.y += w * o[k].y; acc.z += w * o[k].z; acc.w += w * o[k].w;
+          wsum += w;
+        }
+      }
     }
+  }
+  float lse = -INFINITY;
+  if (wsum > 0.f) {
     const float inv = 1.0f / wsum;
     acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv;
     lse = m + logf(wsum);
@@ -267,13 +299,11 @@ __global__ void __launch_bounds__(128) combine_kernel(Workspace ws, int H,
 }  // namespace
 
 cudaError_t launch_append_host_pos(const AppendParams& p, cudaStream_t s) {
-  append_kernel<false><<<p.B, 128, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(append_kernel<false>, dim3(p.B), dim3(128), 0, s, p);
 }
 
 cudaError_t launch_append_device_pos(const AppendParams& p, cudaStream_t s) {
-  append_kernel<true><<<p.B, 128, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(append_kernel<true>, dim3(p.B), dim3(128), 0, s, p);
 }
 
 cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int max_end_pos,
@@ -284,21 +314,21 @@ cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int m
   size_t smem = sizeof(int) * (size_t)Kpad;
   cudaError_t e = ensure_smem<sparse_prep_kernel>(sizeof(int) * (size_t)mla::kMaxTopK);
   if (e != cudaSuccess) return e;
-  sparse_prep_kernel<<<B, 1024, smem, s>>>(topk, K, Kpad, end_pos, max_end_pos, ws, gidx_out,
-                                           gcount_out);
-  return cudaGetLastError();
+  return launch_pdl(sparse_prep_kernel, dim3(B), dim3(1024), smem, s, topk, K, Kpad, end_pos,
+                    max_end_pos, ws, gidx_out, gcount_out);
 }
 
 cudaError_t launch_schedule(const int* end_pos, int max_end_pos, const Workspace& ws, int B,
                             int target, int granule, cudaStream_t s) {
-  schedule_kernel<<<1, 1024, 0, s>>>(end_pos, max_end_pos, ws, B, target, granule);
-  return cudaGetLastError();
+  const int threads = B >= 1024 ? 1024 : ((B + 31) / 32) * 32;
+  return launch_pdl(schedule_kernel, dim3(1), dim3(threads), 0, s, end_pos, max_end_pos, ws, B,
+                    target, granule);
 }
 
 cudaError_t launch_combine(const Workspace& ws, int B, int H, void* out, float* lse,
                            cudaStream_t s) {
-  combine_kernel<<<dim3(H, B), 128, 0, s>>>(ws, H, static_cast<__nv_bfloat16*>(out), lse);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(H, B), dim3(128), 0, s, ws, H,
+                    static_cast<__nv_bfloat16*>(out), lse);
 }
 
 }  // namespace mla

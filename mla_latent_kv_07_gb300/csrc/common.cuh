@@ -1,10 +1,12 @@
-// common.cuh -- constants, parameter blocks and the workspace layout shared by
-// the host API (mla_api.cu) and the kernels.  No kernel code lives here.
+// common.cuh -- constants, parameter blocks, the workspace layout and the
+// launch helper shared by the host API (mla_api.cu) and the kernels.
 #pragma once
 
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
+
+#include <utility>
 
 namespace mla {
 
@@ -126,14 +128,45 @@ cudaError_t ensure_smem(size_t bytes) {
   return e;
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// programmatic stream serialisation, so its CTAs may start while the kernel
+// before it in the stream is finishing.  Each kernel calls pdl_wait() before
+// its first access to global memory that an earlier kernel may write or read
+// (griddepcontrol.wait returns once the previous grid has completed and its
+// writes are visible), then pdl_trigger() so the next kernel may begin to
+// launch.  The data dependencies stay those of plain stream order; what
+// overlaps is launch latency and per-CTA set-up.  Launched without the
+// attribute, both instructions are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // Launchers (defined in the kernel translation units).
 cudaError_t launch_append_host_pos(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_append_device_pos(const AppendParams& p, cudaStream_t s);
 cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int max_end_pos,
                                const Workspace& ws, int B, int* gidx_out, int* gcount_out,
                                cudaStream_t s);
-// end_pos != nullptr: dense (lengths = clamped end_pos); nullptr: the
-// lengths were already written (sparse prep).
+// end_pos != nullptr: dense (lengths = clamped end_pos, and the schedule is the
+// first kernel of the call, so it clears the status word); nullptr: the
+// lengths were already written (sparse prep) and the status word cleared.
 cudaError_t launch_schedule(const int* end_pos, int max_end_pos, const Workspace& ws, int B,
                             int target_units, int granule, cudaStream_t s);
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s);
@@ -142,6 +175,9 @@ int decode_mma_granule();
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s);
 int decode_tc_granule();
 bool decode_tc_supported(int H);
+// units for one wave of the pair kernel: min(SMs / 2, CTA pairs that can be
+// resident at once), which the GPU's cluster placement may hold below SMs / 2
+int decode_tc_units(int fmt, bool sparse, int num_sms);
 cudaError_t launch_combine(const Workspace& ws, int B, int H, void* out, float* lse,
                            cudaStream_t s);
 

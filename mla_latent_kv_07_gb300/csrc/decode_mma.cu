@@ -158,6 +158,8 @@ template <int kFmt, bool kSparse>
 __global__ void __launch_bounds__(kThreads) decode_mma_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>(smem_raw);
+  pdl_wait();   // the schedule of this call is complete
+  pdl_trigger();
   const Unit u = p.ws.units[blockIdx.x];
   if (u.b < 0) return;
   const int hg = blockIdx.y;            // head group
@@ -295,8 +297,7 @@ cudaError_t launch_variant(const DecodeParams& p, cudaStream_t s) {
   cudaError_t e = ensure_smem<decode_mma_kernel<kFmt, kSparse>>(smem);
   if (e != cudaSuccess) return e;
   dim3 grid(p.ws.max_units, p.H / kHeads);
-  decode_mma_kernel<kFmt, kSparse><<<grid, kThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(decode_mma_kernel<kFmt, kSparse>, grid, dim3(kThreads), smem, s, p);
 }
 
 }  // namespace

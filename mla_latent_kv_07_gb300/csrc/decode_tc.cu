@@ -69,7 +69,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between resca
 constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemS0 = 400, kTmemS1 = 448;
 constexpr long kSpinLimit = 1L << 26;   // polls (~seconds) before giving up
 constexpr int kQRow = 576 + 16;   // staged query row (bytes), padded against bank conflicts
-constexpr int kORow = 512 + 16;   // staged half-output row (128 fp32), padded
+constexpr int kORow = 1024 + 16;  // staged output row (256 fp32), padded
 
 template <int kFmt, bool kSparse>
 struct Cfg {
@@ -88,7 +88,8 @@ struct Cfg {
   static constexpr int kSmem = kBarOff + 1024 + 1024;      // barriers/flags + base alignment slack
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kStage % 1024 == 0 && kOplBytes % 1024 == 0, "1 KB alignment of swizzled tiles");
-  static_assert(kStagesBytes >= 128 * kQRow && kStagesBytes >= 128 * kORow, "staging fits the stages");
+  static_assert(kStagesBytes >= 128 * kQRow, "query staging fits the stages");
+  static_assert(kBarOff >= 128 * kORow, "output staging fits the stages, P and exchange buffers");
 };
 
 struct TcParams {
@@ -293,13 +294,10 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(sm + C::kBarOff);
 
   const int unit_id = blockIdx.x >> 1;
-  const Unit u = p.ws.units[unit_id];
-  if (u.b < 0) return;  // both CTAs of the cluster read the same unit
   uint32_t rank;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
   const uint32_t peer = rank ^ 1u;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ntiles = (u.t1 - u.t0 + kN - 1) / kN;
   Waiter wt{bars, p.ws.status};
 
   auto stage_base = [&](int j) { return sm + j * C::kStage; };
@@ -342,10 +340,18 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   const uint32_t tmem = bars->tmem;
   cluster_sync();  // the peer's barriers are initialised before any remote arrive
 
+  // The set-up above may overlap the previous kernel; from here on this
+  // call's schedule (and everything before it in the stream) is complete.
+  pdl_wait();
+  pdl_trigger();
+  const Unit u = p.ws.units[unit_id];
+  const bool live = u.b >= 0;   // both CTAs of the cluster read the same unit
+  const int ntiles = live ? (u.t1 - u.t0 + kN - 1) / kN : 0;
+
   // Q half -> tensor memory (A operand of QK): lane h, 2 bf16 per column.
   // All 128 rows are bulk-copied into (still unused) stage memory at once,
   // then each thread moves its row to its TMEM lane.
-  if (warp >= 4 && warp < 8) {
+  if (live && warp >= 4 && warp < 8) {
     const int h = threadIdx.x - 128;
     const size_t qrow = (size_t)u.b * p.H + h;
     uint8_t* qs = sm + h * kQRow;
@@ -636,22 +642,22 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       if (lane == 0) bar_arrive(&bars->pfull[b]);
     }
     // ------------------------------------------------------------ epilogue
-    if (ntiles > 0) ok = ok && wt.wait(&bars->pfree[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1);
-    tc_after();
-    // O half (128 heads x 256) -> workspace, normalised by l: staged through
-    // the (now idle) stage memory in two 128-column halves, one bulk store
-    // of 512 bytes per head row
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    float* po = p.ws.part_o + ((size_t)unit_id * p.H + h) * kDc + rank * kHalf;
-    uint8_t* orow = sm + h * kORow;
+    if (live) {
+      if (ntiles > 0) ok = ok && wt.wait(&bars->pfree[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1);
+      tc_after();
+      // O half (128 heads x 256 fp32) -> workspace, normalised by l.  With the
+      // last PV complete, every stage, P and exchange buffer is idle (the peer
+      // sent its last partial before this CTA's last softmax step), so the
+      // whole half is staged at once, one padded 1 KB row per head, and
+      // leaves as one bulk store per row.
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      float* po = p.ws.part_o + ((size_t)unit_id * p.H + h) * kDc + rank * kHalf;
+      uint8_t* orow = sm + h * kORow;
 #pragma unroll 1
-    for (int half = 0; half < 2; ++half) {
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kHalf / 32; ++c) {
         uint32_t r[16], q[16];
-        const uint32_t col = kTmemO + 128 * half + 32 * c;
-        TC_LD16(lane_base + col, r);
-        TC_LD16(lane_base + col + 16, q);
+        TC_LD16(lane_base + kTmemO + 32 * c, r);
+        TC_LD16(lane_base + kTmemO + 32 * c + 16, q);
         tc_wait_ld();
         float4* dst = reinterpret_cast<float4*>(orow + 128 * c);
 #pragma unroll
@@ -663,14 +669,13 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         }
       }
       fence_async_smem();
-      bulk_store(po + 128 * half, orow, 512);
+      bulk_store(po, orow, kHalf * 4);
       bulk_commit();
-      bulk_wait_read();   // the staging row is reused by the second half
+      if (rank == 0)
+        p.ws.part_lse[(size_t)unit_id * p.H + h] =
+            (ok && l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+      bulk_wait_all();
     }
-    bulk_wait_all();
-    if (rank == 0)
-      p.ws.part_lse[(size_t)unit_id * p.H + h] =
-          (ok && l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
   } else if (C::kConv && warp >= 12) {
     // ------------------------------------------------------------ converter
     const int t = threadIdx.x - 384;
@@ -756,28 +761,73 @@ bool encode3(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base
 }
 
 template <int kFmt, bool kSparse>
-cudaError_t launch_tc_variant(const TcParams& tp, cudaStream_t s) {
+void fill_launch(cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr, int grid, cudaStream_t s) {
   using C = Cfg<kFmt, kSparse>;
-  cudaError_t e = ensure_smem<decode_tc_kernel<kFmt, kSparse>>(C::kSmem);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2 * tp.p.ws.max_units);
-  cfg.blockDim = dim3(C::kThreads);
-  cfg.dynamicSmemBytes = C::kSmem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  *cfg = {};
+  cfg->gridDim = dim3(grid);
+  cfg->blockDim = dim3(C::kThreads);
+  cfg->dynamicSmemBytes = C::kSmem;
+  cfg->stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg->attrs = attr;
+  cfg->numAttrs = 2;
+}
+
+template <int kFmt, bool kSparse>
+cudaError_t launch_tc_variant(const TcParams& tp, cudaStream_t s) {
+  using C = Cfg<kFmt, kSparse>;
+  cudaError_t e = ensure_smem<decode_tc_kernel<kFmt, kSparse>>(C::kSmem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[2];
+  fill_launch<kFmt, kSparse>(&cfg, attr, 2 * tp.p.ws.max_units, s);
   return cudaLaunchKernelEx(&cfg, decode_tc_kernel<kFmt, kSparse>, tp);
+}
+
+// CTA pairs of this variant that can be resident at once on the current
+// device (cached per device); 0 if the query fails.
+template <int kFmt, bool kSparse>
+int resident_pairs() {
+  static std::mutex mu;
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return 0;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] == 0) {
+    using C = Cfg<kFmt, kSparse>;
+    int n = 0;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[2];
+    fill_launch<kFmt, kSparse>(&cfg, attr, 2, nullptr);
+    cfg.numAttrs = 1;   // the cluster shape alone decides residency
+    if (ensure_smem<decode_tc_kernel<kFmt, kSparse>>(C::kSmem) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, decode_tc_kernel<kFmt, kSparse>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    cache[dev] = n > 0 ? n : -1;
+  }
+  return cache[dev] > 0 ? cache[dev] : 0;
 }
 
 }  // namespace
 
 int decode_tc_granule() { return kN; }
+
+int decode_tc_units(int fmt, bool sparse, int num_sms) {
+  const int n = fmt == 0 ? (sparse ? resident_pairs<0, true>() : resident_pairs<0, false>())
+                         : (sparse ? resident_pairs<1, true>() : resident_pairs<1, false>());
+  const int half = num_sms / 2;
+  return n > 0 && n < half ? n : half;
+}
 
 bool decode_tc_supported(int H) { return H == 128 && get_encoder() != nullptr; }
 

@@ -150,7 +150,7 @@ mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cuda
   const bool tc = use_tc_path(a.H);
   cudaError_t e = mla::launch_schedule(
       K ? nullptr : a.end_pos, a.max_end_pos, ws, a.B,
-      tc ? mla::target_units_tc(sms) : mla::target_units_mma(a.H, sms),
+      tc ? mla::decode_tc_units(a.cache->fmt, K > 0, sms) : mla::target_units_mma(a.H, sms),
       tc ? mla::decode_tc_granule() : mla::decode_mma_granule(), s);
   if (e != cudaSuccess) return cuda_fail(e, "schedule");
   const bool traced = trace_start(s);
@@ -212,10 +212,8 @@ mla_status mla_decode(const mla_cache* cache, const void* q_latent, const void* 
   mla::Workspace ws;
   mla_status st = check_decode(a, 0, &ws);
   if (st != MLA_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws.status, 0, 16, s);
-  if (e != cudaSuccess) return cuda_fail(e, "memset");
-  return run_decode(a, ws, 0, s);
+  // the schedule kernel, first of the dense call, clears the status word
+  return run_decode(a, ws, 0, static_cast<cudaStream_t>(stream));
 }
 
 mla_status mla_decode_sparse(const mla_cache* cache, const void* q_latent, const void* q_pe,
@@ -284,11 +282,13 @@ const char* mla_status_string(mla_status status) {
 const char* mla_last_error(void) { return g_last_error; }
 
 mla_status mla_trace_begin(int32_t max_records) {
-  if (g_trace.on || max_records <= 0 || max_records > (1 << 20)) return MLA_ERR_INVALID_ARG;
+  if (g_trace.on || max_records < 0 || max_records > (1 << 20)) return MLA_ERR_INVALID_ARG;
   Trace t;
   t.cap = max_records;
-  t.ev = new (std::nothrow) cudaEvent_t[2 * (size_t)max_records];
-  if (!t.ev) return MLA_ERR_INVALID_ARG;
+  if (max_records > 0) {
+    t.ev = new (std::nothrow) cudaEvent_t[2 * (size_t)max_records];
+    if (!t.ev) return MLA_ERR_INVALID_ARG;
+  }
   for (int i = 0; i < 2 * max_records; ++i) {
     cudaError_t e = cudaEventCreate(&t.ev[i]);
     if (e != cudaSuccess) {
@@ -318,7 +318,7 @@ mla_status mla_trace_end(float* main_kernel_ms, int32_t* timed_launches, int32_t
     if (e != cudaSuccess) st = cuda_fail(e, "trace_end");
   }
   for (int i = 0; i < 2 * t.cap; ++i) cudaEventDestroy(t.ev[i]);
-  delete[] t.ev;
+  delete[] t.ev;   // null when only launches were counted
   if (main_kernel_ms) *main_kernel_ms = (float)total;
   if (timed_launches) *timed_launches = t.n;
   if (kernel_launches) *kernel_launches = t.launches;

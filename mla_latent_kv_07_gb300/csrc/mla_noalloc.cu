@@ -17,8 +17,8 @@
 // calls cudaMalloc, cudaFree or any allocating routine.
 //
 // Every call uses the same array and leaves its contents behind; the status
-// word is cleared at the start of each call and every other region is written
-// before it is read.  Calls whose work overlaps on the GPU (different streams,
+// word is cleared by the first kernel of each call and every other region is
+// written before it is read.  Calls whose work overlaps on the GPU (different streams,
 // or different host threads without ordering) race on the array: order them.
 #include <mutex>
 
@@ -113,11 +113,12 @@ mla_status mla_decode_noalloc(const mla_cache* c, const void* q_latent, const vo
   p.K = 0;
 
   const bool tc = mla::decode_tc_supported(H);
-  cudaError_t e = cudaMemsetAsync(ws.status, 0, 16, s);   // the only region read before written
-  if (e == cudaSuccess)
-    e = mla::launch_schedule(end_pos, max_end_pos, ws, B,
-                             tc ? mla::target_units_tc(sms) : mla::target_units_mma(H, sms),
-                             tc ? mla::decode_tc_granule() : mla::decode_mma_granule(), s);
+  // the schedule kernel clears the status word, the only region read before
+  // it is written
+  cudaError_t e = mla::launch_schedule(
+      end_pos, max_end_pos, ws, B,
+      tc ? mla::decode_tc_units(c->fmt, false, sms) : mla::target_units_mma(H, sms),
+      tc ? mla::decode_tc_granule() : mla::decode_mma_granule(), s);
   if (e == cudaSuccess) e = tc ? mla::launch_decode_tc(p, s) : mla::launch_decode_mma(p, s);
   if (e == cudaSuccess) e = mla::launch_combine(ws, B, H, out, lse, s);
   if (e != cudaSuccess) {

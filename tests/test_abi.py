@@ -109,3 +109,18 @@ def test_workspace_size_rejects_bad_arguments(L):
     assert L.mla_workspace_size(4, 24, 64, 0) == 0
     assert L.mla_workspace_size(4, 128, 64, -1) == 0
     assert L.mla_workspace_size(4, 128, 64, 9000) == 0
+
+
+def test_trace_counts_launches_without_events(L):
+    # max_records = 0 only counts launches: no events are created, so this
+    # needs no GPU; a second begin while tracing is on, and a negative count,
+    # are refused
+    assert L.mla_trace_begin(-1) == 1
+    assert L.mla_trace_begin(0) == 0
+    try:
+        assert L.mla_trace_begin(0) == 1
+    finally:
+        ms, n, k = ctypes.c_float(1.0), ctypes.c_int32(1), ctypes.c_int32(1)
+        assert L.mla_trace_end(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(k)) == 0
+    assert (ms.value, n.value, k.value) == (0.0, 0, 0)
+    assert L.mla_trace_end(None, None, None) == 1   # not tracing
