@@ -68,8 +68,7 @@ constexpr int kXBytes = (kN / 4) * 128 * 16;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
 constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemS0 = 400, kTmemS1 = 448;
 constexpr long kSpinLimit = 1L << 26;   // polls (~seconds) before giving up
-constexpr int kQRow = 576 + 16;   // staged query row (bytes), padded against bank conflicts
-constexpr int kORow = 1024 + 16;  // staged output row (256 fp32), padded
+constexpr int kSwBlk = 128 * 128;         // one 128-row x 128-byte swizzled block: 16 KB
 
 template <int kFmt, bool kSparse>
 struct Cfg {
@@ -88,8 +87,11 @@ struct Cfg {
   static constexpr int kSmem = kBarOff + 1024 + 1024;      // barriers/flags + base alignment slack
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kStage % 1024 == 0 && kOplBytes % 1024 == 0, "1 KB alignment of swizzled tiles");
-  static_assert(kStagesBytes >= 128 * kQRow, "query staging fits the stages");
-  static_assert(kBarOff >= 128 * kORow, "output staging fits the stages, P and exchange buffers");
+  // the query is staged in the P and exchange buffers (5 swizzled blocks), the
+  // output half in the stage memory onwards (8 blocks of 32 fp32 columns)
+  static_assert(2 * kPBytes + 2 * kXBytes >= 5 * kSwBlk, "query staging fits P and X");
+  static_assert(kPOff % 1024 == 0, "1 KB alignment of the query staging");
+  static_assert(kBarOff >= 8 * kSwBlk, "output staging fits the stages, P and exchange buffers");
 };
 
 struct TcParams {
@@ -97,6 +99,9 @@ struct TcParams {
   CUtensorMap m_kv;   // bf16: latent (box 64 x 48), FP8: codes (box 256 x 48)
   CUtensorMap m_pe;   // rotary (box 64 x 48, 128-byte swizzle)
   CUtensorMap m_sc;   // FP8 scales (box 4 x 48)
+  CUtensorMap m_ql;   // q_latent [B][128][512] (box 64 x 128, 128-byte swizzle)
+  CUtensorMap m_qp;   // q_pe [B][128][64] (box 64 x 128, 128-byte swizzle)
+  CUtensorMap m_po;   // partial outputs [units][128][512] fp32 (box 32 x 128, 128-byte swizzle)
 };
 
 // ------------------------------------------------------------------ PTX
@@ -210,6 +215,13 @@ __device__ __forceinline__ void tma3(void* dst, const CUtensorMap* m, int c0, in
       "l"(m), "r"(c0), "r"(c1), "r"(c2), "r"(sa(bar))
       : "memory");
 }
+__device__ __forceinline__ void tma3_store(const CUtensorMap* m, int c0, int c1, int c2,
+                                           const void* src) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(m),
+      "r"(c0), "r"(c1), "r"(c2), "r"(sa(src))
+      : "memory");
+}
 __device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -224,9 +236,6 @@ __device__ __forceinline__ void bulk_store(void* gdst, const void* src, uint32_t
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // named barrier 1 among the 128 softmax threads
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
@@ -243,6 +252,7 @@ struct Bars {
   uint64_t sfull[2], sfree[2], pfull[2], pfree[2], xfull[2], xempty[2];
   uint64_t drain;   // final commit of the MMA issuer
   uint64_t qbar;    // query rows staged in shared memory
+  uint64_t qready;  // query half in tensor memory
   uint32_t tmem;
   volatile int abort;
 };
@@ -326,6 +336,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     }
     bar_init(&bars->drain, 1);
     bar_init(&bars->qbar, 1);
+    bar_init(&bars->qready, 4);
     bars->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -349,36 +360,45 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   const int ntiles = live ? (u.t1 - u.t0 + kN - 1) / kN : 0;
 
   // Q half -> tensor memory (A operand of QK): lane h, 2 bf16 per column.
-  // All 128 rows are bulk-copied into (still unused) stage memory at once,
-  // then each thread moves its row to its TMEM lane.
+  // Five TMA boxes stage the 128 rows (4 latent blocks of 64 columns, the 64
+  // rotary columns, 128-byte swizzled) in the P and exchange buffers, which
+  // are idle until the first tile, so the producer starts on the cache at
+  // once.  Each thread then moves its row to its TMEM lane and signals the MMA
+  // issuer, and the peer that its exchange buffers may be written.
   if (live && warp >= 4 && warp < 8) {
     const int h = threadIdx.x - 128;
-    const size_t qrow = (size_t)u.b * p.H + h;
-    uint8_t* qs = sm + h * kQRow;
-    if (h == 0) bar_expect_tx(&bars->qbar, 128 * (kHalf * 2 + kPeHalf * 2));
-    softmax_sync();
-    bulk_copy(qs, static_cast<const __nv_bfloat16*>(p.q_latent) + qrow * kDc + rank * kHalf,
-              kHalf * 2, &bars->qbar);
-    bulk_copy(qs + kHalf * 2, static_cast<const __nv_bfloat16*>(p.q_pe) + qrow * kDr + rank * kPeHalf,
-              kPeHalf * 2, &bars->qbar);
+    uint8_t* qs = sm + C::kPOff;
+    if (h == 0) {
+      bar_expect_tx(&bars->qbar, 5 * kSwBlk);
+      for (int blk = 0; blk < 4; ++blk)
+        tma3(qs + blk * kSwBlk, &tp.m_ql, rank * kHalf + blk * 64, 0, u.b, &bars->qbar);
+      tma3(qs + 4 * kSwBlk, &tp.m_qp, 0, 0, u.b, &bars->qbar);
+    }
     wt.drain(&bars->qbar, 0);
-    const uint4* qv = reinterpret_cast<const uint4*>(qs);
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
 #pragma unroll
-    for (int c = 0; c < 9; ++c) {  // 144 columns = 9 x 16
+    for (int c = 0; c < 9; ++c) {  // 144 columns = 9 x 16 = 36 chunks of 16 bytes
       uint32_t r[16];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        const uint4 v = qv[c * 4 + k];
+        const int q = 4 * c + k;   // chunk of this CTA's 288-column half row
+        const uint8_t* src = q < 32 ? qs + (q >> 3) * kSwBlk + swz_chunk(h, q & 7)
+                                    : qs + 4 * kSwBlk + swz_chunk(h, (q - 32) + 4 * (int)rank);
+        const uint4 v = *reinterpret_cast<const uint4*>(src);
         r[4 * k] = v.x; r[4 * k + 1] = v.y; r[4 * k + 2] = v.z; r[4 * k + 3] = v.w;
       }
       TC_ST16(lane_base + kTmemQ + 16 * c, r);
     }
     tc_wait_st();
+    tc_before();
+    __syncwarp();
+    if (lane == 0) {
+      bar_arrive(&bars->qready);
+      // phase 0 of the peer's xempty[0/1]: this CTA's exchange buffers are free
+      bar_arrive_remote(mapa(&bars->xempty[0], peer));
+      bar_arrive_remote(mapa(&bars->xempty[1], peer));
+    }
   }
-  tc_before();
-  __syncthreads();
-  tc_after();
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -440,6 +460,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       constexpr uint32_t id_pv = idesc(128, kHalf, true);
       int nq = 0, np = 0;
       long idle = 0;
+      if (live && wt.wait(&bars->qready, 0)) tc_after();
       while (np < ntiles && !bars->abort) {
         bool did = false;
         // PV first: it is on the critical path (the softmax waits for it), and
@@ -510,7 +531,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       tc_before();
       __syncwarp();
       if (lane == 0) bar_arrive(&bars->sfree[b]);
-      if (!wt.wait(&bars->xempty[b], use2 ^ 1)) break;
+      if (!wt.wait(&bars->xempty[b], use2)) break;   // phase 0: the peer's query staging is done
       const uint32_t xd = mapa(xbuf(b) + 4 * h, peer);
 #pragma unroll
       for (int c = 0; c < kN / 4; ++c) {
@@ -648,33 +669,37 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       // O half (128 heads x 256 fp32) -> workspace, normalised by l.  With the
       // last PV complete, every stage, P and exchange buffer is idle (the peer
       // sent its last partial before this CTA's last softmax step), so the
-      // whole half is staged at once, one padded 1 KB row per head, and
-      // leaves as one bulk store per row.
+      // whole half is staged at once as 8 swizzled blocks of 32 columns and
+      // leaves as 8 TMA stores.
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      float* po = p.ws.part_o + ((size_t)unit_id * p.H + h) * kDc + rank * kHalf;
-      uint8_t* orow = sm + h * kORow;
 #pragma unroll 1
       for (int c = 0; c < kHalf / 32; ++c) {
         uint32_t r[16], q[16];
         TC_LD16(lane_base + kTmemO + 32 * c, r);
         TC_LD16(lane_base + kTmemO + 32 * c + 16, q);
         tc_wait_ld();
-        float4* dst = reinterpret_cast<float4*>(orow + 128 * c);
+        uint8_t* blk = sm + c * kSwBlk;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          dst[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
-                               __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
-          dst[4 + k] = make_float4(__uint_as_float(q[4 * k]) * inv, __uint_as_float(q[4 * k + 1]) * inv,
-                                   __uint_as_float(q[4 * k + 2]) * inv, __uint_as_float(q[4 * k + 3]) * inv);
+          *reinterpret_cast<float4*>(blk + swz_chunk(h, k)) =
+              make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
+                          __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
+          *reinterpret_cast<float4*>(blk + swz_chunk(h, 4 + k)) =
+              make_float4(__uint_as_float(q[4 * k]) * inv, __uint_as_float(q[4 * k + 1]) * inv,
+                          __uint_as_float(q[4 * k + 2]) * inv, __uint_as_float(q[4 * k + 3]) * inv);
         }
       }
       fence_async_smem();
-      bulk_store(po, orow, kHalf * 4);
-      bulk_commit();
+      softmax_sync();
+      if (h == 0) {
+        for (int c = 0; c < kHalf / 32; ++c)
+          tma3_store(&tp.m_po, rank * kHalf + 32 * c, 0, unit_id, sm + c * kSwBlk);
+        bulk_commit();
+      }
       if (rank == 0)
         p.ws.part_lse[(size_t)unit_id * p.H + h] =
             (ok && l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
-      bulk_wait_all();
+      if (h == 0) bulk_wait_all();
     }
   } else if (C::kConv && warp >= 12) {
     // ------------------------------------------------------------ converter
@@ -749,12 +774,12 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
 }
 
 bool encode3(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
-             uint64_t S, uint64_t B, uint32_t box0, CUtensorMapSwizzle sw) {
+             uint64_t S, uint64_t B, uint32_t box0, CUtensorMapSwizzle sw, uint32_t box1 = kN) {
   auto enc = get_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {inner, S, B};
   cuuint64_t strides[2] = {inner * esize, inner * esize * S};
-  cuuint32_t box[3] = {box0, (cuuint32_t)kN, 1};
+  cuuint32_t box[3] = {box0, box1, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
              sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -850,6 +875,13 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s) {
     ok = ok && encode3(&tp.m_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.pe, kDr, S, B, 64,
                        CU_TENSOR_MAP_SWIZZLE_128B);
   }
+  ok = ok &&
+       encode3(&tp.m_ql, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.q_latent, kDc, 128, B, 64,
+               CU_TENSOR_MAP_SWIZZLE_128B, 128) &&
+       encode3(&tp.m_qp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.q_pe, kDr, 128, B, 64,
+               CU_TENSOR_MAP_SWIZZLE_128B, 128) &&
+       encode3(&tp.m_po, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.ws.part_o, kDc, 128,
+               (uint64_t)p.ws.max_units, 32, CU_TENSOR_MAP_SWIZZLE_128B, 128);
   if (!ok) return cudaErrorInvalidValue;
   if (p.fmt == 0) return p.K ? launch_tc_variant<0, true>(tp, s) : launch_tc_variant<0, false>(tp, s);
   return p.K ? launch_tc_variant<1, true>(tp, s) : launch_tc_variant<1, false>(tp, s);
