@@ -173,7 +173,7 @@ cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s);
 int decode_mma_granule();
 // tensor-memory path (H = 128): one CTA pair per unit
 cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s);
-int decode_tc_granule();
+int decode_tc_granule(int fmt, bool sparse);   // positions per tile of the variant
 bool decode_tc_supported(int H);
 // units for one wave of the pair kernel: min(SMs / 2, CTA pairs that can be
 // resident at once), which the GPU's cluster placement may hold below SMs / 2

@@ -55,50 +55,61 @@
 namespace mla {
 namespace {
 
-constexpr int kN = 48;                     // positions per tile (MMA N for QK, K for PV)
 constexpr int kHalf = kDc / 2;             // 256 latent columns per CTA
 constexpr int kPeHalf = kDr / 2;           // 32 rotary columns per CTA
-constexpr int kBlkBytes = kN * 128;        // one 64-column swizzled block of a tile: 6 KB
-constexpr int kOplBytes = 4 * kBlkBytes;   // latent half operand: 24 KB
-constexpr int kOpeBytes = kBlkBytes;       // rotary operand (full 64 columns): 6 KB
-constexpr int kPBytes = 128 * 128;         // P: 128 heads x 64 (48 used) bf16, swizzled
-// exchange buffer: float4 chunk c (positions 4c..4c+3) of head h at index
-// c * 128 + h, so a warp's remote store is one contiguous 512-byte run
-constexpr int kXBytes = (kN / 4) * 128 * 16;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
-constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemS0 = 400, kTmemS1 = 448;
+constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemS = 400;
 constexpr long kSpinLimit = 1L << 26;   // polls (~seconds) before giving up
 constexpr int kSwBlk = 128 * 128;         // one 128-row x 128-byte swizzled block: 16 KB
 
+// Shared-memory plan per variant.  Tiles are 48 positions (MMA N for QK, K
+// for PV), with two S, P and exchange buffers.  An operand stage holds the
+// swizzled bf16 latent half and rotary tile the MMAs read; it is taken from
+// the load (dense bf16) or the conversion (FP8, gathers) of its tile until
+// PV of that tile completes.  Variants with a converter load the rows as
+// stored -- FP8 codes or gathered bf16 half rows, the 4 FP8 scales of each
+// row, the 64 rotary values -- into a separate ring of raw slots, which the
+// converter frees as soon as it has read them.  So a load never waits for a
+// PV, and the HBM latency stays out of the operand stages' cycle.
 template <int kFmt, bool kSparse>
 struct Cfg {
   static constexpr bool kConv = kFmt == 1 || kSparse;       // converter warps present
+  static constexpr int kN = 48;    // positions per tile
+  static constexpr int kBufs = 2;  // S, P and exchange buffers
   static constexpr int kThreads = kConv ? 512 : 384;
+  static constexpr int kBlkBytes = kN * 128;       // one 64-column swizzled block of a tile
+  static constexpr int kOplBytes = 4 * kBlkBytes;  // latent half operand
+  static constexpr int kOpeBytes = kBlkBytes;      // rotary operand (full 64 columns)
+  static constexpr int kPBytes = ((kN + 63) / 64) * kSwBlk;  // P: 128 heads x kN bf16, swizzled
+  // exchange buffer: float4 chunk c (positions 4c..4c+3) of head h at index
+  // c * 128 + h, so a warp's remote store is one contiguous 512-byte run
+  static constexpr int kXBytes = (kN / 4) * 128 * 16;
+  static constexpr int kStage = kOplBytes + kOpeBytes;
+  static constexpr int kStages = kConv ? (kFmt == 1 ? 3 : 2) : 4;
   static constexpr int kRawRow = kFmt == 1 ? kHalf : kHalf * 2;  // bytes of a raw latent half row
-  static constexpr int kRawBytes = kConv ? kN * kRawRow : 0;
   static constexpr int kScBytes = kFmt == 1 ? 1024 : 0;          // 48 x 16 B, padded
-  static constexpr int kRpeBytes = kSparse ? kN * 128 : 0;
-  static constexpr int kStage = kOplBytes + kOpeBytes + kRawBytes + kScBytes + kRpeBytes;
-  static constexpr int kStages = kSparse ? 2 : (kFmt == 1 ? 3 : 4);
-  static constexpr int kStagesBytes = kStages * kStage;
-  static constexpr int kPOff = kStagesBytes;
-  static constexpr int kXOff = kPOff + 2 * kPBytes;
-  static constexpr int kBarOff = kXOff + 2 * kXBytes;
+  static constexpr int kRaw = kConv ? kN * kRawRow + kScBytes + kN * 128 : 0;
+  static constexpr int kRawSlots = kConv ? 2 : 0;
+  static constexpr int kRawOff = kStages * kStage;
+  static constexpr int kPOff = kRawOff + kRawSlots * kRaw;
+  static constexpr int kXOff = kPOff + kBufs * kPBytes;
+  static constexpr int kBarOff = kXOff + kBufs * kXBytes;
   static constexpr int kSmem = kBarOff + 1024 + 1024;      // barriers/flags + base alignment slack
   static_assert(kSmem <= 232448, "shared memory budget");
-  static_assert(kStage % 1024 == 0 && kOplBytes % 1024 == 0, "1 KB alignment of swizzled tiles");
+  static_assert(kStage % 1024 == 0 && kRaw % 1024 == 0, "1 KB alignment of swizzled tiles");
+  static_assert(kN % 16 == 0 && kTmemS + kBufs * kN <= 512, "tile width");
   // the query is staged in the P and exchange buffers (5 swizzled blocks), the
-  // output half in the stage memory onwards (8 blocks of 32 fp32 columns)
-  static_assert(2 * kPBytes + 2 * kXBytes >= 5 * kSwBlk, "query staging fits P and X");
+  // output half from offset 0 (8 blocks of 32 fp32 columns)
+  static_assert(kBufs * (kPBytes + kXBytes) >= 5 * kSwBlk, "query staging fits P and X");
   static_assert(kPOff % 1024 == 0, "1 KB alignment of the query staging");
-  static_assert(kBarOff >= 8 * kSwBlk, "output staging fits the stages, P and exchange buffers");
+  static_assert(kBarOff >= 8 * kSwBlk, "output staging fits the idle buffers");
 };
 
 struct TcParams {
   DecodeParams p;
-  CUtensorMap m_kv;   // bf16: latent (box 64 x 48), FP8: codes (box 256 x 48)
-  CUtensorMap m_pe;   // rotary (box 64 x 48, 128-byte swizzle)
-  CUtensorMap m_sc;   // FP8 scales (box 4 x 48)
+  CUtensorMap m_kv;   // bf16: latent (box 64 x N), FP8: codes (box 256 x N)
+  CUtensorMap m_pe;   // rotary (box 64 x N, 128-byte swizzle)
+  CUtensorMap m_sc;   // FP8 scales (box 4 x N)
   CUtensorMap m_ql;   // q_latent [B][128][512] (box 64 x 128, 128-byte swizzle)
   CUtensorMap m_qp;   // q_pe [B][128][64] (box 64 x 128, 128-byte swizzle)
   CUtensorMap m_po;   // partial outputs [units][128][512] fp32 (box 32 x 128, 128-byte swizzle)
@@ -236,7 +247,11 @@ __device__ __forceinline__ void bulk_store(void* gdst, const void* src, uint32_t
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// the bulk stores of this thread have read their shared-memory sources (their
+// global writes complete with the grid)
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 // named barrier 1 among the 128 softmax threads
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -248,7 +263,10 @@ __device__ __forceinline__ uint32_t swz_chunk(int row, int chunk) {
 
 // Shared state of the CTA (barriers, flags) at the tail of shared memory.
 struct Bars {
-  uint64_t full[4], deq[4], empty[4];
+  uint64_t full[4];    // tile landed: stage (dense bf16) or raw slot
+  uint64_t deq[4];     // operand stage converted
+  uint64_t empty[4];   // PV done: operand stage free
+  uint64_t rfree[2];   // raw slot read by the converter
   uint64_t sfull[2], sfree[2], pfull[2], pfree[2], xfull[2], xempty[2];
   uint64_t drain;   // final commit of the MMA issuer
   uint64_t qbar;    // query rows staged in shared memory
@@ -256,6 +274,7 @@ struct Bars {
   uint32_t tmem;
   volatile int abort;
 };
+static_assert(sizeof(Bars) <= 1024, "barrier block");
 
 struct Waiter {
   Bars* bars;
@@ -294,10 +313,35 @@ __device__ __forceinline__ void dequant16(uint4 v, float sc, uint4& lo, uint4& h
   hi = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// Epilogue: O columns [32 c0, 32 c1) of TMEM lane h, times inv, into the
+// 128-byte swizzled output blocks c0..c1-1 (16 KB each) at `out`.
+__device__ __forceinline__ void stage_output(uint32_t lane_base, uint8_t* out, int h, float inv,
+                                             int c0, int c1) {
+#pragma unroll 1
+  for (int c = c0; c < c1; ++c) {
+    uint32_t r[16], q[16];
+    TC_LD16(lane_base + kTmemO + 32 * c, r);
+    TC_LD16(lane_base + kTmemO + 32 * c + 16, q);
+    tc_wait_ld();
+    uint8_t* blk = out + c * kSwBlk;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      *reinterpret_cast<float4*>(blk + swz_chunk(h, k)) =
+          make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
+                      __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
+      *reinterpret_cast<float4*>(blk + swz_chunk(h, 4 + k)) =
+          make_float4(__uint_as_float(q[4 * k]) * inv, __uint_as_float(q[4 * k + 1]) * inv,
+                      __uint_as_float(q[4 * k + 2]) * inv, __uint_as_float(q[4 * k + 3]) * inv);
+    }
+  }
+}
+
 template <int kFmt, bool kSparse>
 __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     decode_tc_kernel(const __grid_constant__ TcParams tp) {
   using C = Cfg<kFmt, kSparse>;
+  constexpr int kN = C::kN, kBlkBytes = C::kBlkBytes, kOplBytes = C::kOplBytes,
+                kOpeBytes = C::kOpeBytes;
   const DecodeParams& p = tp.p;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -310,14 +354,17 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Waiter wt{bars, p.ws.status};
 
-  auto stage_base = [&](int j) { return sm + j * C::kStage; };
-  auto opl = [&](int j) { return stage_base(j); };
-  auto ope = [&](int j) { return stage_base(j) + kOplBytes; };
-  auto raw = [&](int j) { return stage_base(j) + kOplBytes + kOpeBytes; };
-  auto rsc = [&](int j) { return stage_base(j) + kOplBytes + kOpeBytes + C::kRawBytes; };
-  auto rpe = [&](int j) { return stage_base(j) + kOplBytes + kOpeBytes + C::kRawBytes + C::kScBytes; };
-  auto pbuf = [&](int b) { return sm + C::kPOff + b * kPBytes; };
-  auto xbuf = [&](int b) { return reinterpret_cast<float*>(sm + C::kXOff + b * kXBytes); };
+  auto opl = [&](int j) { return sm + j * C::kStage; };               // operand stage j
+  auto ope = [&](int j) { return sm + j * C::kStage + kOplBytes; };
+  auto raw = [&](int r) { return sm + C::kRawOff + r * C::kRaw; };    // raw slot r
+  auto rsc = [&](int r) { return raw(r) + kN * C::kRawRow; };
+  auto rpe = [&](int r) { return raw(r) + kN * C::kRawRow + C::kScBytes; };
+  auto pbuf = [&](int b) { return sm + C::kPOff + b * C::kPBytes; };
+  auto xbuf = [&](int b) { return reinterpret_cast<float*>(sm + C::kXOff + b * C::kXBytes); };
+  // tile i uses S, P and exchange buffer bsel(i); bpar(i) is the parity of
+  // the phase that tile completes on that buffer's barriers
+  auto bsel = [](int i) { return i % C::kBufs; };
+  auto bpar = [](int i) { return (uint32_t)((i / C::kBufs) & 1); };
 
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
@@ -326,6 +373,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       bar_init(&bars->deq[j], 4);
       bar_init(&bars->empty[j], 1);
     }
+    for (int r = 0; r < 2; ++r) bar_init(&bars->rfree[r], 4);
     for (int b = 0; b < 2; ++b) {
       bar_init(&bars->sfull[b], 1);
       bar_init(&bars->sfree[b], 8);   // softmax and exchange warps both read S
@@ -402,11 +450,15 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
+    // dense bf16: tile i lands swizzled in operand stage i % kStages, once PV
+    // of its previous tile is done; converter variants: in raw slot
+    // i % kRawSlots, once the converter has read its previous tile
+    constexpr int kSlots = C::kConv ? C::kRawSlots : C::kStages;
     int issued = 0;
     for (int i = 0; i < ntiles && !bars->abort; ++i) {
-      const int j = i % C::kStages;
-      const uint32_t use = i / C::kStages;
-      if (!wt.wait(&bars->empty[j], (use & 1) ^ 1)) break;
+      const int j = i % kSlots;
+      const uint32_t use = i / kSlots;
+      if (!wt.wait(C::kConv ? &bars->rfree[j] : &bars->empty[j], (use & 1) ^ 1)) break;
       const int e0 = u.t0 + i * kN;
       if (!kSparse) {
         if (lane == 0) {
@@ -414,12 +466,13 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
             bar_expect_tx(&bars->full[j], kOplBytes + kOpeBytes);
             for (int blk = 0; blk < 4; ++blk)
               tma3(opl(j) + blk * kBlkBytes, &tp.m_kv, rank * kHalf + blk * 64, e0, u.b, &bars->full[j]);
+            tma3(ope(j), &tp.m_pe, 0, e0, u.b, &bars->full[j]);
           } else {
-            bar_expect_tx(&bars->full[j], kN * kHalf + kN * 16 + kOpeBytes);
+            bar_expect_tx(&bars->full[j], kN * kHalf + kN * 16 + kN * 128);
             tma3(raw(j), &tp.m_kv, rank * kHalf, e0, u.b, &bars->full[j]);
             tma3(rsc(j), &tp.m_sc, 0, e0, u.b, &bars->full[j]);
+            tma3(rpe(j), &tp.m_pe, 0, e0, u.b, &bars->full[j]);
           }
-          tma3(ope(j), &tp.m_pe, 0, e0, u.b, &bars->full[j]);
         }
       } else {
         const int v = min(kN, u.t1 - e0);
@@ -446,15 +499,15 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     // copies still in flight must land before this CTA's shared memory goes
     // away; on the normal path every stage was already consumed
     if (lane == 0 && bars->abort) {
-      for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
-        wt.drain(&bars->full[i % C::kStages], (i / C::kStages) & 1);
+      for (int i = issued > kSlots ? issued - kSlots : 0; i < issued; ++i)
+        wt.drain(&bars->full[i % kSlots], (i / kSlots) & 1);
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer
     // Event-driven: QK of the next tile is issued as soon as its stage, its
-    // converted operand and its S buffer are ready (at most two tiles ahead
-    // of PV: the S buffers are double); PV of the next tile as soon as its P
-    // is written.  Neither waits behind the other's inputs.
+    // converted operand and its S buffer are ready (at most kBufs tiles ahead
+    // of the softmax); PV of the next tile as soon as its P is written.
+    // Neither waits behind the other's inputs.
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc(128, kN, false);
       constexpr uint32_t id_pv = idesc(128, kHalf, true);
@@ -466,13 +519,13 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         // PV first: it is on the critical path (the softmax waits for it), and
         // issuing the 18 QK instructions takes about as long as running them
         if (np < nq) {
-          const int i = np, j = i % C::kStages, b = i & 1;
-          if (bar_try(&bars->pfull[b], (i >> 1) & 1)) {
+          const int i = np, j = i % C::kStages, b = bsel(i);
+          if (bar_try(&bars->pfull[b], bpar(i))) {
             tc_after();
             const uint32_t pa = sa(pbuf(b)), va = sa(opl(j));
 #pragma unroll
             for (int kk = 0; kk < kN / 16; ++kk)
-              mma_ss(tmem + kTmemO, sdesc(pa + 32 * kk, 16, 1024),
+              mma_ss(tmem + kTmemO, sdesc(pa + (kk >> 2) * kSwBlk + (kk & 3) * 32, 16, 1024),
                      sdesc(va + 2048 * kk, kBlkBytes, 1024), id_pv, (i > 0 || kk > 0) ? 1 : 0);
             mma_commit(&bars->pfree[b]);
             mma_commit(&bars->empty[j]);
@@ -481,12 +534,12 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           }
         }
         if (nq < ntiles && nq < np + 3) {
-          const int k = nq, j = k % C::kStages, b = k & 1;
+          const int k = nq, j = k % C::kStages, b = bsel(k);
           const uint32_t use = k / C::kStages;
-          if (bar_try(&bars->full[j], use & 1) && (!C::kConv || bar_try(&bars->deq[j], use & 1)) &&
-              bar_try(&bars->sfree[b], ((k >> 1) & 1) ^ 1)) {
+          if (bar_try(C::kConv ? &bars->deq[j] : &bars->full[j], use & 1) &&
+              bar_try(&bars->sfree[b], bpar(k) ^ 1)) {
             tc_after();
-            const uint32_t sd = tmem + (b ? kTmemS1 : kTmemS0);
+            const uint32_t sd = tmem + kTmemS + b * kN;
             const uint32_t la = sa(opl(j)), pe = sa(ope(j)) + rank * (kPeHalf * 2);
 #pragma unroll
             for (int kk = 0; kk < kHalf / 16; ++kk)
@@ -513,33 +566,29 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     }
   } else if (warp >= 8 && warp < 12) {
     // ------------------------------------------------------------ exchange
-    // Send only: partial S of tile i -> peer's exchange buffer i&1 (a warp
-    // writes 512 contiguous bytes per store), then release the S buffer.
+    // Send only: partial S of tile i -> the peer's exchange buffer (a warp
+    // writes 512 contiguous bytes per store), after releasing the S buffer.
     const int h = threadIdx.x - 256;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     for (int i = 0; i < ntiles; ++i) {
-      const int b = i & 1;
-      const uint32_t use2 = (i >> 1) & 1;
-      if (!wt.wait(&bars->sfull[b], use2)) break;
+      const int b = bsel(i);
+      if (!wt.wait(&bars->sfull[b], bpar(i))) break;
       tc_after();
-      const uint32_t sb = lane_base + (b ? kTmemS1 : kTmemS0);
-      uint32_t r0[16], r1[16], r2[16];
-      TC_LD16(sb, r0);
-      TC_LD16(sb + 16, r1);
-      TC_LD16(sb + 32, r2);
+      const uint32_t sb = lane_base + kTmemS + b * kN;
+      uint32_t r[kN];
+#pragma unroll
+      for (int c = 0; c < kN / 16; ++c) TC_LD16(sb + 16 * c, (r + 16 * c));
       tc_wait_ld();
       tc_before();
       __syncwarp();
       if (lane == 0) bar_arrive(&bars->sfree[b]);
-      if (!wt.wait(&bars->xempty[b], use2)) break;   // phase 0: the peer's query staging is done
+      if (!wt.wait(&bars->xempty[b], bpar(i))) break;   // phase 0: the peer's query staging is done
       const uint32_t xd = mapa(xbuf(b) + 4 * h, peer);
 #pragma unroll
-      for (int c = 0; c < kN / 4; ++c) {
-        const uint32_t* src = c < 4 ? r0 + 4 * c : (c < 8 ? r1 + 4 * (c - 4) : r2 + 4 * (c - 8));
+      for (int c = 0; c < kN / 4; ++c)
         asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(xd + 16 * 128 * c),
-                     "r"(src[0]), "r"(src[1]), "r"(src[2]), "r"(src[3])
+                     "r"(r[4 * c]), "r"(r[4 * c + 1]), "r"(r[4 * c + 2]), "r"(r[4 * c + 3])
                      : "memory");
-      }
       __syncwarp();
       if (lane == 0) bar_arrive_remote(mapa(&bars->xfull[b], peer));
     }
@@ -551,30 +600,25 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int i = 0; i < ntiles; ++i) {
-      const int j = i % C::kStages, b = i & 1;
-      const uint32_t use2 = (i >> 1) & 1;
+      const int j = i % C::kStages, b = bsel(i);
+      const uint32_t par = bpar(i);
       float sc[kN];
-      ok = ok && wt.wait(&bars->sfull[b], use2);
+      ok = ok && wt.wait(&bars->sfull[b], par);
       {
         tc_after();
-        const uint32_t sb = lane_base + (b ? kTmemS1 : kTmemS0);
-        uint32_t r0[16], r1[16], r2[16];
-        TC_LD16(sb, r0);
-        TC_LD16(sb + 16, r1);
-        TC_LD16(sb + 32, r2);
+        const uint32_t sb = lane_base + kTmemS + b * kN;
+        uint32_t r[kN];
+#pragma unroll
+        for (int c = 0; c < kN / 16; ++c) TC_LD16(sb + 16 * c, (r + 16 * c));
         tc_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          sc[c] = __uint_as_float(r0[c]);
-          sc[16 + c] = __uint_as_float(r1[c]);
-          sc[32 + c] = __uint_as_float(r2[c]);
-        }
+        for (int c = 0; c < kN; ++c) sc[c] = __uint_as_float(r[c]);
         tc_before();
         __syncwarp();
-        if (lane == 0) bar_arrive(&bars->sfree[b]);   // QK of tile i+2 may overwrite
+        if (lane == 0) bar_arrive(&bars->sfree[b]);   // QK of tile i + kBufs may overwrite
       }
       // + the peer's partial (fp32 addition commutes: both CTAs get the same S)
-      ok = ok && wt.wait(&bars->xfull[b], use2);
+      ok = ok && wt.wait(&bars->xfull[b], par);
       {
         const float4* xr = reinterpret_cast<const float4*>(xbuf(b)) + h;
 #pragma unroll
@@ -593,9 +637,9 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
 #pragma unroll
       for (int c = 0; c < kN; ++c) sc[c] = c < valid ? sc[c] * sl2 : -INFINITY;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        mx[c] = fmaxf(fmaxf(fmaxf(sc[c], sc[c + 8]), fmaxf(sc[c + 16], sc[c + 24])),
-                      fmaxf(sc[c + 32], sc[c + 40]));
+      for (int c = 0; c < 8; ++c) mx[c] = sc[c];
+#pragma unroll
+      for (int c = 8; c < kN; ++c) mx[c & 7] = fmaxf(mx[c & 7], sc[c]);
       const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                              fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const bool need = ok && mt > m_ref + kRescaleThreshold;
@@ -607,7 +651,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           // the previous use of that buffer is known complete, so the parity
           // wait cannot be fooled by a phase two steps back), then scale this
           // lane's row
-          ok = ok && wt.wait(&bars->pfree[(i - 1) & 1], ((i - 1) >> 1) & 1);
+          ok = ok && wt.wait(&bars->pfree[bsel(i - 1)], bpar(i - 1));
           tc_after();
 #pragma unroll 1
           for (int c = 0; c < kHalf / 32; ++c) {
@@ -629,7 +673,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         m_ref = m_new;
       }
       // P row of head h (bf16); l sums the rounded values
-      ok = ok && wt.wait(&bars->pfree[b], use2 ^ 1);
+      ok = ok && wt.wait(&bars->pfree[b], par ^ 1);
       uint8_t* prow = pbuf(b);
       float ls[kN / 8];
 #pragma unroll
@@ -645,9 +689,12 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           pk[k] = *reinterpret_cast<const uint32_t*>(&two);
         }
         ls[c] = part;
-        *reinterpret_cast<uint4*>(prow + swz_chunk(h, c)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        *reinterpret_cast<uint4*>(prow + (c >> 3) * kSwBlk + swz_chunk(h, c & 7)) =
+            make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + (ls[4] + ls[5]);
+#pragma unroll
+      for (int c = 1; c < kN / 8; ++c) ls[0] += ls[c];
+      l += ls[0];
       if (!C::kConv && valid < kN) {
         // dense bf16 tail: rows past the unit hold whatever the cache holds
         // there; zero them so P = 0 never meets a non-finite value
@@ -664,31 +711,14 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     }
     // ------------------------------------------------------------ epilogue
     if (live) {
-      if (ntiles > 0) ok = ok && wt.wait(&bars->pfree[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1);
+      if (ntiles > 0) ok = ok && wt.wait(&bars->pfree[bsel(ntiles - 1)], bpar(ntiles - 1));
       tc_after();
       // O half (128 heads x 256 fp32) -> workspace, normalised by l.  With the
       // last PV complete, every stage, P and exchange buffer is idle (the peer
       // sent its last partial before this CTA's last softmax step), so the
       // whole half is staged at once as 8 swizzled blocks of 32 columns and
       // leaves as 8 TMA stores.
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-#pragma unroll 1
-      for (int c = 0; c < kHalf / 32; ++c) {
-        uint32_t r[16], q[16];
-        TC_LD16(lane_base + kTmemO + 32 * c, r);
-        TC_LD16(lane_base + kTmemO + 32 * c + 16, q);
-        tc_wait_ld();
-        uint8_t* blk = sm + c * kSwBlk;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          *reinterpret_cast<float4*>(blk + swz_chunk(h, k)) =
-              make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
-                          __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
-          *reinterpret_cast<float4*>(blk + swz_chunk(h, 4 + k)) =
-              make_float4(__uint_as_float(q[4 * k]) * inv, __uint_as_float(q[4 * k + 1]) * inv,
-                          __uint_as_float(q[4 * k + 2]) * inv, __uint_as_float(q[4 * k + 3]) * inv);
-        }
-      }
+      stage_output(lane_base, sm, h, l > 0.f ? 1.f / l : 0.f, 0, kHalf / 32);
       fence_async_smem();
       softmax_sync();
       if (h == 0) {
@@ -699,15 +729,17 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       if (rank == 0)
         p.ws.part_lse[(size_t)unit_id * p.H + h] =
             (ok && l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
-      if (h == 0) bulk_wait_all();
+      if (h == 0) bulk_wait_read();
     }
   } else if (C::kConv && warp >= 12) {
     // ------------------------------------------------------------ converter
+    // raw slot r of tile i -> operand stage j, once the rows have landed and
+    // PV of the stage's previous tile is done
     const int t = threadIdx.x - 384;
     for (int i = 0; i < ntiles; ++i) {
-      const int j = i % C::kStages;
-      const uint32_t use = i / C::kStages;
-      if (!wt.wait(&bars->full[j], use & 1)) break;
+      const int r = i % C::kRawSlots, j = i % C::kStages;
+      if (!wt.wait(&bars->full[r], (i / C::kRawSlots) & 1)) break;
+      if (!wt.wait(&bars->empty[j], ((i / C::kStages) & 1) ^ 1)) break;
       const int valid = min(kN, u.t1 - (u.t0 + i * kN));
       uint8_t* dst = opl(j);
       if (kFmt == 1) {
@@ -716,8 +748,8 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           const int row = idx >> 4, q = idx & 15;  // codes [16q, 16q + 16) of the half row
           uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
           if (row < valid) {
-            const uint4 v = *reinterpret_cast<const uint4*>(raw(j) + row * kHalf + q * 16);
-            const float sc = reinterpret_cast<const float*>(rsc(j) + row * 16)[rank * 2 + (q >> 3)];
+            const uint4 v = *reinterpret_cast<const uint4*>(raw(r) + row * kHalf + q * 16);
+            const float sc = reinterpret_cast<const float*>(rsc(r) + row * 16)[rank * 2 + (q >> 3)];
             dequant16(v, sc, lo, hi);
           }
           const int blk = q >> 2, ch = (q & 3) * 2;
@@ -729,22 +761,23 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         for (int idx = t; idx < kN * 32; idx += 128) {
           const int row = idx >> 5, q = idx & 31;
           uint4 v = make_uint4(0, 0, 0, 0);
-          if (row < valid) v = *reinterpret_cast<const uint4*>(raw(j) + row * C::kRawRow + q * 16);
+          if (row < valid) v = *reinterpret_cast<const uint4*>(raw(r) + row * C::kRawRow + q * 16);
           *reinterpret_cast<uint4*>(dst + (q >> 3) * kBlkBytes + swz_chunk(row, q & 7)) = v;
         }
       }
-      if (kSparse) {
-        // rotary rows -> swizzled operand
-        for (int idx = t; idx < kN * 8; idx += 128) {
-          const int row = idx >> 3, q = idx & 7;
-          uint4 v = make_uint4(0, 0, 0, 0);
-          if (row < valid) v = *reinterpret_cast<const uint4*>(rpe(j) + row * 128 + q * 16);
-          *reinterpret_cast<uint4*>(ope(j) + swz_chunk(row, q)) = v;
-        }
+      // rotary rows -> swizzled operand
+      for (int idx = t; idx < kN * 8; idx += 128) {
+        const int row = idx >> 3, q = idx & 7;
+        uint4 v = make_uint4(0, 0, 0, 0);
+        if (row < valid) v = *reinterpret_cast<const uint4*>(rpe(r) + row * 128 + q * 16);
+        *reinterpret_cast<uint4*>(ope(j) + swz_chunk(row, q)) = v;
       }
       fence_async_smem();
       __syncwarp();
-      if (lane == 0) bar_arrive(&bars->deq[j]);
+      if (lane == 0) {
+        bar_arrive(&bars->deq[j]);
+        bar_arrive(&bars->rfree[r]);
+      }
     }
   }
 
@@ -774,7 +807,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encoder() {
 }
 
 bool encode3(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
-             uint64_t S, uint64_t B, uint32_t box0, CUtensorMapSwizzle sw, uint32_t box1 = kN) {
+             uint64_t S, uint64_t B, uint32_t box0, uint32_t box1, CUtensorMapSwizzle sw) {
   auto enc = get_encoder();
   if (!enc) return false;
   cuuint64_t dims[3] = {inner, S, B};
@@ -845,7 +878,10 @@ int resident_pairs() {
 
 }  // namespace
 
-int decode_tc_granule() { return kN; }
+int decode_tc_granule(int fmt, bool sparse) {
+  return fmt == 0 ? (sparse ? Cfg<0, true>::kN : Cfg<0, false>::kN)
+                  : (sparse ? Cfg<1, true>::kN : Cfg<1, false>::kN);
+}
 
 int decode_tc_units(int fmt, bool sparse, int num_sms) {
   const int n = fmt == 0 ? (sparse ? resident_pairs<0, true>() : resident_pairs<0, false>())
@@ -861,27 +897,29 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s) {
   memset(&tp, 0, sizeof(tp));
   tp.p = p;
   const uint64_t S = (uint64_t)p.max_seq_len, B = (uint64_t)p.B;
+  const uint32_t n = (uint32_t)decode_tc_granule(p.fmt, p.K > 0);   // tile rows
   bool ok = true;
   if (!p.K) {
     if (p.fmt == 0) {
-      ok = encode3(&tp.m_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.kv, kDc, S, B, 64,
+      ok = encode3(&tp.m_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.kv, kDc, S, B, 64, n,
                    CU_TENSOR_MAP_SWIZZLE_128B);
     } else {
-      ok = encode3(&tp.m_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.kv, kDc, S, B, kHalf,
+      ok = encode3(&tp.m_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.kv, kDc, S, B, kHalf, n,
                    CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           encode3(&tp.m_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.kv_scale, kNblk, S, B, kNblk,
+           encode3(&tp.m_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.kv_scale, kNblk, S, B, kNblk, n,
                    CU_TENSOR_MAP_SWIZZLE_NONE);
     }
-    ok = ok && encode3(&tp.m_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.pe, kDr, S, B, 64,
-                       CU_TENSOR_MAP_SWIZZLE_128B);
+    // bf16: straight into the operand layout; FP8: plain rows for the converter
+    ok = ok && encode3(&tp.m_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.pe, kDr, S, B, 64, n,
+                       p.fmt == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   ok = ok &&
-       encode3(&tp.m_ql, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.q_latent, kDc, 128, B, 64,
-               CU_TENSOR_MAP_SWIZZLE_128B, 128) &&
-       encode3(&tp.m_qp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.q_pe, kDr, 128, B, 64,
-               CU_TENSOR_MAP_SWIZZLE_128B, 128) &&
+       encode3(&tp.m_ql, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.q_latent, kDc, 128, B, 64, 128,
+               CU_TENSOR_MAP_SWIZZLE_128B) &&
+       encode3(&tp.m_qp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.q_pe, kDr, 128, B, 64, 128,
+               CU_TENSOR_MAP_SWIZZLE_128B) &&
        encode3(&tp.m_po, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.ws.part_o, kDc, 128,
-               (uint64_t)p.ws.max_units, 32, CU_TENSOR_MAP_SWIZZLE_128B, 128);
+               (uint64_t)p.ws.max_units, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   if (p.fmt == 0) return p.K ? launch_tc_variant<0, true>(tp, s) : launch_tc_variant<0, false>(tp, s);
   return p.K ? launch_tc_variant<1, true>(tp, s) : launch_tc_variant<1, false>(tp, s);

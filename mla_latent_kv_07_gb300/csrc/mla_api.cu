@@ -151,7 +151,7 @@ mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cuda
   cudaError_t e = mla::launch_schedule(
       K ? nullptr : a.end_pos, a.max_end_pos, ws, a.B,
       tc ? mla::decode_tc_units(a.cache->fmt, K > 0, sms) : mla::target_units_mma(a.H, sms),
-      tc ? mla::decode_tc_granule() : mla::decode_mma_granule(), s);
+      tc ? mla::decode_tc_granule(a.cache->fmt, K > 0) : mla::decode_mma_granule(), s);
   if (e != cudaSuccess) return cuda_fail(e, "schedule");
   const bool traced = trace_start(s);
   e = tc ? mla::launch_decode_tc(make_params(a, ws, K), s)
