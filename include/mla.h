@@ -163,6 +163,8 @@ MLA_API mla_status mla_decode(const mla_cache* cache, const void* q_latent, cons
  *   gcount_out  NULL, or device int32 [B]: their count
  *   workspace   >= mla_workspace_size(B, H, max_end_pos, K) bytes
  *   other arguments as for mla_decode
+ * The rows are gathered by cache-row index b * max_seq_len + position, an
+ * int32: B * cache->max_seq_len above 2^31 - 1 returns MLA_ERR_UNSUPPORTED.
  */
 MLA_API mla_status mla_decode_sparse(const mla_cache* cache, const void* q_latent, const void* q_pe,
                              const int32_t* end_pos, int32_t max_end_pos, int32_t B, int32_t H,

@@ -1,7 +1,8 @@
 // aux_kernels.cu -- the small kernels around the decode:
 //   append   cache-write step with FP8 block quantisation
 //            ("DeepSeek-V3.2-Exp . KV cache", cache-write excerpt)
-//   prep     top-k list -> sorted, de-duplicated, valid gather list
+//   prep     top-k list -> sorted, de-duplicated, valid gather list (a bitmap
+//            of the sequence's positions)
 //            (same page, MQA-decode excerpt: the index mask is a scatter of
 //            zeros into -inf, so repeats act once and order does not matter)
 //   schedule split every sequence's positions into units of about equal size
@@ -102,13 +103,19 @@ __device__ int block_exclusive_scan(int v, int* smem /* >= 33 ints */, int* tota
 }
 
 // ------------------------------------------------------------ sparse prep
-// One CTA per sequence: invalid entries become INT_MAX, a bitonic sort puts
-// the list in order, repeats are dropped and the survivors compacted.
+// One CTA per sequence.  The positions [0, T) are taken in windows of
+// kPrepWindow: every valid list entry in the window sets its bit in a shared
+// bitmap (repeats set it once), then each thread counts the set bits of its
+// run of words, a block scan turns the counts into output offsets, and the
+// set positions are written in increasing order.  Invalid entries set
+// nothing; the list's tail is -1.
+constexpr int kPrepWindow = 1 << 18;   // positions per pass: a 32 KB bitmap
+
 __global__ void __launch_bounds__(1024) sparse_prep_kernel(const int* __restrict__ topk, int K,
-                                                          int Kpad, const int* __restrict__ end_pos,
+                                                          const int* __restrict__ end_pos,
                                                           int max_end_pos, Workspace ws,
                                                           int* gidx_out, int* gcount_out) {
-  extern __shared__ int sv[];
+  __shared__ uint32_t bm[kPrepWindow / 32];
   __shared__ int scan_smem[33];
   pdl_wait();
   pdl_trigger();
@@ -118,48 +125,46 @@ __global__ void __launch_bounds__(1024) sparse_prep_kernel(const int* __restrict
     if (threadIdx.x == 0) atomicOr(ws.status, kDevEndPosClamped);
     T = T < 0 ? 0 : max_end_pos;
   }
-  for (int k = threadIdx.x; k < Kpad; k += blockDim.x) {
-    int v = k < K ? topk[(size_t)b * K + k] : INT_MAX;
-    sv[k] = (v >= 0 && v < T) ? v : INT_MAX;
-  }
-  __syncthreads();
-  for (int size = 2; size <= Kpad; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < Kpad; i += blockDim.x) {
-        int j = i ^ stride;
-        if (j > i) {
-          bool up = (i & size) == 0;
-          int a = sv[i], c = sv[j];
-          if ((a > c) == up) { sv[i] = c; sv[j] = a; }
-        }
-      }
-      __syncthreads();
-    }
-  }
-  // each thread owns a contiguous run of the sorted list
-  const int per = (Kpad + blockDim.x - 1) / blockDim.x;
-  const int k0 = threadIdx.x * per;
-  int keep = 0;
-  for (int k = k0; k < k0 + per && k < Kpad; ++k)
-    keep += (sv[k] != INT_MAX && (k == 0 || sv[k] != sv[k - 1])) ? 1 : 0;
-  int total;
-  int dst = block_exclusive_scan(keep, scan_smem, &total);
+  const int* list = topk + (size_t)b * K;
   int* g = ws.gidx + (size_t)b * K;
-  for (int k = k0; k < k0 + per && k < Kpad; ++k) {
-    if (sv[k] != INT_MAX && (k == 0 || sv[k] != sv[k - 1])) {
-      g[dst] = sv[k];
-      if (gidx_out) gidx_out[(size_t)b * K + dst] = sv[k];
-      ++dst;
+  int written = 0;
+  for (int base = 0; base < T; base += kPrepWindow) {
+    const int span = min(kPrepWindow, T - base);
+    const int nw = (span + 31) / 32;
+    for (int w = threadIdx.x; w < nw; w += blockDim.x) bm[w] = 0u;
+    __syncthreads();
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+      const int e = list[k];
+      if (e >= base && e - base < span) atomicOr(&bm[(e - base) >> 5], 1u << ((e - base) & 31));
     }
+    __syncthreads();
+    const int per = (nw + blockDim.x - 1) / blockDim.x;
+    const int w0 = threadIdx.x * per;
+    int cnt = 0;
+    for (int w = w0; w < w0 + per && w < nw; ++w) cnt += __popc(bm[w]);
+    int total;
+    int dst = written + block_exclusive_scan(cnt, scan_smem, &total);
+    for (int w = w0; w < w0 + per && w < nw; ++w) {
+      uint32_t bits = bm[w];
+      while (bits) {
+        const int pos = base + 32 * w + __ffs(bits) - 1;
+        bits &= bits - 1u;
+        g[dst] = pos;
+        if (gidx_out) gidx_out[(size_t)b * K + dst] = pos;
+        ++dst;
+      }
+    }
+    written += total;
+    __syncthreads();   // the bitmap is cleared for the next window
   }
-  for (int k = total + threadIdx.x; k < K; k += blockDim.x) {
+  for (int k = written + threadIdx.x; k < K; k += blockDim.x) {
     g[k] = -1;
     if (gidx_out) gidx_out[(size_t)b * K + k] = -1;
   }
   if (threadIdx.x == 0) {
-    ws.gcount[b] = total;
-    ws.lengths[b] = total;
-    if (gcount_out) gcount_out[b] = total;
+    ws.gcount[b] = written;
+    ws.lengths[b] = written;
+    if (gcount_out) gcount_out[b] = written;
   }
 }
 
@@ -309,13 +314,8 @@ cudaError_t launch_append_device_pos(const AppendParams& p, cudaStream_t s) {
 cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int max_end_pos,
                                const Workspace& ws, int B, int* gidx_out, int* gcount_out,
                                cudaStream_t s) {
-  int Kpad = 2;
-  while (Kpad < K) Kpad <<= 1;
-  size_t smem = sizeof(int) * (size_t)Kpad;
-  cudaError_t e = ensure_smem<sparse_prep_kernel>(sizeof(int) * (size_t)mla::kMaxTopK);
-  if (e != cudaSuccess) return e;
-  return launch_pdl(sparse_prep_kernel, dim3(B), dim3(1024), smem, s, topk, K, Kpad, end_pos,
-                    max_end_pos, ws, gidx_out, gcount_out);
+  return launch_pdl(sparse_prep_kernel, dim3(B), dim3(1024), 0, s, topk, K, end_pos, max_end_pos, ws,
+                    gidx_out, gcount_out);
 }
 
 cudaError_t launch_schedule(const int* end_pos, int max_end_pos, const Workspace& ws, int B,

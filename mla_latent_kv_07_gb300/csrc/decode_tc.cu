@@ -87,7 +87,10 @@ struct Cfg {
   static constexpr int kStage = kOplBytes + kOpeBytes;
   static constexpr int kStages = kConv ? (kFmt == 1 ? 3 : 2) : 4;
   static constexpr int kRawRow = kFmt == 1 ? kHalf : kHalf * 2;  // bytes of a raw latent half row
-  static constexpr int kScBytes = kFmt == 1 ? 1024 : 0;          // 48 x 16 B, padded
+  // FP8 scales, 16 B per row: dense tiles land as 48 consecutive rows; a
+  // gather lands 4 rows per 128-byte slot (a tensor copy's shared-memory
+  // destination is 128-byte aligned)
+  static constexpr int kScBytes = kFmt == 1 ? (kSparse ? 2048 : 1024) : 0;
   static constexpr int kRaw = kConv ? kN * kRawRow + kScBytes + kN * 128 : 0;
   static constexpr int kRawSlots = kConv ? 2 : 0;
   static constexpr int kRawOff = kStages * kStage;
@@ -233,14 +236,17 @@ __device__ __forceinline__ void tma3_store(const CUtensorMap* m, int c0, int c1,
       "r"(c0), "r"(c1), "r"(c2), "r"(sa(src))
       : "memory");
 }
-__device__ __forceinline__ void bulk_copy(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+
+// Four rows r0..r3 of a 2D tensor map (box: one row high), columns from c0,
+// stacked at dst; completes on bar.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* m, int c0, int r0, int r1,
+                                            int r2, int r3, uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          sa(dst)),
-      "l"(src), "r"(bytes), "r"(sa(bar))
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(sa(dst)),
+      "l"(m), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(sa(bar))
       : "memory");
 }
-
 __device__ __forceinline__ void bulk_store(void* gdst, const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
                "r"(sa(src)), "r"(bytes)
@@ -475,23 +481,27 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           }
         }
       } else {
+        // gathered rows, four per TMA instruction (tile::gather4 on row-high
+        // boxes): lane g takes rows 4g..4g+3 of the tile -- its latent half,
+        // the FP8 scales, the rotary row -- each landing 128-byte aligned.  A
+        // short last group repeats its last row; the converter ignores rows
+        // past the unit.
         const int v = min(kN, u.t1 - e0);
-        const uint32_t row_bytes = C::kRawRow + (kFmt == 1 ? 16 : 0) + 128;
-        if (lane == 0) bar_expect_tx(&bars->full[j], (uint32_t)v * row_bytes);
+        const int groups = (v + 3) / 4;
+        constexpr uint32_t kGroupBytes = 4 * (C::kRawRow + (kFmt == 1 ? 16 : 0) + 128);
+        if (lane == 0) bar_expect_tx(&bars->full[j], (uint32_t)groups * kGroupBytes);
         __syncwarp();
-        for (int c = lane; c < v; c += 32) {
-          const int pos = p.ws.gidx[(size_t)u.b * p.K + e0 + c];
-          const size_t row = (size_t)u.b * p.max_seq_len + pos;
-          const uint8_t* kvb = static_cast<const uint8_t*>(p.kv);
-          if (kFmt == 1) {
-            bulk_copy(raw(j) + c * C::kRawRow, kvb + row * kDc + rank * kHalf, C::kRawRow, &bars->full[j]);
-            bulk_copy(rsc(j) + c * 16, p.kv_scale + row * kNblk, 16, &bars->full[j]);
-          } else {
-            bulk_copy(raw(j) + c * C::kRawRow, kvb + (row * kDc + rank * kHalf) * 2, C::kRawRow,
+        if (lane < groups) {
+          const int* gl = p.ws.gidx + (size_t)u.b * p.K + e0;
+          const int base = u.b * p.max_seq_len, c = 4 * lane;
+          int r[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) r[k] = base + gl[min(c + k, v - 1)];
+          tma_gather4(raw(j) + c * C::kRawRow, &tp.m_kv, rank * kHalf, r[0], r[1], r[2], r[3],
                       &bars->full[j]);
-          }
-          bulk_copy(rpe(j) + c * 128, static_cast<const uint8_t*>(p.pe) + row * kDr * 2, 128,
-                    &bars->full[j]);
+          if (kFmt == 1)
+            tma_gather4(rsc(j) + lane * 128, &tp.m_sc, 0, r[0], r[1], r[2], r[3], &bars->full[j]);
+          tma_gather4(rpe(j) + c * 128, &tp.m_pe, 0, r[0], r[1], r[2], r[3], &bars->full[j]);
         }
       }
       issued = i + 1;
@@ -749,7 +759,8 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
           if (row < valid) {
             const uint4 v = *reinterpret_cast<const uint4*>(raw(r) + row * kHalf + q * 16);
-            const float sc = reinterpret_cast<const float*>(rsc(r) + row * 16)[rank * 2 + (q >> 3)];
+            const uint8_t* srow = rsc(r) + (kSparse ? (row >> 2) * 128 + (row & 3) * 16 : row * 16);
+            const float sc = reinterpret_cast<const float*>(srow)[rank * 2 + (q >> 3)];
             dequant16(v, sc, lo, hi);
           }
           const int blk = q >> 2, ch = (q & 3) * 2;
@@ -816,6 +827,20 @@ bool encode3(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
              sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2D map over `rows` rows of `inner` elements, box `box0` x 1 row, no swizzle
+bool encode2_rows(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, uint64_t inner,
+                  uint64_t rows, uint32_t box0) {
+  auto enc = get_encoder();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * esize};
+  cuuint32_t box[2] = {box0, 1};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int kFmt, bool kSparse>
@@ -899,7 +924,15 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s) {
   const uint64_t S = (uint64_t)p.max_seq_len, B = (uint64_t)p.B;
   const uint32_t n = (uint32_t)decode_tc_granule(p.fmt, p.K > 0);   // tile rows
   bool ok = true;
-  if (!p.K) {
+  if (p.K) {
+    // gathers: 2D maps over all rows [B * S], one row high, for tile::gather4
+    const uint64_t rows = B * S;
+    ok = encode2_rows(&tp.m_kv, p.fmt == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                      p.fmt == 0 ? 2 : 1, p.kv, kDc, rows, kHalf) &&
+         encode2_rows(&tp.m_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.pe, kDr, rows, kDr) &&
+         (p.fmt == 0 || encode2_rows(&tp.m_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.kv_scale, kNblk,
+                                     rows, kNblk));
+  } else {
     if (p.fmt == 0) {
       ok = encode3(&tp.m_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.kv, kDc, S, B, 64, n,
                    CU_TENSOR_MAP_SWIZZLE_128B);

@@ -224,6 +224,7 @@ mla_status mla_decode_sparse(const mla_cache* cache, const void* q_latent, const
                              size_t ws_bytes, void* stream) {
   g_last_error[0] = 0;
   if (!topk_idx || K <= 0 || K > mla::kMaxTopK || !aligned4(topk_idx)) return MLA_ERR_INVALID_ARG;
+  if (cache && B > 0 && (int64_t)B * cache->max_seq_len > 0x7fffffffLL) return MLA_ERR_UNSUPPORTED;
   if ((kv_new == nullptr) != (pe_new == nullptr)) return MLA_ERR_INVALID_ARG;
   if (kv_new && (!aligned16(kv_new) || !aligned16(pe_new) || B > mla::kMaxAppendB))
     return MLA_ERR_INVALID_ARG;

@@ -102,6 +102,9 @@ def test_sparse_rejects_bad_arguments(L):
     assert sp(K=8193) == 1
     assert sp(topk=None) == 1
     assert sp(kv_new=f, pe_new=None) == 1                   # one of the pair only
+    big = _cache(fmt=1, B=2, S=1 << 30)                     # row index b * S + pos past int32
+    assert L.mla_decode_sparse(ctypes.byref(big), f, f, f, 64, 2, 128, 0.1, f, 2048, None, None,
+                               f, None, None, None, f, 1 << 30, None) == 3
 
 
 def test_workspace_size_rejects_bad_arguments(L):

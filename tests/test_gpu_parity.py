@@ -181,6 +181,39 @@ def test_sparse_fused_append_sees_the_new_row():
     check_close(f64(lse).reshape(-1), ref_lse, "lse")
 
 
+def test_sparse_gather_lists_span_bitmap_windows():
+    # positions past 2^18 and 2^19: the list prep takes the sequence in
+    # windows of 2^18 positions; entries on both sides of each window edge,
+    # at T - 1, at T (invalid), negative, and repeated
+    B, S, H, K = 1, 530000, 128, 1536
+    rng = np.random.default_rng(71)
+    topk = rng.integers(-5, S + 10, (B, K)).astype(np.int32)
+    edges = [0, 262143, 262144, 262145, 524287, 524288, 529999, 530000, -1]
+    topk[0, :len(edges)] = edges
+    topk[0, 20:40] = topk[0, 10]
+    ends = np.array([S], np.int32)
+    # only the rows the list names carry data (the rest stay zero): a small
+    # host footprint for a cache of 530000 positions
+    kv = np.zeros((B, S, 512), np.uint16)
+    pe = np.zeros((B, S, 64), np.uint16)
+    used = np.unique(topk[(topk >= 0) & (topk < S)])
+    kv[0, used] = bits(_rand_bf16((used.size, 512), 72))
+    pe[0, used] = bits(_rand_bf16((used.size, 64), 73))
+    q, sc = orc.quantize_rows(kv)
+    oc = {"fmt": 1, "kv": q, "kv_scale": sc, "pe": pe}
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((B, H, 512), 74), _rand_bf16((B, H, 64), 75)
+    gidx = torch.empty((B, K), dtype=torch.int32, device="cuda")
+    gcnt = torch.empty((B,), dtype=torch.int32, device="cuda")
+    out, lse = mla.decode_sparse(dc, ql.cuda(), qp.cuda(), torch.from_numpy(ends).cuda(), S, 0.12,
+                                 torch.from_numpy(topk).cuda(), gidx=gidx, gcount=gcnt)
+    ref_g, ref_c = orc.sparse_gather_lists(topk, ends)
+    assert np.array_equal(gidx.cpu().numpy(), ref_g) and np.array_equal(gcnt.cpu().numpy(), ref_c)
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), ends, 0.12, topk=topk)
+    check_close(f64(out).reshape(-1, 512), ref, "out")
+    check_close(f64(lse).reshape(-1), ref_lse, "lse")
+
+
 # ------------------------------------------------------ full-size workloads
 
 def _run_dense_workload(w, per_seq):
