@@ -26,11 +26,12 @@
 // Tensor memory (512 columns): O half [0,256) fp32; Q half [256,400) bf16 (2
 // per column); S double buffer [400,448) and [448,496) fp32.
 //
-// Warp roles (384 threads; 512 when a converter is needed):
-//   warp 0  producer: TMA tiles (dense) or per-row bulk copies (gather)
+// Warp roles (512 threads; 640 when a converter is needed):
+//   warp 0  producer: TMA tiles (dense) or four-row TMA gathers (gather)
 //   warp 1  MMA issuer (one thread) and tensor-memory owner
-//   warps 4-7  softmax: thread h <-> head h <-> TMEM lane h; online softmax
-//              (lazy rescale), P, epilogue
+//   warps 4-7 and 12-15 (16-19 with a converter)  softmax: two threads per
+//              head h <-> TMEM lane h, each half of the tile's positions;
+//              online softmax (lazy rescale), P, epilogue
 //   warps 8-11 exchange: partial S of each tile from TMEM -> peer (DSMEM),
 //              as soon as it is computed.  Distributed shared memory moves
 //              ~40 GB/s per SM with ~0.3 us latency on this part, so sending
@@ -76,7 +77,10 @@ struct Cfg {
   static constexpr bool kConv = kFmt == 1 || kSparse;       // converter warps present
   static constexpr int kN = 48;    // positions per tile
   static constexpr int kBufs = 2;  // S, P and exchange buffers
-  static constexpr int kThreads = kConv ? 512 : 384;
+  // warps: 0 producer, 1 MMA, 4-7 softmax (first half), 8-11 exchange,
+  // 12-15 converter (if any), then 4 warps of the softmax's second half
+  static constexpr int kHiWarp = kConv ? 16 : 12;
+  static constexpr int kThreads = 32 * (kHiWarp + 4);
   static constexpr int kBlkBytes = kN * 128;       // one 64-column swizzled block of a tile
   static constexpr int kOplBytes = 4 * kBlkBytes;  // latent half operand
   static constexpr int kOpeBytes = kBlkBytes;      // rotary operand (full 64 columns)
@@ -97,7 +101,7 @@ struct Cfg {
   static constexpr int kPOff = kRawOff + kRawSlots * kRaw;
   static constexpr int kXOff = kPOff + kBufs * kPBytes;
   static constexpr int kBarOff = kXOff + kBufs * kXBytes;
-  static constexpr int kSmem = kBarOff + 1024 + 1024;      // barriers/flags + base alignment slack
+  static constexpr int kSmem = kBarOff + 4096 + 1024;      // barriers/flags + base alignment slack
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kStage % 1024 == 0 && kRaw % 1024 == 0, "1 KB alignment of swizzled tiles");
   static_assert(kN % 16 == 0 && kTmemS + kBufs * kN <= 512, "tile width");
@@ -210,6 +214,11 @@ __device__ __forceinline__ void mma_commit(uint64_t* b) {
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), \
         "=r"(r[14]), "=r"(r[15])                                                                \
       : "r"(taddr))
+#define TC_LD8(taddr, r)                                                                   \
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"    \
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),    \
+                 "=r"(r[6]), "=r"(r[7])                                                    \
+               : "r"(taddr))
 #define TC_ST16(taddr, r)                                                                     \
   asm volatile(                                                                               \
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12," \
@@ -258,8 +267,19 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
-// named barrier 1 among the 128 softmax threads
-__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// named barrier 1 among the 256 softmax threads; barriers 2..5 between the
+// two softmax warps that serve the same 32 heads
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void pair_sync(int q) {
+  asm volatile("bar.sync %0, 64;" ::"r"(2 + q) : "memory");
+}
+// 2^x with the hardware approximation (relative error far below the bf16
+// rounding P receives); 0 for -inf
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 
 // byte offset of 16-byte chunk `chunk` of row `row` in a 128-byte-swizzled block
@@ -279,8 +299,10 @@ struct Bars {
   uint64_t qready;  // query half in tensor memory
   uint32_t tmem;
   volatile int abort;
+  float pair_max[2][256];   // softmax: tile maxima of the pair's halves, by tile parity
+  float l_half[256];        // epilogue: the pair's halves of l
 };
-static_assert(sizeof(Bars) <= 1024, "barrier block");
+static_assert(sizeof(Bars) <= 4096, "barrier block");
 
 struct Waiter {
   Bars* bars;
@@ -382,11 +404,11 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     for (int r = 0; r < 2; ++r) bar_init(&bars->rfree[r], 4);
     for (int b = 0; b < 2; ++b) {
       bar_init(&bars->sfull[b], 1);
-      bar_init(&bars->sfree[b], 8);   // softmax and exchange warps both read S
-      bar_init(&bars->pfull[b], 4);
+      bar_init(&bars->sfree[b], 12);   // softmax (8) and exchange (4) warps read S
+      bar_init(&bars->pfull[b], 8);
       bar_init(&bars->pfree[b], 1);
       bar_init(&bars->xfull[b], 4);
-      bar_init(&bars->xempty[b], 4);
+      bar_init(&bars->xempty[b], 8);   // the peer's softmax warps
     }
     bar_init(&bars->drain, 1);
     bar_init(&bars->qbar, 1);
@@ -452,6 +474,12 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       bar_arrive_remote(mapa(&bars->xempty[0], peer));
       bar_arrive_remote(mapa(&bars->xempty[1], peer));
     }
+  }
+  // the second-half softmax warps count towards that phase too (it completes
+  // only with the first half's arrivals, after the staged rows were read)
+  if (live && warp >= C::kHiWarp && lane == 0) {
+    bar_arrive_remote(mapa(&bars->xempty[0], peer));
+    bar_arrive_remote(mapa(&bars->xempty[1], peer));
   }
 
   if (warp == 0) {
@@ -602,9 +630,16 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       __syncwarp();
       if (lane == 0) bar_arrive_remote(mapa(&bars->xfull[b], peer));
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if ((warp >= 4 && warp < 8) || (warp >= C::kHiWarp && warp < C::kHiWarp + 4)) {
     // ------------------------------------------------------------ softmax
-    const int h = threadIdx.x - 128;
+    // Two threads per head h (TMEM lane h): half sh = 0 takes the tile's
+    // positions [0,16) and [32,40), half 1 [16,32) and [40,48) (16- and
+    // 8-column TMEM loads).  The pair agrees on each tile's maximum through
+    // shared memory and a 64-thread barrier, so both take the same rescale
+    // decisions; each rescales and, at the end, normalises half of the O row.
+    const int sh = warp >= 8 ? 1 : 0;
+    const int h = 32 * (warp & 3) + lane;
+    const int p0 = 16 * sh, p1 = 32 + 8 * sh;   // first position of each run
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY, l = 0.f;
@@ -612,17 +647,17 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     for (int i = 0; i < ntiles; ++i) {
       const int j = i % C::kStages, b = bsel(i);
       const uint32_t par = bpar(i);
-      float sc[kN];
+      float sc[24];
       ok = ok && wt.wait(&bars->sfull[b], par);
       {
         tc_after();
         const uint32_t sb = lane_base + kTmemS + b * kN;
-        uint32_t r[kN];
-#pragma unroll
-        for (int c = 0; c < kN / 16; ++c) TC_LD16(sb + 16 * c, (r + 16 * c));
+        uint32_t r[24];
+        TC_LD16(sb + p0, r);
+        TC_LD8(sb + p1, (r + 16));
         tc_wait_ld();
 #pragma unroll
-        for (int c = 0; c < kN; ++c) sc[c] = __uint_as_float(r[c]);
+        for (int k = 0; k < 24; ++k) sc[k] = __uint_as_float(r[k]);
         tc_before();
         __syncwarp();
         if (lane == 0) bar_arrive(&bars->sfree[b]);   // QK of tile i + kBufs may overwrite
@@ -632,26 +667,28 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       {
         const float4* xr = reinterpret_cast<const float4*>(xbuf(b)) + h;
 #pragma unroll
-        for (int c = 0; c < kN / 4; ++c) {
-          const float4 v = xr[128 * c];
-          sc[4 * c] += v.x; sc[4 * c + 1] += v.y; sc[4 * c + 2] += v.z; sc[4 * c + 3] += v.w;
+        for (int k = 0; k < 6; ++k) {
+          const float4 v = xr[128 * (k < 4 ? p0 / 4 + k : p1 / 4 + k - 4)];
+          sc[4 * k] += v.x; sc[4 * k + 1] += v.y; sc[4 * k + 2] += v.z; sc[4 * k + 3] += v.w;
         }
         __syncwarp();
         // my buffer b may be refilled: the values read above are already in
         // registers, so no release ordering is needed
         if (lane == 0) bar_arrive_remote_relaxed(mapa(&bars->xempty[b], peer));
       }
-      // masked, scaled scores; lazy rescale of the running reference max
+      // masked, scaled scores; the tile maximum of the pair
       const int valid = min(kN, u.t1 - (u.t0 + i * kN));
-      float mx[8];
 #pragma unroll
-      for (int c = 0; c < kN; ++c) sc[c] = c < valid ? sc[c] * sl2 : -INFINITY;
+      for (int k = 0; k < 24; ++k)
+        sc[k] = (k < 16 ? p0 + k : p1 + k - 16) < valid ? sc[k] * sl2 : -INFINITY;
+      float mx[4] = {sc[0], sc[1], sc[2], sc[3]};
 #pragma unroll
-      for (int c = 0; c < 8; ++c) mx[c] = sc[c];
-#pragma unroll
-      for (int c = 8; c < kN; ++c) mx[c & 7] = fmaxf(mx[c & 7], sc[c]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int k = 4; k < 24; ++k) mx[k & 3] = fmaxf(mx[k & 3], sc[k]);
+      float* pm = bars->pair_max[i & 1];
+      pm[sh * 128 + h] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      pair_sync(warp & 3);
+      const float mt = fmaxf(pm[h], pm[128 + h]);
+      // lazy rescale of the running reference max
       const bool need = ok && mt > m_ref + kRescaleThreshold;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? mt : m_ref;
@@ -660,11 +697,11 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           // O holds tiles < i: wait for PV of tile i-1 (its P buffer's release;
           // the previous use of that buffer is known complete, so the parity
           // wait cannot be fooled by a phase two steps back), then scale this
-          // lane's row
+          // thread's half of the lane's row
           ok = ok && wt.wait(&bars->pfree[bsel(i - 1)], bpar(i - 1));
           tc_after();
 #pragma unroll 1
-          for (int c = 0; c < kHalf / 32; ++c) {
+          for (int c = 4 * sh; c < 4 * sh + 4; ++c) {
             uint32_t r[16], q[16];
             TC_LD16(lane_base + kTmemO + 32 * c, r);
             TC_LD16(lane_base + kTmemO + 32 * c + 16, q);
@@ -682,34 +719,34 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         l *= alpha;
         m_ref = m_new;
       }
-      // P row of head h (bf16); l sums the rounded values
+      // this half of head h's P row (bf16), in the 16-byte chunks p0/8,
+      // p0/8 + 1 and p1/8; l sums the rounded values
       ok = ok && wt.wait(&bars->pfree[b], par ^ 1);
       uint8_t* prow = pbuf(b);
-      float ls[kN / 8];
+      float ls[3];
 #pragma unroll
-      for (int c = 0; c < kN / 8; ++c) {
+      for (int c = 0; c < 3; ++c) {
         uint32_t pk[4];
         float part = 0.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const __nv_bfloat162 two = __floats2bfloat162_rn(exp2f(sc[8 * c + 2 * k] - m_ref),
-                                                           exp2f(sc[8 * c + 2 * k + 1] - m_ref));
+          const __nv_bfloat162 two = __floats2bfloat162_rn(ex2_approx(sc[8 * c + 2 * k] - m_ref),
+                                                           ex2_approx(sc[8 * c + 2 * k + 1] - m_ref));
           const float2 back = __bfloat1622float2(two);
           part += back.x + back.y;
           pk[k] = *reinterpret_cast<const uint32_t*>(&two);
         }
         ls[c] = part;
-        *reinterpret_cast<uint4*>(prow + (c >> 3) * kSwBlk + swz_chunk(h, c & 7)) =
+        const int chunk = c < 2 ? p0 / 8 + c : p1 / 8;
+        *reinterpret_cast<uint4*>(prow + (chunk >> 3) * kSwBlk + swz_chunk(h, chunk & 7)) =
             make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-#pragma unroll
-      for (int c = 1; c < kN / 8; ++c) ls[0] += ls[c];
-      l += ls[0];
+      l += (ls[0] + ls[1]) + ls[2];
       if (!C::kConv && valid < kN) {
         // dense bf16 tail: rows past the unit hold whatever the cache holds
         // there; zero them so P = 0 never meets a non-finite value
         uint8_t* v = opl(j);
-        for (int idx = h; idx < (kN - valid) * 32; idx += 128) {
+        for (int idx = sh * 128 + h; idx < (kN - valid) * 32; idx += 256) {
           const int row = valid + idx / 32, blk = (idx / 8) & 3, ch = idx & 7;
           *reinterpret_cast<uint4*>(v + blk * kBlkBytes + swz_chunk(row, ch)) = make_uint4(0, 0, 0, 0);
         }
@@ -723,25 +760,29 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     if (live) {
       if (ntiles > 0) ok = ok && wt.wait(&bars->pfree[bsel(ntiles - 1)], bpar(ntiles - 1));
       tc_after();
-      // O half (128 heads x 256 fp32) -> workspace, normalised by l.  With the
-      // last PV complete, every stage, P and exchange buffer is idle (the peer
-      // sent its last partial before this CTA's last softmax step), so the
-      // whole half is staged at once as 8 swizzled blocks of 32 columns and
-      // leaves as 8 TMA stores.
-      stage_output(lane_base, sm, h, l > 0.f ? 1.f / l : 0.f, 0, kHalf / 32);
+      // O half (128 heads x 256 fp32) -> workspace, normalised by the head's
+      // l (the sum of the pair's halves).  With the last PV complete, every
+      // stage, P and exchange buffer is idle (the peer sent its last partial
+      // before this CTA's last softmax step), so the whole half is staged at
+      // once as 8 swizzled blocks of 32 columns (4 per thread of the pair)
+      // and leaves as 8 TMA stores.
+      bars->l_half[sh * 128 + h] = l;
+      softmax_sync();
+      const float lt = bars->l_half[h] + bars->l_half[128 + h];
+      stage_output(lane_base, sm, h, lt > 0.f ? 1.f / lt : 0.f, 4 * sh, 4 * sh + 4);
       fence_async_smem();
       softmax_sync();
-      if (h == 0) {
+      if (sh == 0 && h == 0) {
         for (int c = 0; c < kHalf / 32; ++c)
           tma3_store(&tp.m_po, rank * kHalf + 32 * c, 0, unit_id, sm + c * kSwBlk);
         bulk_commit();
       }
-      if (rank == 0)
+      if (rank == 0 && sh == 0)
         p.ws.part_lse[(size_t)unit_id * p.H + h] =
-            (ok && l > 0.f) ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
-      if (h == 0) bulk_wait_read();
+            (ok && lt > 0.f) ? (m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
+      if (sh == 0 && h == 0) bulk_wait_read();
     }
-  } else if (C::kConv && warp >= 12) {
+  } else if (C::kConv && warp >= 12 && warp < 16) {
     // ------------------------------------------------------------ converter
     // raw slot r of tile i -> operand stage j, once the rows have landed and
     // PV of the stage's previous tile is done
