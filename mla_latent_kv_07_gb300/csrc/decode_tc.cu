@@ -37,8 +37,9 @@
 //              ~40 GB/s per SM with ~0.3 us latency on this part, so sending
 //              runs as its own pipeline stage, ahead of the softmax; the
 //              softmax adds the peer's partial when it reads its own.
-//   warps 12-15 converter (FP8 caches and gathers): raw rows -> bf16 operand
-//              tile bf16(fp32(e4m3 * scale)) in the 128-byte swizzled layout
+//   warps 2-3 and 12-15 converter (FP8 caches and gathers): raw rows -> bf16
+//              operand tile bf16(fp32(e4m3 * scale)) in the 128-byte
+//              swizzled layout
 //
 // Every wait is bounded; on expiry the kernel raises a status bit, stops
 // issuing work, and still runs its teardown (cluster barrier, TMEM release).
@@ -62,6 +63,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between resca
 constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemS = 400;
 constexpr long kSpinLimit = 1L << 26;   // polls (~seconds) before giving up
 constexpr int kSwBlk = 128 * 128;         // one 128-row x 128-byte swizzled block: 16 KB
+constexpr int kConvWarps = 6;             // converter: warps 2-3 and 12-15
 
 // Shared-memory plan per variant.  Tiles are 48 positions (MMA N for QK, K
 // for PV), with two S, P and exchange buffers.  An operand stage holds the
@@ -80,6 +82,11 @@ struct Cfg {
   // warps: 0 producer, 1 MMA, 4-7 softmax (first half), 8-11 exchange,
   // 12-15 converter (if any), then 4 warps of the softmax's second half
   static constexpr int kHiWarp = kConv ? 16 : 12;
+  // QK may be issued at most this many tiles past the last issued PV: enough
+  // run-ahead to keep the tensor pipe busy through the exchange and softmax
+  // of a tile, no more -- the pipe runs its queue in order, so each queued QK
+  // delays the PV behind it (measured: 2 starves the pipe, 3 is best).
+  static constexpr int kQkAhead = 3;
   static constexpr int kThreads = 32 * (kHiWarp + 4);
   static constexpr int kBlkBytes = kN * 128;       // one 64-column swizzled block of a tile
   static constexpr int kOplBytes = 4 * kBlkBytes;  // latent half operand
@@ -398,10 +405,10 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int j = 0; j < C::kStages; ++j) {
       bar_init(&bars->full[j], 1);
-      bar_init(&bars->deq[j], 4);
+      bar_init(&bars->deq[j], kConvWarps);
       bar_init(&bars->empty[j], 1);
     }
-    for (int r = 0; r < 2; ++r) bar_init(&bars->rfree[r], 4);
+    for (int r = 0; r < 2; ++r) bar_init(&bars->rfree[r], kConvWarps);
     for (int b = 0; b < 2; ++b) {
       bar_init(&bars->sfull[b], 1);
       bar_init(&bars->sfree[b], 12);   // softmax (8) and exchange (4) warps read S
@@ -571,7 +578,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
             did = true;
           }
         }
-        if (nq < ntiles && nq < np + 3) {
+        if (nq < ntiles && nq < np + C::kQkAhead) {
           const int k = nq, j = k % C::kStages, b = bsel(k);
           const uint32_t use = k / C::kStages;
           if (bar_try(C::kConv ? &bars->deq[j] : &bars->full[j], use & 1) &&
@@ -782,11 +789,11 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
             (ok && lt > 0.f) ? (m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
       if (sh == 0 && h == 0) bulk_wait_read();
     }
-  } else if (C::kConv && warp >= 12 && warp < 16) {
+  } else if (C::kConv && (warp == 2 || warp == 3 || (warp >= 12 && warp < 16))) {
     // ------------------------------------------------------------ converter
     // raw slot r of tile i -> operand stage j, once the rows have landed and
-    // PV of the stage's previous tile is done
-    const int t = threadIdx.x - 384;
+    // PV of the stage's previous tile is done; kConvWarps warps share a tile
+    const int t = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 384 + 64;
     for (int i = 0; i < ntiles; ++i) {
       const int r = i % C::kRawSlots, j = i % C::kStages;
       if (!wt.wait(&bars->full[r], (i / C::kRawSlots) & 1)) break;
@@ -795,7 +802,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       uint8_t* dst = opl(j);
       if (kFmt == 1) {
         // 48 rows x 16 chunks of 16 codes -> 2 swizzled 16-byte chunks each
-        for (int idx = t; idx < kN * 16; idx += 128) {
+        for (int idx = t; idx < kN * 16; idx += 32 * kConvWarps) {
           const int row = idx >> 4, q = idx & 15;  // codes [16q, 16q + 16) of the half row
           uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
           if (row < valid) {
@@ -810,7 +817,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         }
       } else {
         // gathered bf16 rows: 48 rows x 32 chunks of 8 values
-        for (int idx = t; idx < kN * 32; idx += 128) {
+        for (int idx = t; idx < kN * 32; idx += 32 * kConvWarps) {
           const int row = idx >> 5, q = idx & 31;
           uint4 v = make_uint4(0, 0, 0, 0);
           if (row < valid) v = *reinterpret_cast<const uint4*>(raw(r) + row * C::kRawRow + q * 16);
@@ -818,7 +825,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         }
       }
       // rotary rows -> swizzled operand
-      for (int idx = t; idx < kN * 8; idx += 128) {
+      for (int idx = t; idx < kN * 8; idx += 32 * kConvWarps) {
         const int row = idx >> 3, q = idx & 7;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (row < valid) v = *reinterpret_cast<const uint4*>(rpe(r) + row * 128 + q * 16);
