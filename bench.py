@@ -234,6 +234,68 @@ class Setup:
 
 # --------------------------------------------------------------- GPU arm
 
+def read_ceiling_gbs(st, stream, reps: int = 24):
+    """HBM read rate of the library's streaming read kernel over the same
+    rotated cache tensors the steps read (every pass cold in L2), in GB/s.
+    The passes are captured in a CUDA graph, as the steps are, so the
+    launches run back to back on the device."""
+    sink = torch.zeros(1, dtype=torch.int32, device=st.device)
+    tensors = [[t for t in (c.kv, c.pe, c.kv_scale) if t is not None] for c in st.caches]
+    with torch.cuda.stream(stream):
+        for ts in tensors[:2]:
+            for t in ts:
+                mla.read_ceiling(t, sink, stream=stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    nbytes = 0
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(reps):
+            for t in tensors[i % len(tensors)]:
+                mla.read_ceiling(t, sink, stream=stream)
+                nbytes += t.numel() * t.element_size()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9, nbytes / reps
+
+
+def run_warm(st, stream, steps: int = 200):
+    """The same step with one cache (or one top-k list) every time, so the
+    cache stays in L2: (step us, decode-kernel us).  None when one copy of
+    the step's bytes does not fit in L2."""
+    w = st.w
+    if layout.step_bytes(st.tokens, w.B, w.H, w.fmt) * 1.2 > st.l2_bytes:
+        return None
+    for _ in range(3):
+        st.step(0)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(steps):
+            st.step(0)
+    kgraph = torch.cuda.CUDAGraph()
+    mla.trace_begin(steps)
+    with torch.cuda.graph(kgraph, stream=stream):
+        for _ in range(steps):
+            st.step(0)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        graph.replay()          # warms L2 with the one cache
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        kgraph.replay()
+    kern_ms, timed, _ = mla.trace_end()
+    return {"step_us": round(e0.elapsed_time(e1) * 1e3 / steps, 3),
+            "kernel_us": round(kern_ms * 1e3 / max(timed, 1), 3),
+            "note": "one cache resident in L2 (warm); the headline is the cold, rotated number"}
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch.distributed as dist
     device = torch.device("cuda", local_rank)
@@ -291,6 +353,7 @@ def run_gpu(args, rank, world, local_rank):
         kgraph.replay()
     kern_ms, timed, _ = mla.trace_end()
     clocks = sampler.stop() if sampler else None
+    ceil_gbs, ceil_bytes = read_ceiling_gbs(st, stream)
     ms = slowest(ms, device)
     step_s = ms / 1e3 / K
     cache_bytes = st.tokens * layout.cache_bytes_per_token(w.fmt)
@@ -313,8 +376,10 @@ def run_gpu(args, rank, world, local_rank):
                 "peak_source": f"of {pk_src}", "kernel": kernel,
                 "kernel_us": round(kern_s * 1e6, 3),
                 "hbm_frac_of_step": round(cache_bytes / step_s / 1e9 / pk["hbm_gbs"], 4),
+                "cache_read_frac_of_read_ceiling": round(cache_bytes / kern_s / 1e9 / ceil_gbs, 4),
                 "roofline_time_us": round(max(t_hbm, t_tc) * 1e6, 3)}
 
+    warm = run_warm(st, stream)
     e2e = run_e2e(st, K, W) if not args.no_e2e else None
     cpu = run_cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu) else None
     if rank != 0:
@@ -334,6 +399,10 @@ def run_gpu(args, rank, world, local_rank):
         "tokens_per_s": round(tokens_per_s, 1),
         "wall_ms_per_step": round(t_wall * 1e3 / K, 6),
         "roofline": roofline,
+        "warm": warm,
+        "read_ceiling": {"gbs": round(ceil_gbs, 1), "kernel": "read_ceiling_kernel",
+                         "bytes_per_pass": int(ceil_bytes),
+                         "sample": "the step's rotated cache tensors, streamed with 16-byte loads"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,

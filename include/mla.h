@@ -228,6 +228,16 @@ MLA_API mla_status mla_trace_begin(int32_t max_records);
 MLA_API mla_status mla_trace_end(float* main_kernel_ms, int32_t* timed_launches,
                                  int32_t* kernel_launches);
 
+/*
+ * mla_read_ceiling -- stream `bytes` of device memory at `buf` and XOR-fold
+ * them into *sink (a measurement aid with no counterpart on the pages: the
+ * HBM read rate this device achieves with plain 16-byte streaming loads, the
+ * ceiling the decode's cache reads are compared with).  buf 16-byte aligned,
+ * bytes a positive multiple of 16, sink a device uint32 (4-byte aligned);
+ * otherwise MLA_ERR_INVALID_ARG.  Asynchronous on `stream`.
+ */
+MLA_API mla_status mla_read_ceiling(const void* buf, size_t bytes, uint32_t* sink, void* stream);
+
 /* Human-readable name of a status code (static string). */
 MLA_API const char* mla_status_string(mla_status status);
 

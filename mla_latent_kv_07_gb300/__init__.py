@@ -71,6 +71,8 @@ def lib() -> ctypes.CDLL:
             L.mla_last_error.restype = ctypes.c_char_p
             L.mla_decode_noalloc.argtypes = [P, P, P, P, I32, I32, I32, F, P, P, P]
             L.mla_decode_noalloc.restype = I32
+            L.mla_read_ceiling.argtypes = [P, SZ, P, P]
+            L.mla_read_ceiling.restype = I32
             L.mla_trace_begin.argtypes = [I32]
             L.mla_trace_begin.restype = I32
             L.mla_trace_end.argtypes = [P, P, P]
@@ -218,6 +220,18 @@ def workspace_status(workspace, stream=None) -> int:
     _check(lib().mla_workspace_status(_ptr(workspace), ctypes.byref(flags), _stream(stream)),
            "mla_workspace_status")
     return int(flags.value)
+
+
+def read_ceiling(buf: torch.Tensor, sink: torch.Tensor, stream=None) -> None:
+    """Stream all bytes of the contiguous CUDA tensor `buf` (a measurement of
+    the achievable HBM read rate); XOR-folds them into the int32 `sink`."""
+    if not (buf.is_cuda and buf.is_contiguous()):
+        raise ValueError("buf must be a contiguous CUDA tensor")
+    if sink.dtype != torch.int32 or not sink.is_cuda or sink.numel() < 1:
+        raise ValueError("sink must be a CUDA int32 tensor")
+    nbytes = buf.numel() * buf.element_size()
+    _check(lib().mla_read_ceiling(buf.data_ptr(), nbytes, sink.data_ptr(), _stream(stream)),
+           "mla_read_ceiling")
 
 
 def trace_begin(max_records: int) -> None:

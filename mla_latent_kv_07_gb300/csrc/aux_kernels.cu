@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(1024) sparse_prep_kernel(const int* __restrict
 // granule and grown until sum_b ceil(len_b / chunk) <= target.
 __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ end_pos,
                                                        int max_end_pos, Workspace ws, int B,
-                                                       int target, int granule) {
+                                                       int target, int granule, int direct) {
   __shared__ int scan_smem[33];
   __shared__ unsigned long long total_len;
   __shared__ int count_smem;
@@ -231,11 +231,12 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
   for (int b = b0; b < b0 + per && b < B; ++b) {
     const int len = ws.lengths[b];
     const int n = (int)((len + chunk - 1) / chunk);
-    ws.seq[b] = make_int2(u, n);
+    const int one = direct && n == 1;
+    ws.seq[b] = make_int2(u, one ? -1 : n);
     for (int i = 0; i < n; ++i) {
       int t0 = (int)(i * chunk);
       int t1 = (int)((i + 1) * chunk < len ? (i + 1) * chunk : len);
-      ws.units[u + i] = Unit{b, t0, t1, 0};
+      ws.units[u + i] = Unit{b, t0, t1, one};
     }
     u += n;
   }
@@ -255,6 +256,7 @@ __global__ void __launch_bounds__(128) combine_kernel(Workspace ws, int H,
   pdl_trigger();
   const int h = blockIdx.x, b = blockIdx.y;
   const int2 sq = ws.seq[b];
+  if (sq.y < 0) return;   // a single unit: the decode kernel wrote the result
   const int n = sq.y;
   const int c = threadIdx.x * 4;
   const float* pl = ws.part_lse + (size_t)sq.x * H + h;            // unit stride H
@@ -301,7 +303,44 @@ __global__ void __launch_bounds__(128) combine_kernel(Workspace ws, int H,
   if (lse_out && threadIdx.x == 0) lse_out[(size_t)b * H + h] = lse;
 }
 
+// ----------------------------------------------------------- read ceiling
+// Streams n16 16-byte words (8 loads in flight per thread, streaming cache
+// hint) and folds them into one XOR per CTA, so no load is dead code: the
+// achievable HBM read rate of this device, for comparison with the decode.
+__global__ void __launch_bounds__(512) read_ceiling_kernel(const uint4* __restrict__ buf, size_t n16,
+                                                          uint32_t* __restrict__ sink) {
+  pdl_wait();
+  pdl_trigger();
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  uint32_t acc = 0;
+  for (; i < n16; i += 8 * stride) {
+    uint4 v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      v[k] = i + k * stride < n16 ? __ldcs(buf + i + k * stride) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc ^= v[k].x ^ v[k].y ^ v[k].z ^ v[k].w;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc ^= __shfl_xor_sync(0xffffffffu, acc, o);
+  // one atomic per CTA: same-address atomics serialise in L2
+  __shared__ uint32_t part[16];
+  if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    uint32_t x = 0;
+    for (int k = 0; k < (int)(blockDim.x >> 5); ++k) x ^= part[k];
+    atomicXor(sink, x);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_read_ceiling(const void* buf, size_t bytes, uint32_t* sink, int sms, cudaStream_t s) {
+  return launch_pdl(read_ceiling_kernel, dim3(4 * sms), dim3(512), 0, s,
+                    static_cast<const uint4*>(buf), bytes / 16, sink);
+}
 
 cudaError_t launch_append_host_pos(const AppendParams& p, cudaStream_t s) {
   return launch_pdl(append_kernel<false>, dim3(p.B), dim3(128), 0, s, p);
@@ -319,10 +358,10 @@ cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int m
 }
 
 cudaError_t launch_schedule(const int* end_pos, int max_end_pos, const Workspace& ws, int B,
-                            int target, int granule, cudaStream_t s) {
+                            int target, int granule, bool direct, cudaStream_t s) {
   const int threads = B >= 1024 ? 1024 : ((B + 31) / 32) * 32;
   return launch_pdl(schedule_kernel, dim3(1), dim3(threads), 0, s, end_pos, max_end_pos, ws, B,
-                    target, granule);
+                    target, granule, direct ? 1 : 0);
 }
 
 cudaError_t launch_combine(const Workspace& ws, int B, int H, void* out, float* lse,

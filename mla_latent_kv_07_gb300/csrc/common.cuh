@@ -23,16 +23,18 @@ constexpr uint32_t kDevAppendSkipped = 0x2u;
 constexpr uint32_t kDevTimeout = 0x4u;
 
 // One unit of decode work: positions [t0, t1) of sequence b (dense), or
-// entries [t0, t1) of b's gather list (sparse).  b < 0: no work.
+// entries [t0, t1) of b's gather list (sparse).  b < 0: no work.  direct: the
+// unit is its sequence's only one and the decode writes the final output and
+// log-sum-exp itself (the combine skips the sequence).
 struct Unit {
-  int b, t0, t1, pad;
+  int b, t0, t1, direct;
 };
 
 // Workspace carve-up.  Every region starts on a 256-byte boundary.
 struct Workspace {
   uint32_t* status;   // device status word (MLA_DEV_* bits)
   int* n_units;       // units actually scheduled
-  int2* seq;          // [B] (first unit, unit count)
+  int2* seq;          // [B] (first unit, unit count; -1: written by the decode)
   int* lengths;       // [B] clamped end_pos (dense) or gather count (sparse)
   Unit* units;        // [max_units]
   float* part_lse;    // [max_units, H]
@@ -109,6 +111,8 @@ struct DecodeParams {
   const void* q_pe;       // bf16 [B, H, 64]
   int B, H;
   float scale_log2;       // softmax_scale * log2(e)
+  void* out;              // bf16 [B, H, 512] (sequences with a direct unit)
+  float* lse;             // fp32 [B, H] or null
   Workspace ws;
   int K;                  // sparse list length (0 = dense)
 };
@@ -167,8 +171,9 @@ cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int m
 // end_pos != nullptr: dense (lengths = clamped end_pos, and the schedule is the
 // first kernel of the call, so it clears the status word); nullptr: the
 // lengths were already written (sparse prep) and the status word cleared.
+// direct: a sequence that gets a single unit is finished by the decode kernel.
 cudaError_t launch_schedule(const int* end_pos, int max_end_pos, const Workspace& ws, int B,
-                            int target_units, int granule, cudaStream_t s);
+                            int target_units, int granule, bool direct, cudaStream_t s);
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s);
 int decode_mma_granule();
 // tensor-memory path (H = 128): one CTA pair per unit
@@ -180,5 +185,7 @@ bool decode_tc_supported(int H);
 int decode_tc_units(int fmt, bool sparse, int num_sms);
 cudaError_t launch_combine(const Workspace& ws, int B, int H, void* out, float* lse,
                            cudaStream_t s);
+// streams `bytes` (a multiple of 16) of device memory, XOR-folding into *sink
+cudaError_t launch_read_ceiling(const void* buf, size_t bytes, uint32_t* sink, int sms, cudaStream_t s);
 
 }  // namespace mla

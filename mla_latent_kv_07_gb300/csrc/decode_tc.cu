@@ -127,6 +127,7 @@ struct TcParams {
   CUtensorMap m_ql;   // q_latent [B][128][512] (box 64 x 128, 128-byte swizzle)
   CUtensorMap m_qp;   // q_pe [B][128][64] (box 64 x 128, 128-byte swizzle)
   CUtensorMap m_po;   // partial outputs [units][128][512] fp32 (box 32 x 128, 128-byte swizzle)
+  CUtensorMap m_out;  // final output [B][128][512] bf16 (box 64 x 128, 128-byte swizzle)
 };
 
 // ------------------------------------------------------------------ PTX
@@ -368,6 +369,32 @@ __device__ __forceinline__ void stage_output(uint32_t lane_base, uint8_t* out, i
           make_float4(__uint_as_float(q[4 * k]) * inv, __uint_as_float(q[4 * k + 1]) * inv,
                       __uint_as_float(q[4 * k + 2]) * inv, __uint_as_float(q[4 * k + 3]) * inv);
     }
+  }
+}
+
+// Epilogue of a sequence's only unit: O columns [32 c0, 32 c1) of TMEM lane
+// h, times inv, rounded to bf16, into 128-byte swizzled blocks of 64 columns
+// (16 KB each) at `out`.
+__device__ __forceinline__ void stage_output_bf16(uint32_t lane_base, uint8_t* out, int h, float inv,
+                                                  int c0, int c1) {
+#pragma unroll 1
+  for (int c = c0; c < c1; ++c) {
+    uint32_t r[32];
+    TC_LD16(lane_base + kTmemO + 32 * c, r);
+    TC_LD16(lane_base + kTmemO + 32 * c + 16, (r + 16));
+    tc_wait_ld();
+    uint32_t pk[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const __nv_bfloat162 two = __floats2bfloat162_rn(__uint_as_float(r[2 * k]) * inv,
+                                                       __uint_as_float(r[2 * k + 1]) * inv);
+      pk[k] = *reinterpret_cast<const uint32_t*>(&two);
+    }
+    uint8_t* blk = out + (c >> 1) * kSwBlk;
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      *reinterpret_cast<uint4*>(blk + swz_chunk(h, (c & 1) * 4 + k)) =
+          make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
   }
 }
 
@@ -773,20 +800,35 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       // before this CTA's last softmax step), so the whole half is staged at
       // once as 8 swizzled blocks of 32 columns (4 per thread of the pair)
       // and leaves as 8 TMA stores.
+      // A sequence's only unit writes the final bf16 output (4 blocks of 64
+      // columns) and log-sum-exp itself.
       bars->l_half[sh * 128 + h] = l;
       softmax_sync();
       const float lt = bars->l_half[h] + bars->l_half[128 + h];
-      stage_output(lane_base, sm, h, lt > 0.f ? 1.f / lt : 0.f, 4 * sh, 4 * sh + 4);
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      if (u.direct)
+        stage_output_bf16(lane_base, sm, h, inv, 4 * sh, 4 * sh + 4);
+      else
+        stage_output(lane_base, sm, h, inv, 4 * sh, 4 * sh + 4);
       fence_async_smem();
       softmax_sync();
       if (sh == 0 && h == 0) {
-        for (int c = 0; c < kHalf / 32; ++c)
-          tma3_store(&tp.m_po, rank * kHalf + 32 * c, 0, unit_id, sm + c * kSwBlk);
+        if (u.direct) {
+          for (int c = 0; c < kHalf / 64; ++c)
+            tma3_store(&tp.m_out, rank * kHalf + 64 * c, 0, u.b, sm + c * kSwBlk);
+        } else {
+          for (int c = 0; c < kHalf / 32; ++c)
+            tma3_store(&tp.m_po, rank * kHalf + 32 * c, 0, unit_id, sm + c * kSwBlk);
+        }
         bulk_commit();
       }
-      if (rank == 0 && sh == 0)
-        p.ws.part_lse[(size_t)unit_id * p.H + h] =
-            (ok && lt > 0.f) ? (m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
+      if (rank == 0 && sh == 0) {
+        const float lse = (ok && lt > 0.f) ? (m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
+        if (!u.direct)
+          p.ws.part_lse[(size_t)unit_id * p.H + h] = lse;
+        else if (p.lse)
+          p.lse[(size_t)u.b * p.H + h] = lse;
+      }
       if (sh == 0 && h == 0) bulk_wait_read();
     }
   } else if (C::kConv && (warp == 2 || warp == 3 || (warp >= 12 && warp < 16))) {
@@ -1000,7 +1042,9 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s) {
        encode3(&tp.m_qp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.q_pe, kDr, 128, B, 64, 128,
                CU_TENSOR_MAP_SWIZZLE_128B) &&
        encode3(&tp.m_po, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.ws.part_o, kDc, 128,
-               (uint64_t)p.ws.max_units, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+               (uint64_t)p.ws.max_units, 32, 128, CU_TENSOR_MAP_SWIZZLE_128B) &&
+       encode3(&tp.m_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.out, kDc, 128, B, 64, 128,
+               CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return cudaErrorInvalidValue;
   if (p.fmt == 0) return p.K ? launch_tc_variant<0, true>(tp, s) : launch_tc_variant<0, false>(tp, s);
   return p.K ? launch_tc_variant<1, true>(tp, s) : launch_tc_variant<1, false>(tp, s);

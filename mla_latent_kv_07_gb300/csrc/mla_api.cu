@@ -126,6 +126,8 @@ mla::DecodeParams make_params(const DecodeArgs& a, const mla::Workspace& ws, int
   p.B = a.B;
   p.H = a.H;
   p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
+  p.out = a.out;
+  p.lse = a.lse;
   p.ws = ws;
   p.K = K;
   return p;
@@ -151,7 +153,7 @@ mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cuda
   cudaError_t e = mla::launch_schedule(
       K ? nullptr : a.end_pos, a.max_end_pos, ws, a.B,
       tc ? mla::decode_tc_units(a.cache->fmt, K > 0, sms) : mla::target_units_mma(a.H, sms),
-      tc ? mla::decode_tc_granule(a.cache->fmt, K > 0) : mla::decode_mma_granule(), s);
+      tc ? mla::decode_tc_granule(a.cache->fmt, K > 0) : mla::decode_mma_granule(), tc, s);
   if (e != cudaSuccess) return cuda_fail(e, "schedule");
   const bool traced = trace_start(s);
   e = tc ? mla::launch_decode_tc(make_params(a, ws, K), s)
@@ -266,6 +268,18 @@ mla_status mla_workspace_status(const void* workspace, uint32_t* flags, void* st
   cudaError_t e = cudaMemcpyAsync(flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "status");
+}
+
+mla_status mla_read_ceiling(const void* buf, size_t bytes, uint32_t* sink, void* stream) {
+  g_last_error[0] = 0;
+  if (!buf || !sink || bytes == 0 || (bytes & 15u) || !aligned16(buf) || !aligned4(sink))
+    return MLA_ERR_INVALID_ARG;
+  int sms = 0;
+  if (num_sms(&sms) != 0) return MLA_ERR_UNSUPPORTED;
+  cudaError_t e = mla::launch_read_ceiling(buf, bytes, sink, sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "read_ceiling");
+  trace_launches(1);
+  return MLA_OK;
 }
 
 const char* mla_status_string(mla_status status) {

@@ -109,6 +109,8 @@ mla_status mla_decode_noalloc(const mla_cache* c, const void* q_latent, const vo
   p.B = B;
   p.H = H;
   p.scale_log2 = softmax_scale * 1.4426950408889634f;
+  p.out = out;
+  p.lse = lse;
   p.ws = ws;
   p.K = 0;
 
@@ -118,7 +120,7 @@ mla_status mla_decode_noalloc(const mla_cache* c, const void* q_latent, const vo
   cudaError_t e = mla::launch_schedule(
       end_pos, max_end_pos, ws, B,
       tc ? mla::decode_tc_units(c->fmt, false, sms) : mla::target_units_mma(H, sms),
-      tc ? mla::decode_tc_granule(c->fmt, false) : mla::decode_mma_granule(), s);
+      tc ? mla::decode_tc_granule(c->fmt, false) : mla::decode_mma_granule(), tc, s);
   if (e == cudaSuccess) e = tc ? mla::launch_decode_tc(p, s) : mla::launch_decode_mma(p, s);
   if (e == cudaSuccess) e = mla::launch_combine(ws, B, H, out, lse, s);
   if (e != cudaSuccess) {

@@ -127,3 +127,12 @@ def test_trace_counts_launches_without_events(L):
         assert L.mla_trace_end(ctypes.byref(ms), ctypes.byref(n), ctypes.byref(k)) == 0
     assert (ms.value, n.value, k.value) == (0.0, 0, 0)
     assert L.mla_trace_end(None, None, None) == 1   # not tracing
+
+
+def test_read_ceiling_rejects_bad_arguments(L):
+    f = ctypes.c_void_p(FAKE)
+    assert L.mla_read_ceiling(None, 1024, f, None) == 1
+    assert L.mla_read_ceiling(f, 0, f, None) == 1
+    assert L.mla_read_ceiling(f, 1000, f, None) == 1          # not a multiple of 16
+    assert L.mla_read_ceiling(ctypes.c_void_p(FAKE + 8), 1024, f, None) == 1
+    assert L.mla_read_ceiling(f, 1024, None, None) == 1

@@ -110,6 +110,24 @@ def test_rows_past_end_pos_are_never_used():
     check_close(f64(lse).reshape(-1), ref_lse, "lse")
 
 
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_single_unit_sequences_write_directly(fmt):
+    # sequences of one or two tiles get a single unit, which writes the final
+    # output (and lse, when asked) itself; the long one is split and combined
+    B, S, H = 3, 512, 128
+    oc = oracle_cache(_rand_bf16((B, S, 512), 91), _rand_bf16((B, S, 64), 92), fmt)
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((B, H, 512), 93), _rand_bf16((B, H, 64), 94)
+    ends = np.array([30, 96, 500], np.int32)
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), ends, 0.16)
+    for want_lse in (True, False):
+        out, lse = mla.decode(dc, ql.cuda(), qp.cuda(), torch.from_numpy(ends).cuda(), S, 0.16,
+                              want_lse=want_lse)
+        check_close(f64(out).reshape(-1, 512), ref, f"out (lse={want_lse})")
+        if want_lse:
+            check_close(f64(lse).reshape(-1), ref_lse, "lse")
+
+
 def test_empty_and_clamped_sequences():
     B, S, H = 3, 64, 16
     oc = oracle_cache(_rand_bf16((B, S, 512), 31), _rand_bf16((B, S, 64), 32), 0)
@@ -138,6 +156,18 @@ def test_workspace_too_small_is_refused():
     with pytest.raises(mla.MLAError) as e:
         mla.decode(dc, ql, qp, torch.tensor([32], dtype=torch.int32).cuda(), 32, 0.1, workspace=ws)
     assert e.value.code == 4
+
+
+def test_read_ceiling_reads_every_word():
+    # the streaming read kernel folds every 32-bit word: its XOR equals the
+    # XOR of the buffer (an odd length exercises the tail loop)
+    rng = np.random.default_rng(81)
+    words = rng.integers(0, 2**32, size=(1 << 22) + 4 * 37, dtype=np.uint64).astype(np.uint32)
+    buf = torch.from_numpy(words.view(np.int32)).cuda()
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    mla.read_ceiling(buf, sink)
+    torch.cuda.synchronize()
+    assert int(sink.cpu().numpy().view(np.uint32)[0]) == int(np.bitwise_xor.reduce(words))
 
 
 # ---------------------------------------------------------- small sparse
