@@ -78,7 +78,11 @@ template <int kFmt, bool kSparse>
 struct Cfg {
   static constexpr bool kConv = kFmt == 1 || kSparse;       // converter warps present
   static constexpr int kN = 48;    // positions per tile
-  static constexpr int kBufs = 2;  // S, P and exchange buffers
+  static constexpr int kBufs = 2;  // S and P buffers
+  // exchange buffers: two, except with FP8 caches, whose fourth operand stage
+  // takes the room of the second (the softmax reads a tile's exchange buffer
+  // well before the peer's partial of the next tile is due)
+  static constexpr int kXBufs = kFmt == 1 ? 1 : 2;
   // warps: 0 producer, 1 MMA, 4-7 softmax (first half), 8-11 exchange,
   // 12-15 converter (if any), then 4 warps of the softmax's second half
   static constexpr int kHiWarp = kConv ? 16 : 12;
@@ -96,7 +100,7 @@ struct Cfg {
   // c * 128 + h, so a warp's remote store is one contiguous 512-byte run
   static constexpr int kXBytes = (kN / 4) * 128 * 16;
   static constexpr int kStage = kOplBytes + kOpeBytes;
-  static constexpr int kStages = kConv ? (kFmt == 1 ? 3 : 2) : 4;
+  static constexpr int kStages = kConv ? (kFmt == 1 ? 4 : 2) : 4;
   static constexpr int kRawRow = kFmt == 1 ? kHalf : kHalf * 2;  // bytes of a raw latent half row
   // FP8 scales, 16 B per row: dense tiles land as 48 consecutive rows; a
   // gather lands 4 rows per 128-byte slot (a tensor copy's shared-memory
@@ -107,15 +111,20 @@ struct Cfg {
   static constexpr int kRawOff = kStages * kStage;
   static constexpr int kPOff = kRawOff + kRawSlots * kRaw;
   static constexpr int kXOff = kPOff + kBufs * kPBytes;
-  static constexpr int kBarOff = kXOff + kBufs * kXBytes;
+  static constexpr int kBarOff = kXOff + kXBufs * kXBytes;
+  // query staging (5 swizzled blocks): the P and exchange buffers, or with
+  // FP8 caches operand stages 1-3, which the converter fills only once the
+  // query has moved to tensor memory
+  static constexpr int kQOff = kFmt == 1 ? kStage : kPOff;
   static constexpr int kSmem = kBarOff + 4096 + 1024;      // barriers/flags + base alignment slack
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kStage % 1024 == 0 && kRaw % 1024 == 0, "1 KB alignment of swizzled tiles");
   static_assert(kN % 16 == 0 && kTmemS + kBufs * kN <= 512, "tile width");
-  // the query is staged in the P and exchange buffers (5 swizzled blocks), the
-  // output half from offset 0 (8 blocks of 32 fp32 columns)
-  static_assert(kBufs * (kPBytes + kXBytes) >= 5 * kSwBlk, "query staging fits P and X");
-  static_assert(kPOff % 1024 == 0, "1 KB alignment of the query staging");
+  // the output half is staged from offset 0 (8 blocks of 32 fp32 columns)
+  static_assert(kFmt == 1 ? (kStages - 1) * kStage >= 5 * kSwBlk
+                          : kBufs * kPBytes + kXBufs * kXBytes >= 5 * kSwBlk,
+                "query staging fits");
+  static_assert(kQOff % 1024 == 0 && kPOff % 1024 == 0, "1 KB alignment of the query staging");
   static_assert(kBarOff >= 8 * kSwBlk, "output staging fits the idle buffers");
 };
 
@@ -427,6 +436,8 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   // the phase that tile completes on that buffer's barriers
   auto bsel = [](int i) { return i % C::kBufs; };
   auto bpar = [](int i) { return (uint32_t)((i / C::kBufs) & 1); };
+  auto xsel = [](int i) { return i % C::kXBufs; };   // the same for exchange buffers
+  auto xpar = [](int i) { return (uint32_t)((i / C::kXBufs) & 1); };
 
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
@@ -477,7 +488,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   // issuer, and the peer that its exchange buffers may be written.
   if (live && warp >= 4 && warp < 8) {
     const int h = threadIdx.x - 128;
-    uint8_t* qs = sm + C::kPOff;
+    uint8_t* qs = sm + C::kQOff;
     if (h == 0) {
       bar_expect_tx(&bars->qbar, 5 * kSwBlk);
       for (int blk = 0; blk < 4; ++blk)
@@ -654,15 +665,16 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       tc_before();
       __syncwarp();
       if (lane == 0) bar_arrive(&bars->sfree[b]);
-      if (!wt.wait(&bars->xempty[b], bpar(i))) break;   // phase 0: the peer's query staging is done
-      const uint32_t xd = mapa(xbuf(b) + 4 * h, peer);
+      const int xb = xsel(i);
+      if (!wt.wait(&bars->xempty[xb], xpar(i))) break;   // phase 0: the peer's query staging is done
+      const uint32_t xd = mapa(xbuf(xb) + 4 * h, peer);
 #pragma unroll
       for (int c = 0; c < kN / 4; ++c)
         asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(xd + 16 * 128 * c),
                      "r"(r[4 * c]), "r"(r[4 * c + 1]), "r"(r[4 * c + 2]), "r"(r[4 * c + 3])
                      : "memory");
       __syncwarp();
-      if (lane == 0) bar_arrive_remote(mapa(&bars->xfull[b], peer));
+      if (lane == 0) bar_arrive_remote(mapa(&bars->xfull[xb], peer));
     }
   } else if ((warp >= 4 && warp < 8) || (warp >= C::kHiWarp && warp < C::kHiWarp + 4)) {
     // ------------------------------------------------------------ softmax
@@ -697,9 +709,10 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         if (lane == 0) bar_arrive(&bars->sfree[b]);   // QK of tile i + kBufs may overwrite
       }
       // + the peer's partial (fp32 addition commutes: both CTAs get the same S)
-      ok = ok && wt.wait(&bars->xfull[b], par);
+      const int xb = xsel(i);
+      ok = ok && wt.wait(&bars->xfull[xb], xpar(i));
       {
-        const float4* xr = reinterpret_cast<const float4*>(xbuf(b)) + h;
+        const float4* xr = reinterpret_cast<const float4*>(xbuf(xb)) + h;
 #pragma unroll
         for (int k = 0; k < 6; ++k) {
           const float4 v = xr[128 * (k < 4 ? p0 / 4 + k : p1 / 4 + k - 4)];
@@ -708,7 +721,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         __syncwarp();
         // my buffer b may be refilled: the values read above are already in
         // registers, so no release ordering is needed
-        if (lane == 0) bar_arrive_remote_relaxed(mapa(&bars->xempty[b], peer));
+        if (lane == 0) bar_arrive_remote_relaxed(mapa(&bars->xempty[xb], peer));
       }
       // masked, scaled scores; the tile maximum of the pair
       const int valid = min(kN, u.t1 - (u.t0 + i * kN));
@@ -838,6 +851,8 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     const int t = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 384 + 64;
     for (int i = 0; i < ntiles; ++i) {
       const int r = i % C::kRawSlots, j = i % C::kStages;
+      // FP8: stages 1-3 hold the staged query until it is in tensor memory
+      if (kFmt == 1 && i == 1 && !wt.wait(&bars->qready, 0)) break;
       if (!wt.wait(&bars->full[r], (i / C::kRawSlots) & 1)) break;
       if (!wt.wait(&bars->empty[j], ((i / C::kStages) & 1) ^ 1)) break;
       const int valid = min(kN, u.t1 - (u.t0 + i * kN));
