@@ -218,6 +218,32 @@ def decode_absorbed(cache: dict, q_latent, q_pe, end_pos, softmax_scale: float,
     return (out, lse, w) if w is not None else (out, lse)
 
 
+def decode_absorbed_mtp(cache: dict, q_latent, q_pe, end_pos, softmax_scale: float):
+    """fp64 absorbed decode of s new tokens per sequence (multi-token decode).
+
+    q_latent [B, s, H, 512], q_pe [B, s, H, 64].  The s new tokens of sequence
+    b sit at positions end_pos[b]-s .. end_pos[b]-1; token j attends, as the
+    causal mask of "DeepSeek-V3.2-Exp . KV cache" (the upper-triangular -inf
+    mask over the current step's tokens) prescribes, to the cache positions up
+    to and including its own: 0 .. end_pos[b]-s+j.  That is the single-token
+    decode with end_pos[b] - (s-1-j) (a token with no position attends to
+    nothing: out 0, lse -inf).  Returns (out [B, s, H, 512], lse [B, s, H]).
+    """
+    ql = np.asarray(q_latent)
+    qp = np.asarray(q_pe)
+    B, s, H = ql.shape[:3]
+    ep = np.asarray(end_pos, np.int64)
+    out = np.empty((B, s, H, DC), np.float64)
+    lse = np.empty((B, s, H), np.float64)
+    for j in range(s):
+        e = np.maximum(ep - (s - 1 - j), 0).astype(np.int32)
+        o, l = decode_absorbed(cache, np.ascontiguousarray(ql[:, j]), np.ascontiguousarray(qp[:, j]), e,
+                               softmax_scale)
+        out[:, j] = o.reshape(B, H, DC)
+        lse[:, j] = l.reshape(B, H)
+    return out, lse
+
+
 def decode_naive(cache: dict, wkv_b, q_nope, q_pe, end_pos, softmax_scale: float):
     """fp64 non-absorbed MHA: keys/values expanded through wkv_b [H, 256, 512].
 

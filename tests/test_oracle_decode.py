@@ -11,7 +11,10 @@ What fixes the answers here, independent of the oracle's own code:
     (an index list covering every position equals dense attention; repeated
     and out-of-range indices change nothing);
   * the cache geometry of that page: a call that writes row 1,000 reads rows
-    0..1,000.
+    0..1,000;
+  * multi-token decode: a brute-force float64 attention with the explicit
+    causal mask matrix over the step's s tokens (token j at position
+    T-s+j sees positions 0..T-s+j).
 """
 import math
 
@@ -274,3 +277,47 @@ def test_append_then_read_geometry():
     assert np.array_equal(before[0], after[0]) and np.array_equal(before[1], after[1])
     with pytest.raises(IndexError):
         orc.cache_append(cache, _bits(kv_new), _bits(pe_new), [S])
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_multi_token_decode_brute_force(fmt):
+    # brute force: scores of all s tokens against all S cache rows in numpy,
+    # masked by the explicit [s, S] causal mask matrix built from positions
+    rng = np.random.default_rng(31)
+    B, S, H, s = 3, 24, 4, 3
+    cache = _rand_cache(rng, B, S, fmt)
+    ql = orc.bf16_round(rng.standard_normal((B, s, H, DC)).astype(np.float32))
+    qp = orc.bf16_round(rng.standard_normal((B, s, H, DR)).astype(np.float32))
+    ends = np.array([24, 9, 2], np.int32)          # the last sequence: token 0 has no position
+    out, lse = orc.decode_absorbed_mtp(cache, ql, qp, ends, 0.21)
+    lat = _latents(cache)
+    rot = orc.bf16_bits_to_f64(cache["pe"])
+    qlf, qpf = orc.bf16_bits_to_f64(ql), orc.bf16_bits_to_f64(qp)
+    for b in range(B):
+        T = int(ends[b])
+        pos_tok = T - s + np.arange(s)                          # positions of the new tokens
+        mask = np.arange(S)[None, :] <= pos_tok[:, None]         # [s, S]: row t visible to token j
+        mask &= np.arange(S)[None, :] < T
+        for j in range(s):
+            for h in range(H):
+                sc = 0.21 * (lat[b] @ qlf[b, j, h] + rot[b] @ qpf[b, j, h])
+                if not mask[j].any():
+                    assert lse[b, j, h] == -np.inf and np.all(out[b, j, h] == 0)
+                    continue
+                z = sc[mask[j]]
+                m = z.max()
+                w = np.exp(z - m)
+                ref = (w[:, None] * lat[b][mask[j]]).sum(0) / w.sum()
+                assert np.allclose(out[b, j, h], ref, rtol=1e-12, atol=1e-12)
+                assert lse[b, j, h] == pytest.approx(m + math.log(w.sum()), rel=1e-12, abs=1e-12)
+
+
+def test_multi_token_last_token_is_the_single_token_decode():
+    rng = np.random.default_rng(32)
+    cache = _rand_cache(rng, 2, 30)
+    ql = orc.bf16_round(rng.standard_normal((2, 2, 3, DC)).astype(np.float32))
+    qp = orc.bf16_round(rng.standard_normal((2, 2, 3, DR)).astype(np.float32))
+    ends = np.array([30, 17], np.int32)
+    out, lse = orc.decode_absorbed_mtp(cache, ql, qp, ends, 0.3)
+    o1, l1 = orc.decode_absorbed(cache, np.ascontiguousarray(ql[:, 1]), np.ascontiguousarray(qp[:, 1]), ends, 0.3)
+    assert np.array_equal(out[:, 1].reshape(-1, DC), o1) and np.array_equal(lse[:, 1].reshape(-1), l1)
