@@ -146,6 +146,30 @@ MLA_API mla_status mla_decode(const mla_cache* cache, const void* q_latent, cons
                       size_t ws_bytes, void* stream);
 
 /*
+ * mla_decode_mtp -- absorbed decode of s new tokens per sequence at once
+ * (multi-token decode: speculative or multi-token-prediction steps).  The s
+ * new rows of cache slot b are its positions end_pos[b]-s .. end_pos[b]-1
+ * (already appended); token j attends to positions 0 .. end_pos[b]-s+j, the
+ * causal mask among the step's tokens of "DeepSeek-V3.2-Exp . KV cache" (the
+ * upper-triangular -inf mask of a step with several tokens).  A token with no
+ * position gets out = 0, lse = -inf.
+ *
+ *   q_latent    device bf16 [B, s, H, 512];  q_pe  device bf16 [B, s, H, 64]
+ *   end_pos     device int32 [B]
+ *   s           1 <= s <= 16 (s = 1 is mla_decode)
+ *   out         device bf16 [B, s, H, 512];  lse  NULL or device fp32 [B, s, H]
+ *   workspace   >= mla_workspace_size(B * s, H, max_end_pos, 0) bytes
+ *   other arguments as for mla_decode (B <= cache->max_batch)
+ * The B * s (sequence, token) pairs are scheduled as sequences of their own,
+ * so the tokens of one slot read its rows in the same wave (the repeats come
+ * from L2).
+ */
+MLA_API mla_status mla_decode_mtp(const mla_cache* cache, const void* q_latent, const void* q_pe,
+                                  const int32_t* end_pos, int32_t max_end_pos, int32_t B, int32_t s,
+                                  int32_t H, float softmax_scale, void* out, float* lse,
+                                  void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * mla_decode_sparse -- the same decode restricted by the DeepSeek-V3.2 top-k
  * index mask ("DeepSeek-V3.2-Exp . KV cache", MQA-decode excerpt: a tensor of
  * -inf with zeros scattered at the top-k positions is added to the scores,

@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
             L.mla_workspace_size.restype = SZ
             L.mla_decode.argtypes = [P, P, P, P, I32, I32, I32, F, P, P, P, SZ, P]
             L.mla_decode.restype = I32
+            L.mla_decode_mtp.argtypes = [P, P, P, P, I32, I32, I32, I32, F, P, P, P, SZ, P]
+            L.mla_decode_mtp.restype = I32
             L.mla_decode_sparse.argtypes = [P, P, P, P, I32, I32, I32, F, P, I32, P, P, P, P, P,
                                             P, P, SZ, P]
             L.mla_decode_sparse.restype = I32
@@ -172,6 +174,25 @@ def decode(cache: Cache, q_latent, q_pe, end_pos, max_end_pos: int, softmax_scal
                             B, H, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
                             workspace.numel(), _stream(stream)), "mla_decode")
     return out, lse
+
+
+def decode_mtp(cache: Cache, q_latent, q_pe, end_pos, max_end_pos: int, softmax_scale: float,
+               out=None, lse=None, workspace=None, want_lse: bool = True, stream=None):
+    """Multi-token decode of s new tokens per sequence (token j of sequence b
+    attends to positions 0 .. end_pos[b]-s+j); q_latent [B,s,H,512], q_pe
+    [B,s,H,64].  Returns (out bf16 [B,s,H,512], lse fp32 [B,s,H] or None)."""
+    B, s, H, _ = q_latent.shape
+    _need(q_latent, torch.bfloat16, (B, s, H, 512), "q_latent")
+    _need(q_pe, torch.bfloat16, (B, s, H, 64), "q_pe")
+    _need(end_pos, torch.int32, (B,), "end_pos")
+    out, lse = _outputs(B * s, H, q_latent.device, None if out is None else out.view(B * s, H, 512),
+                        None if lse is None else lse.view(B * s, H), want_lse)
+    if workspace is None:
+        workspace = alloc_workspace(B * s, H, max_end_pos, 0, q_latent.device)
+    _check(lib().mla_decode_mtp(cache.ref, _ptr(q_latent), _ptr(q_pe), _ptr(end_pos),
+                                int(max_end_pos), B, s, H, float(softmax_scale), _ptr(out), _ptr(lse),
+                                _ptr(workspace), workspace.numel(), _stream(stream)), "mla_decode_mtp")
+    return out.view(B, s, H, 512), None if lse is None else lse.view(B, s, H)
 
 
 def decode_noalloc(cache: Cache, q_latent, q_pe, end_pos, max_end_pos: int, softmax_scale: float,

@@ -175,7 +175,8 @@ __global__ void __launch_bounds__(1024) sparse_prep_kernel(const int* __restrict
 // granule and grown until sum_b ceil(len_b / chunk) <= target.
 __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ end_pos,
                                                        int max_end_pos, Workspace ws, int B,
-                                                       int target, int granule, int direct) {
+                                                       int target, int granule, int direct,
+                                                       int mtp_s) {
   __shared__ int scan_smem[33];
   __shared__ unsigned long long total_len;
   __shared__ int count_smem;
@@ -192,11 +193,13 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
   for (int b = b0; b < b0 + per && b < B; ++b) {
     int len;
     if (end_pos) {
-      len = end_pos[b];
+      len = end_pos[b / mtp_s];
       if (len < 0 || len > max_end_pos) {
         atomicOr(ws.status, kDevEndPosClamped);
         len = len < 0 ? 0 : max_end_pos;
       }
+      len -= mtp_s - 1 - b % mtp_s;   // token j of the step: one position per later token fewer
+      if (len < 0) len = 0;
       ws.lengths[b] = len;
     } else {
       len = ws.lengths[b];
@@ -358,10 +361,10 @@ cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int m
 }
 
 cudaError_t launch_schedule(const int* end_pos, int max_end_pos, const Workspace& ws, int B,
-                            int target, int granule, bool direct, cudaStream_t s) {
+                            int target, int granule, bool direct, int mtp_s, cudaStream_t s) {
   const int threads = B >= 1024 ? 1024 : ((B + 31) / 32) * 32;
   return launch_pdl(schedule_kernel, dim3(1), dim3(threads), 0, s, end_pos, max_end_pos, ws, B,
-                    target, granule, direct ? 1 : 0);
+                    target, granule, direct ? 1 : 0, mtp_s < 1 ? 1 : mtp_s);
 }
 
 cudaError_t launch_combine(const Workspace& ws, int B, int H, void* out, float* lse,

@@ -17,6 +17,7 @@ constexpr int kBlk = 128;         // FP8 block width
 constexpr int kNblk = kDc / kBlk; // 4 scales per row
 constexpr int kMaxAppendB = 2048; // rows one append call may write
 constexpr int kMaxTopK = 8192;
+constexpr int kMaxMtp = 16;       // new tokens per sequence in one multi-token decode
 
 constexpr uint32_t kDevEndPosClamped = 0x1u;
 constexpr uint32_t kDevAppendSkipped = 0x2u;
@@ -115,6 +116,7 @@ struct DecodeParams {
   float* lse;             // fp32 [B, H] or null
   Workspace ws;
   int K;                  // sparse list length (0 = dense)
+  int mtp_s;              // new tokens per cache slot: sequence b reads slot b / mtp_s (1: plain decode)
 };
 
 // Raise a kernel's dynamic shared memory limit once per device.  The kernel
@@ -172,8 +174,10 @@ cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int m
 // first kernel of the call, so it clears the status word); nullptr: the
 // lengths were already written (sparse prep) and the status word cleared.
 // direct: a sequence that gets a single unit is finished by the decode kernel.
+// mtp_s > 1 (dense): B counts s sequences per cache slot; sequence b is token
+// b % s of slot b / s and attends to end_pos[b / s] - (s - 1 - b % s) positions.
 cudaError_t launch_schedule(const int* end_pos, int max_end_pos, const Workspace& ws, int B,
-                            int target_units, int granule, bool direct, cudaStream_t s);
+                            int target_units, int granule, bool direct, int mtp_s, cudaStream_t s);
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s);
 int decode_mma_granule();
 // tensor-memory path (H = 128): one CTA pair per unit

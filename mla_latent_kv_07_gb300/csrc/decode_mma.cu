@@ -101,7 +101,7 @@ template <int kFmt, bool kSparse>
 __device__ __forceinline__ void load_tile(const DecodeParams& p, const Unit& u, int tile,
                                           Smem& sm, int stage) {
   const int tid = threadIdx.x;
-  const size_t seq_row0 = (size_t)u.b * p.max_seq_len;
+  const size_t seq_row0 = (size_t)(u.b / p.mtp_s) * p.max_seq_len;   // the cache slot
   if (kFmt == 0) {
     // 32 rows x 72 chunks of 16 B (64 latent + 8 rotary)
     for (int c = tid; c < kTile * 72; c += kThreads) {

@@ -539,18 +539,19 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       const uint32_t use = i / kSlots;
       if (!wt.wait(C::kConv ? &bars->rfree[j] : &bars->empty[j], (use & 1) ^ 1)) break;
       const int e0 = u.t0 + i * kN;
+      const int slot = u.b / p.mtp_s;   // cache slot of the sequence (several per slot: multi-token)
       if (!kSparse) {
         if (lane == 0) {
           if (kFmt == 0) {
             bar_expect_tx(&bars->full[j], kOplBytes + kOpeBytes);
             for (int blk = 0; blk < 4; ++blk)
-              tma3(opl(j) + blk * kBlkBytes, &tp.m_kv, rank * kHalf + blk * 64, e0, u.b, &bars->full[j]);
-            tma3(ope(j), &tp.m_pe, 0, e0, u.b, &bars->full[j]);
+              tma3(opl(j) + blk * kBlkBytes, &tp.m_kv, rank * kHalf + blk * 64, e0, slot, &bars->full[j]);
+            tma3(ope(j), &tp.m_pe, 0, e0, slot, &bars->full[j]);
           } else {
             bar_expect_tx(&bars->full[j], kN * kHalf + kN * 16 + kN * 128);
-            tma3(raw(j), &tp.m_kv, rank * kHalf, e0, u.b, &bars->full[j]);
-            tma3(rsc(j), &tp.m_sc, 0, e0, u.b, &bars->full[j]);
-            tma3(rpe(j), &tp.m_pe, 0, e0, u.b, &bars->full[j]);
+            tma3(raw(j), &tp.m_kv, rank * kHalf, e0, slot, &bars->full[j]);
+            tma3(rsc(j), &tp.m_sc, 0, e0, slot, &bars->full[j]);
+            tma3(rpe(j), &tp.m_pe, 0, e0, slot, &bars->full[j]);
           }
         }
       } else {
@@ -1027,6 +1028,7 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s) {
   memset(&tp, 0, sizeof(tp));
   tp.p = p;
   const uint64_t S = (uint64_t)p.max_seq_len, B = (uint64_t)p.B;
+  const uint64_t slots = (uint64_t)(p.B / p.mtp_s);   // cache slots the dense maps cover
   const uint32_t n = (uint32_t)decode_tc_granule(p.fmt, p.K > 0);   // tile rows
   bool ok = true;
   if (p.K) {
@@ -1039,16 +1041,16 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s) {
                                      rows, kNblk));
   } else {
     if (p.fmt == 0) {
-      ok = encode3(&tp.m_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.kv, kDc, S, B, 64, n,
+      ok = encode3(&tp.m_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.kv, kDc, S, slots, 64, n,
                    CU_TENSOR_MAP_SWIZZLE_128B);
     } else {
-      ok = encode3(&tp.m_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.kv, kDc, S, B, kHalf, n,
+      ok = encode3(&tp.m_kv, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, p.kv, kDc, S, slots, kHalf, n,
                    CU_TENSOR_MAP_SWIZZLE_NONE) &&
-           encode3(&tp.m_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.kv_scale, kNblk, S, B, kNblk, n,
+           encode3(&tp.m_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.kv_scale, kNblk, S, slots, kNblk, n,
                    CU_TENSOR_MAP_SWIZZLE_NONE);
     }
     // bf16: straight into the operand layout; FP8: plain rows for the converter
-    ok = ok && encode3(&tp.m_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.pe, kDr, S, B, 64, n,
+    ok = ok && encode3(&tp.m_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.pe, kDr, S, slots, 64, n,
                        p.fmt == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   ok = ok &&

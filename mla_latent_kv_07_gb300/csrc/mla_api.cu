@@ -93,13 +93,14 @@ struct DecodeArgs {
   float* lse;
   void* workspace;
   size_t ws_bytes;
+  int32_t mtp_s;   // new tokens per sequence; B counts B / mtp_s cache slots x mtp_s
 };
 
 mla_status check_decode(const DecodeArgs& a, int K, mla::Workspace* ws) {
   mla_status st = check_cache(a.cache);
   if (st != MLA_OK) return st;
   if (!supported_heads(a.H)) return MLA_ERR_UNSUPPORTED;
-  if (a.B <= 0 || a.B > a.cache->max_batch) return MLA_ERR_INVALID_ARG;
+  if (a.B <= 0 || a.B / a.mtp_s > a.cache->max_batch) return MLA_ERR_INVALID_ARG;
   if (a.max_end_pos <= 0 || a.max_end_pos > a.cache->max_seq_len) return MLA_ERR_OUT_OF_RANGE;
   if (!a.q_latent || !a.q_pe || !a.end_pos || !a.out) return MLA_ERR_INVALID_ARG;
   if (!aligned16(a.q_latent) || !aligned16(a.q_pe) || !aligned16(a.out) || !aligned4(a.end_pos))
@@ -130,6 +131,7 @@ mla::DecodeParams make_params(const DecodeArgs& a, const mla::Workspace& ws, int
   p.lse = a.lse;
   p.ws = ws;
   p.K = K;
+  p.mtp_s = a.mtp_s;
   return p;
 }
 
@@ -153,7 +155,8 @@ mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cuda
   cudaError_t e = mla::launch_schedule(
       K ? nullptr : a.end_pos, a.max_end_pos, ws, a.B,
       tc ? mla::decode_tc_units(a.cache->fmt, K > 0, sms) : mla::target_units_mma(a.H, sms),
-      tc ? mla::decode_tc_granule(a.cache->fmt, K > 0) : mla::decode_mma_granule(), tc, s);
+      tc ? mla::decode_tc_granule(a.cache->fmt, K > 0) : mla::decode_mma_granule(), tc, a.mtp_s,
+      s);
   if (e != cudaSuccess) return cuda_fail(e, "schedule");
   const bool traced = trace_start(s);
   e = tc ? mla::launch_decode_tc(make_params(a, ws, K), s)
@@ -210,11 +213,26 @@ mla_status mla_decode(const mla_cache* cache, const void* q_latent, const void* 
                       size_t ws_bytes, void* stream) {
   g_last_error[0] = 0;
   DecodeArgs a{cache, q_latent, q_pe, end_pos, max_end_pos, B, H, softmax_scale, out, lse,
-               workspace, ws_bytes};
+               workspace, ws_bytes, 1};
   mla::Workspace ws;
   mla_status st = check_decode(a, 0, &ws);
   if (st != MLA_OK) return st;
   // the schedule kernel, first of the dense call, clears the status word
+  return run_decode(a, ws, 0, static_cast<cudaStream_t>(stream));
+}
+
+mla_status mla_decode_mtp(const mla_cache* cache, const void* q_latent, const void* q_pe,
+                          const int32_t* end_pos, int32_t max_end_pos, int32_t B, int32_t s,
+                          int32_t H, float softmax_scale, void* out, float* lse, void* workspace,
+                          size_t ws_bytes, void* stream) {
+  g_last_error[0] = 0;
+  if (s < 1 || s > mla::kMaxMtp || B <= 0 || B > (1 << 30) / s) return MLA_ERR_INVALID_ARG;
+  // B * s sequences; sequence b * s + j is token j of cache slot b
+  DecodeArgs a{cache, q_latent, q_pe, end_pos, max_end_pos, B * s, H, softmax_scale, out, lse,
+               workspace, ws_bytes, s};
+  mla::Workspace ws;
+  mla_status st = check_decode(a, 0, &ws);
+  if (st != MLA_OK) return st;
   return run_decode(a, ws, 0, static_cast<cudaStream_t>(stream));
 }
 
@@ -233,7 +251,7 @@ mla_status mla_decode_sparse(const mla_cache* cache, const void* q_latent, const
   if ((gidx_out && !aligned4(gidx_out)) || (gcount_out && !aligned4(gcount_out)))
     return MLA_ERR_INVALID_ARG;
   DecodeArgs a{cache, q_latent, q_pe, end_pos, max_end_pos, B, H, softmax_scale, out, lse,
-               workspace, ws_bytes};
+               workspace, ws_bytes, 1};
   mla::Workspace ws;
   mla_status st = check_decode(a, K, &ws);
   if (st != MLA_OK) return st;

@@ -136,3 +136,16 @@ def test_read_ceiling_rejects_bad_arguments(L):
     assert L.mla_read_ceiling(f, 1000, f, None) == 1          # not a multiple of 16
     assert L.mla_read_ceiling(ctypes.c_void_p(FAKE + 8), 1024, f, None) == 1
     assert L.mla_read_ceiling(f, 1024, None, None) == 1
+
+
+def test_multi_token_decode_rejects_bad_arguments(L):
+    c = _cache(fmt=0, B=2, S=64)
+    f = ctypes.c_void_p(FAKE)
+
+    def mtp(B=2, s=2, H=128):
+        return L.mla_decode_mtp(ctypes.byref(c), f, f, f, 64, B, s, H, 0.1, f, None, f, 1 << 30, None)
+
+    assert mtp(s=0) == 1
+    assert mtp(s=17) == 1
+    assert mtp(B=3) == 1                                    # more slots than the cache holds
+    assert mtp(H=24) == 3

@@ -170,6 +170,32 @@ def test_read_ceiling_reads_every_word():
     assert int(sink.cpu().numpy().view(np.uint32)[0]) == int(np.bitwise_xor.reduce(words))
 
 
+# ------------------------------------------------------ multi-token decode
+
+@pytest.mark.parametrize("fmt,H,s", [(0, 128, 2), (1, 128, 3), (0, 16, 2), (1, 64, 4)])
+def test_multi_token_decode_all_outputs(fmt, H, s):
+    B, S = 3, 300
+    oc = oracle_cache(_rand_bf16((B, S, 512), 101), _rand_bf16((B, S, 64), 102), fmt)
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((B, s, H, 512), 103), _rand_bf16((B, s, H, 64), 104)
+    ends = np.array([300, 97, 2], np.int32)      # the last: the first tokens see nothing or one row
+    out, lse = mla.decode_mtp(dc, ql.cuda(), qp.cuda(), torch.from_numpy(ends).cuda(), S, 0.14)
+    ref, ref_lse = orc.decode_absorbed_mtp(oc, bits(ql), bits(qp), ends, 0.14)
+    check_close(f64(out).reshape(-1, 512), ref.reshape(-1, 512), "out")
+    check_close(f64(lse).reshape(-1), ref_lse.reshape(-1), "lse")
+
+
+def test_multi_token_decode_with_one_token_is_the_decode():
+    B, S, H = 2, 160, 128
+    oc = oracle_cache(_rand_bf16((B, S, 512), 111), _rand_bf16((B, S, 64), 112), 1)
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((B, H, 512), 113), _rand_bf16((B, H, 64), 114)
+    ends = torch.tensor([160, 61], dtype=torch.int32).cuda()
+    o1, l1 = mla.decode(dc, ql.cuda(), qp.cuda(), ends, S, 0.2)
+    om, lm = mla.decode_mtp(dc, ql.view(B, 1, H, 512).cuda(), qp.view(B, 1, H, 64).cuda(), ends, S, 0.2)
+    assert torch.equal(o1, om.view(B, H, 512)) and torch.equal(l1, lm.view(B, H))
+
+
 # ---------------------------------------------------------- small sparse
 
 def test_sparse_small_lists_and_outputs():
