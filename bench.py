@@ -8,7 +8,7 @@ timed region.  The timed region is one CUDA-graph launch holding exactly K
 steps; successive steps rotate over cache copies (or top-k lists) so that each
 step's working set is not served from L2.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..6]
     python bench.py --impl reference ...     # the CPU oracle, same metric
 
 Prints one JSON line (rank 0).  Under torchrun every rank runs its own
@@ -168,7 +168,8 @@ class Setup:
         self.ends = inputs.end_positions(w).to(device)
         self.ends_host = self.ends.cpu().tolist()
         self.tokens = sum(min(t, w.topk) if w.topk else t for t in self.ends_host)
-        self.ql, self.qp = g((w.B, w.H, 512), inputs.T_QL), g((w.B, w.H, 64), inputs.T_QP)
+        lead = (w.B, w.H) if w.mtp == 1 else (w.B, w.mtp, w.H)
+        self.ql, self.qp = g(lead + (512,), inputs.T_QL), g(lead + (64,), inputs.T_QP)
         self.kv_new, self.pe_new = g((w.B, 512), inputs.T_KVNEW), g((w.B, 64), inputs.T_PENEW)
         step_bytes = layout.step_bytes(self.tokens, w.B, w.H, w.fmt)
         l2 = torch.cuda.get_device_properties(device).L2_cache_size
@@ -186,10 +187,11 @@ class Setup:
             self.topks = None
             self.rotation = f"{self.rot} cache copies ({self.rot * step_bytes / 1e6:.0f} MB read)"
         self.l2_bytes = l2
-        self.out = torch.empty((w.B, w.H, 512), dtype=torch.bfloat16, device=device)
-        self.lse = torch.empty((w.B, w.H), dtype=torch.float32, device=device)
-        self.ws = mla.alloc_workspace(w.B, w.H, w.S, w.topk, device)
-        self.start_pos = [t - 1 for t in self.ends_host]
+        self.out = torch.empty(lead + (512,), dtype=torch.bfloat16, device=device)
+        self.lse = torch.empty(lead, dtype=torch.float32, device=device)
+        self.ws = mla.alloc_workspace(w.B * w.mtp, w.H, w.S, w.topk, device)
+        # the step's new rows: positions end_pos - mtp .. end_pos - 1
+        self.start_pos = [[t - w.mtp + j for t in self.ends_host] for j in range(w.mtp)]
 
     def _make_cache(self, g):
         w = self.w
@@ -227,9 +229,14 @@ class Setup:
                               out=self.out, lse=self.lse, workspace=self.ws)
         else:
             c = self.caches[i % self.rot]
-            mla.cache_append(c, self.kv_new, self.pe_new, self.start_pos)
-            mla.decode(c, self.ql, self.qp, self.ends, w.S, w.softmax_scale, out=self.out,
-                       lse=self.lse, workspace=self.ws)
+            for sp in self.start_pos:
+                mla.cache_append(c, self.kv_new, self.pe_new, sp)
+            if w.mtp > 1:
+                mla.decode_mtp(c, self.ql, self.qp, self.ends, w.S, w.softmax_scale, out=self.out,
+                               lse=self.lse, workspace=self.ws)
+            else:
+                mla.decode(c, self.ql, self.qp, self.ends, w.S, w.softmax_scale, out=self.out,
+                           lse=self.lse, workspace=self.ws)
 
 
 # --------------------------------------------------------------- GPU arm
@@ -358,12 +365,12 @@ def run_gpu(args, rank, world, local_rank):
     step_s = ms / 1e3 / K
     cache_bytes = st.tokens * layout.cache_bytes_per_token(w.fmt)
     value = whole_job_rate(cache_bytes, world, step_s) / 1e12
-    tokens_per_s = whole_job_rate(w.B, world, step_s)
+    tokens_per_s = whole_job_rate(w.B * w.mtp, world, step_s)
 
     # dominant kernel: the decode kernel, timed by its own events
     kern_s = kern_ms / 1e3 / max(timed, 1)
     pk, pk_src = peaks()
-    flops = layout.step_flops(st.tokens, w.H)
+    flops = layout.step_flops(st.tokens, w.H) * w.mtp   # every new token attends (about) all positions
     t_hbm = cache_bytes / (pk["hbm_gbs"] * 1e9)
     t_tc = flops / (pk["bf16_tflops"] * 1e12)
     if t_hbm >= t_tc:
@@ -391,8 +398,10 @@ def run_gpu(args, rank, world, local_rank):
         "data": "synthetic (seeded N(0,1) bf16; FP8 cache quantised by the library's append)",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "end_pos": w.T or f"U[{w.T_lo},{w.T_hi}]",
                    "attended_positions": st.tokens, "cache": "bf16" if w.fmt == 0 else "fp8-e4m3/128",
-                   "topk": w.topk or None, "step": "append new row + decode" if not w.topk
-                   else "fused append + top-k gather decode",
+                   "topk": w.topk or None, "mtp": w.mtp,
+                   "step": ("fused append + top-k gather decode" if w.topk else
+                            "append new row + decode" if w.mtp == 1 else
+                            f"append {w.mtp} new rows + multi-token decode (each cache position counted once)"),
                    "l2": f"inputs larger than L2: rotating {st.rotation}; L2 {st.l2_bytes / 1e6:.0f} MB",
                    "timing": "CUDA graph of exactly K steps, CUDA events on its stream",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
@@ -436,9 +445,14 @@ def run_e2e(st: Setup, K: int, W: int):
                               lse=st.lse, workspace=st.ws)
         else:
             c = st.caches[i % st.rot]
-            mla.cache_append(c, dev["kv_new"], dev["pe_new"], st.start_pos)
-            mla.decode(c, dev["ql"], dev["qp"], dev["ends"], w.S, w.softmax_scale, out=st.out,
-                       lse=st.lse, workspace=st.ws)
+            for sp in st.start_pos:
+                mla.cache_append(c, dev["kv_new"], dev["pe_new"], sp)
+            if w.mtp > 1:
+                mla.decode_mtp(c, dev["ql"], dev["qp"], dev["ends"], w.S, w.softmax_scale, out=st.out,
+                               lse=st.lse, workspace=st.ws)
+            else:
+                mla.decode(c, dev["ql"], dev["qp"], dev["ends"], w.S, w.softmax_scale, out=st.out,
+                           lse=st.lse, workspace=st.ws)
         out_h.copy_(st.out, non_blocking=True)
         lse_h.copy_(st.lse, non_blocking=True)
 
@@ -474,8 +488,9 @@ def oracle_sample(w: inputs.Workload, budget_s: float):
         cache["kv"] = inputs.bf16_bits(kv)
     else:
         cache["kv"], cache["kv_scale"] = orc.quantize_rows(inputs.bf16_bits(kv))
-    ql = inputs.randn_bf16((1, w.H, 512), 1000 * w.index + inputs.T_QL)
-    qp = inputs.randn_bf16((1, w.H, 64), 1000 * w.index + inputs.T_QP)
+    lead = (1, w.H) if w.mtp == 1 else (1, w.mtp, w.H)
+    ql = inputs.randn_bf16(lead + (512,), 1000 * w.index + inputs.T_QL)
+    qp = inputs.randn_bf16(lead + (64,), 1000 * w.index + inputs.T_QP)
     topk = None
     if w.topk:
         topk = inputs.topk_indices(1, w.topk, [int(ends[0])], 1000 * w.index + inputs.T_TOPK).numpy()
@@ -487,7 +502,10 @@ def oracle_sample(w: inputs.Workload, budget_s: float):
 def time_oracle_step(sample, w):
     orc, cache, ql, qp, T, topk, tokens = sample
     t0 = time.perf_counter()
-    orc.decode_absorbed(cache, ql, qp, [T], w.softmax_scale, topk=topk)
+    if w.mtp > 1:
+        orc.decode_absorbed_mtp(cache, ql, qp, [T], w.softmax_scale)
+    else:
+        orc.decode_absorbed(cache, ql, qp, [T], w.softmax_scale, topk=topk)
     return time.perf_counter() - t0, tokens
 
 

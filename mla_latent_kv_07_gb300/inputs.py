@@ -42,6 +42,7 @@ class Workload:
     T_hi: int = 0
     topk: int = 0         # 0: dense decode
     append: bool = False  # a new row is appended at end_pos - 1 before decoding
+    mtp: int = 1          # new tokens per sequence decoded at once (multi-token decode)
     notes: dict = field(default_factory=dict)
 
 
@@ -56,6 +57,9 @@ WORKLOADS = {
                 softmax_scale=SCALE_YARN, T=131072),
     5: Workload(5, "sparse_b16_h128_t32768_k2048_fp8", B=16, H=128, S=32768, fmt=1,
                 softmax_scale=SCALE_YARN, T=32768, topk=2048, append=True),
+    # beyond the headline table: workload 2 with two new tokens per sequence
+    6: Workload(6, "mtp2_b8_h128_t4096_bf16", B=8, H=128, S=4096, fmt=0, softmax_scale=SCALE_YARN,
+                T=4096, mtp=2),
 }
 
 
@@ -96,9 +100,11 @@ def topk_indices(B: int, K: int, end_pos, seed: int) -> torch.Tensor:
 
 
 def queries(w: Workload, device="cpu", H: int | None = None):
+    """q_latent, q_pe: [B, H, .] (or [B, mtp, H, .] for a multi-token workload)."""
     H = H or w.H
-    ql = randn_bf16((w.B, H, DC), 1000 * w.index + T_QL, device)
-    qp = randn_bf16((w.B, H, DR), 1000 * w.index + T_QP, device)
+    lead = (w.B, H) if w.mtp == 1 else (w.B, w.mtp, H)
+    ql = randn_bf16(lead + (DC,), 1000 * w.index + T_QL, device)
+    qp = randn_bf16(lead + (DR,), 1000 * w.index + T_QP, device)
     return ql, qp
 
 
