@@ -244,6 +244,29 @@ def decode_absorbed_mtp(cache: dict, q_latent, q_pe, end_pos, softmax_scale: flo
     return out, lse
 
 
+def _f64(x):
+    x = np.asarray(x)
+    return bf16_bits_to_f64(x) if x.dtype == np.uint16 else x.astype(np.float64)
+
+
+def absorb_q(q_nope, wkv_b):
+    """fp64 q_latent[b, h, c] = sum_n q_nope[b, h, n] * W_UK[h, n, c], with
+    W_UK[h] = wkv_b[h, 0:128, :] ("DeepSeek MLA architecture ...", section 4:
+    the key up-projection folded into the query).  Inputs: bf16 bits or floats."""
+    q = _f64(q_nope)
+    w = _f64(wkv_b)
+    return np.einsum("bhn,hnc->bhc", q, w[:, :128, :])
+
+
+def project_out(x, wkv_b):
+    """fp64 o[b, h, v] = sum_c W_UV[h, v, c] * x[b, h, c], with W_UV[h] =
+    wkv_b[h, 128:256, :] (the value up-projection applied after the latent
+    attention).  Inputs: bf16 bits or floats."""
+    xx = _f64(x)
+    w = _f64(wkv_b)
+    return np.einsum("bhc,hvc->bhv", xx, w[:, 128:, :])
+
+
 def decode_naive(cache: dict, wkv_b, q_nope, q_pe, end_pos, softmax_scale: float):
     """fp64 non-absorbed MHA: keys/values expanded through wkv_b [H, 256, 512].
 

@@ -14,7 +14,10 @@ What fixes the answers here, independent of the oracle's own code:
     0..1,000;
   * multi-token decode: a brute-force float64 attention with the explicit
     causal mask matrix over the step's s tokens (token j at position
-    T-s+j sees positions 0..T-s+j).
+    T-s+j sees positions 0..T-s+j);
+  * the per-head products around the decode: identity weights, a brute-force
+    loop, and query absorption + latent decode + value projection equal to
+    the non-absorbed MHA over W_UK / W_UV-expanded keys and values.
 """
 import math
 
@@ -321,3 +324,52 @@ def test_multi_token_last_token_is_the_single_token_decode():
     out, lse = orc.decode_absorbed_mtp(cache, ql, qp, ends, 0.3)
     o1, l1 = orc.decode_absorbed(cache, np.ascontiguousarray(ql[:, 1]), np.ascontiguousarray(qp[:, 1]), ends, 0.3)
     assert np.array_equal(out[:, 1].reshape(-1, DC), o1) and np.array_equal(lse[:, 1].reshape(-1), l1)
+
+
+def test_absorb_and_project_identity_weights():
+    rng = np.random.default_rng(41)
+    B, H = 2, 3
+    w = np.zeros((H, 256, DC), np.float64)
+    w[:, np.arange(128), np.arange(128)] = 1.0            # W_UK[h] = [I | 0]
+    w[:, 128 + np.arange(128), 128 + np.arange(128)] = 1.0  # W_UV[h] picks c = 128..255
+    qn = rng.standard_normal((B, H, 128))
+    ql = orc.absorb_q(qn, w)
+    assert np.array_equal(ql[..., :128], qn) and np.all(ql[..., 128:] == 0)
+    x = rng.standard_normal((B, H, DC))
+    assert np.array_equal(orc.project_out(x, w), x[..., 128:256])
+
+
+def test_absorb_and_project_brute_force():
+    rng = np.random.default_rng(42)
+    B, H = 2, 2
+    w = orc.bf16_round(rng.standard_normal((H, 256, DC)).astype(np.float32))
+    qn = orc.bf16_round(rng.standard_normal((B, H, 128)).astype(np.float32))
+    x = orc.bf16_round(rng.standard_normal((B, H, DC)).astype(np.float32))
+    wf, qf, xf = (orc.bf16_bits_to_f64(a) for a in (w, qn, x))
+    ql, o = orc.absorb_q(qn, w), orc.project_out(x, w)
+    for b in range(B):
+        for h in range(H):
+            for c in (0, 77, 511):
+                ref = sum(qf[b, h, n] * wf[h, n, c] for n in range(128))
+                assert ql[b, h, c] == pytest.approx(ref, rel=1e-12, abs=1e-12)
+            for v in (0, 64, 127):
+                ref = sum(wf[h, 128 + v, c] * xf[b, h, c] for c in range(DC))
+                assert o[b, h, v] == pytest.approx(ref, rel=1e-12, abs=1e-12)
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_absorbed_pipeline_equals_naive_mha(fmt):
+    # q_nope -> absorb -> latent decode -> project equals attention over the
+    # expanded keys W_UK c_t and values W_UV c_t (section 4 of the MLA page)
+    rng = np.random.default_rng(43)
+    B, S, H = 2, 20, 3
+    cache = _rand_cache(rng, B, S, fmt)
+    w = rng.standard_normal((H, 256, DC)) * 0.05
+    qn = rng.standard_normal((B, H, 128))
+    qp = orc.bf16_round(rng.standard_normal((B, H, DR)).astype(np.float32))
+    ends = np.array([20, 7], np.int32)
+    ql = orc.absorb_q(qn, w)
+    out, _ = orc.decode_absorbed(cache, ql, qp, ends, 0.2)
+    o = orc.project_out(out.reshape(B, H, DC), w)
+    o_naive, _ = orc.decode_naive(cache, w, qn, qp, ends, 0.2)
+    assert np.allclose(o, o_naive, rtol=1e-10, atol=1e-10)
