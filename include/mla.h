@@ -253,6 +253,31 @@ MLA_API mla_status mla_trace_end(float* main_kernel_ms, int32_t* timed_launches,
                                  int32_t* kernel_launches);
 
 /*
+ * mla_absorb_q -- the query side of the absorbed attention ("DeepSeek MLA
+ * architecture ...", section 4: W_UK folded into the query):
+ *   q_latent[b, h, c] = sum_n q_nope[b, h, n] * W_UK[h][n][c]
+ * mla_project_out -- the value side (W_UV applied after the latent-space
+ * attention):
+ *   o[b, h, v] = sum_c W_UV[h][v][c] * x[b, h, c]
+ * wkv_b is the per-head up-projection of "DeepSeek-V3.2-Exp . KV cache",
+ * device bf16 [H, 256, 512]: rows 0..127 of head h are W_UK[h] (n x c), rows
+ * 128..255 are W_UV[h] (v x c).
+ *
+ *   q_nope    device bf16 [B, H, 128]    q_latent  device bf16 [B, H, 512]
+ *   x         device bf16 [B, H, 512] (e.g. the decode's out)
+ *   o         device bf16 [B, H, 128]
+ *   status    NULL or a device uint32 that receives MLA_DEV_PIPELINE_TIMEOUT if a
+ *             bounded wait expired (the affected outputs are then not written)
+ * Products accumulate in fp32 and are rounded to bf16 once.  All pointers
+ * 16-byte aligned (status 4-byte), 1 <= B <= 2^22, 1 <= H <= 2^16; otherwise
+ * MLA_ERR_INVALID_ARG.  Asynchronous on `stream`.
+ */
+MLA_API mla_status mla_absorb_q(const void* q_nope, const void* wkv_b, int32_t B, int32_t H,
+                                void* q_latent, uint32_t* status, void* stream);
+MLA_API mla_status mla_project_out(const void* x, const void* wkv_b, int32_t B, int32_t H, void* o,
+                                   uint32_t* status, void* stream);
+
+/*
  * mla_read_ceiling -- stream `bytes` of device memory at `buf` and XOR-fold
  * them into *sink (a measurement aid with no counterpart on the pages: the
  * HBM read rate this device achieves with plain 16-byte streaming loads, the

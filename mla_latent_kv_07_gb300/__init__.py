@@ -73,6 +73,10 @@ def lib() -> ctypes.CDLL:
             L.mla_last_error.restype = ctypes.c_char_p
             L.mla_decode_noalloc.argtypes = [P, P, P, P, I32, I32, I32, F, P, P, P]
             L.mla_decode_noalloc.restype = I32
+            L.mla_absorb_q.argtypes = [P, P, I32, I32, P, P, P]
+            L.mla_absorb_q.restype = I32
+            L.mla_project_out.argtypes = [P, P, I32, I32, P, P, P]
+            L.mla_project_out.restype = I32
             L.mla_read_ceiling.argtypes = [P, SZ, P, P]
             L.mla_read_ceiling.restype = I32
             L.mla_trace_begin.argtypes = [I32]
@@ -241,6 +245,34 @@ def workspace_status(workspace, stream=None) -> int:
     _check(lib().mla_workspace_status(_ptr(workspace), ctypes.byref(flags), _stream(stream)),
            "mla_workspace_status")
     return int(flags.value)
+
+
+def absorb_q(q_nope, wkv_b, out=None, status=None, stream=None):
+    """q_latent [B,H,512] bf16 = q_nope [B,H,128] . W_UK (rows 0..127 of each
+    head of wkv_b [H,256,512] bf16)."""
+    B, H, _ = q_nope.shape
+    _need(q_nope, torch.bfloat16, (B, H, 128), "q_nope")
+    _need(wkv_b, torch.bfloat16, (H, 256, 512), "wkv_b")
+    if out is None:
+        out = torch.empty((B, H, 512), dtype=torch.bfloat16, device=q_nope.device)
+    _need(out, torch.bfloat16, (B, H, 512), "out")
+    _check(lib().mla_absorb_q(_ptr(q_nope), _ptr(wkv_b), B, H, _ptr(out), _ptr(status), _stream(stream)),
+           "mla_absorb_q")
+    return out
+
+
+def project_out(x, wkv_b, out=None, status=None, stream=None):
+    """o [B,H,128] bf16 = W_UV . x for x [B,H,512] bf16 (W_UV: rows 128..255
+    of each head of wkv_b)."""
+    B, H, _ = x.shape
+    _need(x, torch.bfloat16, (B, H, 512), "x")
+    _need(wkv_b, torch.bfloat16, (H, 256, 512), "wkv_b")
+    if out is None:
+        out = torch.empty((B, H, 128), dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, (B, H, 128), "out")
+    _check(lib().mla_project_out(_ptr(x), _ptr(wkv_b), B, H, _ptr(out), _ptr(status), _stream(stream)),
+           "mla_project_out")
+    return out
 
 
 def read_ceiling(buf: torch.Tensor, sink: torch.Tensor, stream=None) -> None:

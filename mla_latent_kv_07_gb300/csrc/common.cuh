@@ -189,6 +189,12 @@ bool decode_tc_supported(int H);
 int decode_tc_units(int fmt, bool sparse, int num_sms);
 cudaError_t launch_combine(const Workspace& ws, int B, int H, void* out, float* lse,
                            cudaStream_t s);
+// per-head products around the decode (absorb.cu): q_latent = q_nope . W_UK,
+// o = W_UV . x, with wkv_b [H, 256, 512] bf16 holding W_UK and W_UV per head
+cudaError_t launch_absorb_q(const void* q_nope, const void* wkv_b, int B, int H, void* q_latent,
+                            uint32_t* status, cudaStream_t s);
+cudaError_t launch_project_out(const void* x, const void* wkv_b, int B, int H, void* o,
+                               uint32_t* status, cudaStream_t s);
 // streams `bytes` (a multiple of 16) of device memory, XOR-folding into *sink
 cudaError_t launch_read_ceiling(const void* buf, size_t bytes, uint32_t* sink, int sms, cudaStream_t s);
 

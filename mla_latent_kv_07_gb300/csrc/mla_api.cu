@@ -169,6 +169,13 @@ mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cuda
   return MLA_OK;
 }
 
+mla_status check_absorb(const void* x, const void* wkv_b, int32_t B, int32_t H, const void* y,
+                        const uint32_t* status) {
+  if (!x || !wkv_b || !y || !aligned16(x) || !aligned16(wkv_b) || !aligned16(y)) return MLA_ERR_INVALID_ARG;
+  if (status && !aligned4(status)) return MLA_ERR_INVALID_ARG;
+  if (B <= 0 || H <= 0 || B > (1 << 22) || H > (1 << 16)) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
 }  // namespace
 
 extern "C" {
@@ -286,6 +293,28 @@ mla_status mla_workspace_status(const void* workspace, uint32_t* flags, void* st
   cudaError_t e = cudaMemcpyAsync(flags, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   return e == cudaSuccess ? MLA_OK : cuda_fail(e, "status");
+}
+
+mla_status mla_absorb_q(const void* q_nope, const void* wkv_b, int32_t B, int32_t H, void* q_latent,
+                        uint32_t* status, void* stream) {
+  g_last_error[0] = 0;
+  mla_status st = check_absorb(q_nope, wkv_b, B, H, q_latent, status);
+  if (st != MLA_OK) return st;
+  cudaError_t e = mla::launch_absorb_q(q_nope, wkv_b, B, H, q_latent, status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "absorb_q");
+  trace_launches(1);
+  return MLA_OK;
+}
+
+mla_status mla_project_out(const void* x, const void* wkv_b, int32_t B, int32_t H, void* o,
+                           uint32_t* status, void* stream) {
+  g_last_error[0] = 0;
+  mla_status st = check_absorb(x, wkv_b, B, H, o, status);
+  if (st != MLA_OK) return st;
+  cudaError_t e = mla::launch_project_out(x, wkv_b, B, H, o, status, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "project_out");
+  trace_launches(1);
+  return MLA_OK;
 }
 
 mla_status mla_read_ceiling(const void* buf, size_t bytes, uint32_t* sink, void* stream) {

@@ -149,3 +149,14 @@ def test_multi_token_decode_rejects_bad_arguments(L):
     assert mtp(s=17) == 1
     assert mtp(B=3) == 1                                    # more slots than the cache holds
     assert mtp(H=24) == 3
+
+
+def test_absorb_and_project_reject_bad_arguments(L):
+    f = ctypes.c_void_p(FAKE)
+    odd = ctypes.c_void_p(FAKE + 8)
+    for fn in (L.mla_absorb_q, L.mla_project_out):
+        assert fn(None, f, 4, 8, f, None, None) == 1
+        assert fn(f, odd, 4, 8, f, None, None) == 1          # misaligned weights
+        assert fn(f, f, 0, 8, f, None, None) == 1
+        assert fn(f, f, 4, 0, f, None, None) == 1
+        assert fn(f, f, 4, 8, f, ctypes.c_void_p(FAKE + 2), None) == 1   # misaligned status
