@@ -63,7 +63,7 @@ def decode_path(H: int) -> str:
 def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     src = "decode_tc.cu" if kernel == "decode_tc_kernel" else "decode_mma.cu"
-    for name in (src, "common.cuh"):
+    for name in (src, "common.cuh", "tc_ptx.cuh"):
         with open(os.path.join(ROOT, "mla_latent_kv_07_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -190,6 +190,9 @@ class Setup:
         self.out = torch.empty(lead + (512,), dtype=torch.bfloat16, device=device)
         self.lse = torch.empty(lead, dtype=torch.float32, device=device)
         self.ws = mla.alloc_workspace(w.B * w.mtp, w.H, w.S, w.topk, device)
+        if w.absorb:
+            self.q_nope, self.wkv_b = (t.to(device) for t in inputs.absorb_inputs(w))
+            self.o = torch.empty((w.B, w.H, 128), dtype=torch.bfloat16, device=device)
         # the step's new rows: positions end_pos - mtp .. end_pos - 1
         self.start_pos = [[t - w.mtp + j for t in self.ends_host] for j in range(w.mtp)]
 
@@ -231,12 +234,16 @@ class Setup:
             c = self.caches[i % self.rot]
             for sp in self.start_pos:
                 mla.cache_append(c, self.kv_new, self.pe_new, sp)
+            if w.absorb:
+                mla.absorb_q(self.q_nope, self.wkv_b, out=self.ql)
             if w.mtp > 1:
                 mla.decode_mtp(c, self.ql, self.qp, self.ends, w.S, w.softmax_scale, out=self.out,
                                lse=self.lse, workspace=self.ws)
             else:
                 mla.decode(c, self.ql, self.qp, self.ends, w.S, w.softmax_scale, out=self.out,
                            lse=self.lse, workspace=self.ws)
+            if w.absorb:
+                mla.project_out(self.out, self.wkv_b, out=self.o)
 
 
 # --------------------------------------------------------------- GPU arm
@@ -301,6 +308,47 @@ def run_warm(st, stream, steps: int = 200):
     return {"step_us": round(e0.elapsed_time(e1) * 1e3 / steps, 3),
             "kernel_us": round(kern_ms * 1e3 / max(timed, 1), 3),
             "note": "one cache resident in L2 (warm); the headline is the cold, rotated number"}
+
+
+def run_gemms(st, stream, reps: int = 200):
+    """The query absorption and value projection timed on their own: `reps`
+    launches of each captured in a CUDA graph (launches back to back), CUDA
+    events around the replay, cycling through copies of wkv_b that together
+    exceed twice the L2 (every launch reads its weights from HBM).
+    Algorithmic bytes: one head-half of wkv_b (H x 128 x 512 bf16) plus the
+    activations in and out."""
+    w = st.w
+    pk, src = peaks()
+    nw = max(1, math.ceil(2 * st.l2_bytes / (st.wkv_b.numel() * 2)))
+    wcopies = [st.wkv_b] + [st.wkv_b.clone() for _ in range(nw - 1)]
+    res = {}
+    for name, call, act in (
+            ("absorb_q", lambda wk: mla.absorb_q(st.q_nope, wk, out=st.ql, stream=stream),
+             w.B * w.H * (128 + 512) * 2),
+            ("project_out", lambda wk: mla.project_out(st.out, wk, out=st.o, stream=stream),
+             w.B * w.H * (512 + 128) * 2)):
+        with torch.cuda.stream(stream):
+            for i in range(3):
+                call(wcopies[i % nw])
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(reps):
+                call(wcopies[i % nw])
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        t = e0.elapsed_time(e1) / 1e3 / reps
+        nbytes = w.H * 128 * 512 * 2 + act
+        res[name] = {"us": round(t * 1e6, 3), "bytes": nbytes, "gbs": round(nbytes / t / 1e9, 1),
+                     "frac": round(nbytes / t / 1e9 / pk["hbm_gbs"], 4), "peak_source": f"of {src}",
+                     "bound": "hbm (weights; N = batch is far below the MMA's M)"}
+    res["weights"] = f"{nw} rotating copies of wkv_b ({nw * st.wkv_b.numel() * 2 / 1e6:.0f} MB), cold in L2"
+    return res
 
 
 def run_gpu(args, rank, world, local_rank):
@@ -387,6 +435,7 @@ def run_gpu(args, rank, world, local_rank):
                 "roofline_time_us": round(max(t_hbm, t_tc) * 1e6, 3)}
 
     warm = run_warm(st, stream)
+    gemms = run_gemms(st, stream) if w.absorb else None
     e2e = run_e2e(st, K, W) if not args.no_e2e else None
     cpu = run_cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu) else None
     if rank != 0:
@@ -400,6 +449,7 @@ def run_gpu(args, rank, world, local_rank):
                    "attended_positions": st.tokens, "cache": "bf16" if w.fmt == 0 else "fp8-e4m3/128",
                    "topk": w.topk or None, "mtp": w.mtp,
                    "step": ("fused append + top-k gather decode" if w.topk else
+                            "append new row + query absorption + decode + value projection" if w.absorb else
                             "append new row + decode" if w.mtp == 1 else
                             f"append {w.mtp} new rows + multi-token decode (each cache position counted once)"),
                    "l2": f"inputs larger than L2: rotating {st.rotation}; L2 {st.l2_bytes / 1e6:.0f} MB",
@@ -409,6 +459,7 @@ def run_gpu(args, rank, world, local_rank):
         "wall_ms_per_step": round(t_wall * 1e3 / K, 6),
         "roofline": roofline,
         "warm": warm,
+        "gemms": gemms,
         "read_ceiling": {"gbs": round(ceil_gbs, 1), "kernel": "read_ceiling_kernel",
                          "bytes_per_pass": int(ceil_bytes),
                          "sample": "the step's rotated cache tensors, streamed with 16-byte loads"},
@@ -424,13 +475,15 @@ def run_e2e(st: Setup, K: int, W: int):
     """Public API per step with host buffers: H2D of the step's inputs from
     pinned memory, the calls, D2H of the outputs, all inside the timing."""
     w = st.w
-    host_in = {"ql": st.ql.cpu().pin_memory(), "qp": st.qp.cpu().pin_memory(),
+    host_in = {("qn" if w.absorb else "ql"): (st.q_nope if w.absorb else st.ql).cpu().pin_memory(),
+               "qp": st.qp.cpu().pin_memory(),
                "ends": st.ends.cpu().pin_memory(), "kv_new": st.kv_new.cpu().pin_memory(),
                "pe_new": st.pe_new.cpu().pin_memory()}
     if w.topk:
         host_in["topk"] = st.topks[0].cpu().pin_memory()
     dev = {k: torch.empty_like(v, device=st.device) for k, v in host_in.items()}
-    out_h = torch.empty(st.out.shape, dtype=st.out.dtype).pin_memory()
+    res = st.o if w.absorb else st.out   # the step's result
+    out_h = torch.empty(res.shape, dtype=res.dtype).pin_memory()
     lse_h = torch.empty(st.lse.shape, dtype=st.lse.dtype).pin_memory()
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
@@ -447,13 +500,16 @@ def run_e2e(st: Setup, K: int, W: int):
             c = st.caches[i % st.rot]
             for sp in st.start_pos:
                 mla.cache_append(c, dev["kv_new"], dev["pe_new"], sp)
+            ql = mla.absorb_q(dev["qn"], st.wkv_b, out=st.ql) if w.absorb else dev["ql"]
             if w.mtp > 1:
-                mla.decode_mtp(c, dev["ql"], dev["qp"], dev["ends"], w.S, w.softmax_scale, out=st.out,
+                mla.decode_mtp(c, ql, dev["qp"], dev["ends"], w.S, w.softmax_scale, out=st.out,
                                lse=st.lse, workspace=st.ws)
             else:
-                mla.decode(c, dev["ql"], dev["qp"], dev["ends"], w.S, w.softmax_scale, out=st.out,
+                mla.decode(c, ql, dev["qp"], dev["ends"], w.S, w.softmax_scale, out=st.out,
                            lse=st.lse, workspace=st.ws)
-        out_h.copy_(st.out, non_blocking=True)
+            if w.absorb:
+                mla.project_out(st.out, st.wkv_b, out=st.o)
+        out_h.copy_(res, non_blocking=True)
         lse_h.copy_(st.lse, non_blocking=True)
 
     for i in range(min(W, 10)):
@@ -496,13 +552,21 @@ def oracle_sample(w: inputs.Workload, budget_s: float):
         topk = inputs.topk_indices(1, w.topk, [int(ends[0])], 1000 * w.index + inputs.T_TOPK).numpy()
     T = int(ends[0])
     tokens = min(T, w.topk) if w.topk else T
-    return orc, cache, inputs.bf16_bits(ql), inputs.bf16_bits(qp), T, topk, tokens
+    absorb = None
+    if w.absorb:
+        qn, wkv = inputs.absorb_inputs(w)
+        absorb = (inputs.bf16_bits(qn[:1]), inputs.bf16_bits(wkv))
+    return orc, cache, inputs.bf16_bits(ql), inputs.bf16_bits(qp), T, topk, tokens, absorb
 
 
 def time_oracle_step(sample, w):
-    orc, cache, ql, qp, T, topk, tokens = sample
+    orc, cache, ql, qp, T, topk, tokens, absorb = sample
     t0 = time.perf_counter()
-    if w.mtp > 1:
+    if absorb is not None:
+        q_lat = orc.absorb_q(absorb[0], absorb[1])
+        out, _ = orc.decode_absorbed(cache, q_lat, qp, [T], w.softmax_scale)
+        orc.project_out(out.reshape(1, w.H, 512), absorb[1])
+    elif w.mtp > 1:
         orc.decode_absorbed_mtp(cache, ql, qp, [T], w.softmax_scale)
     else:
         orc.decode_absorbed(cache, ql, qp, [T], w.softmax_scale, topk=topk)

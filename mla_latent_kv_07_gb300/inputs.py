@@ -20,6 +20,7 @@ import torch
 DC, DR, BLK = 512, 64, 128
 
 T_KV, T_PE, T_QL, T_QP, T_LEN, T_TOPK, T_KVNEW, T_PENEW = range(1, 9)
+T_QNOPE, T_WKVB = 10, 11   # q_nope and wkv_b (workloads with the absorption products)
 
 # 1/sqrt(qk_nope_head_dim + qk_rope_head_dim) = 1/sqrt(128 + 64), and the YaRN
 # attention-scale correction (0.1 * mscale * ln(rope_factor) + 1)^2 with the
@@ -43,6 +44,7 @@ class Workload:
     topk: int = 0         # 0: dense decode
     append: bool = False  # a new row is appended at end_pos - 1 before decoding
     mtp: int = 1          # new tokens per sequence decoded at once (multi-token decode)
+    absorb: bool = False  # the step also runs the query absorption and value projection
     notes: dict = field(default_factory=dict)
 
 
@@ -60,6 +62,9 @@ WORKLOADS = {
     # beyond the headline table: workload 2 with two new tokens per sequence
     6: Workload(6, "mtp2_b8_h128_t4096_bf16", B=8, H=128, S=4096, fmt=0, softmax_scale=SCALE_YARN,
                 T=4096, mtp=2),
+    # workload 2 as a whole attention step: q_nope -> q_latent -> decode -> o
+    7: Workload(7, "attn_b8_h128_t4096_bf16", B=8, H=128, S=4096, fmt=0, softmax_scale=SCALE_YARN,
+                T=4096, absorb=True),
 }
 
 
@@ -126,3 +131,10 @@ def new_rows(w: Workload, device="cpu"):
 def bf16_bits(t: torch.Tensor):
     """bf16 tensor -> numpy uint16 bit patterns (CPU)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")
+
+
+def absorb_inputs(w: Workload, device="cpu"):
+    """q_nope [B, H, 128] (N(0,1)) and wkv_b [H, 256, 512] (N(0,1) * 0.05, as bf16)."""
+    qn = randn_bf16((w.B, w.H, 128), 1000 * w.index + T_QNOPE, device)
+    wkv = (randn_bf16((w.H, 256, DC), 1000 * w.index + T_WKVB, device).float() * 0.05).to(torch.bfloat16)
+    return qn, wkv
