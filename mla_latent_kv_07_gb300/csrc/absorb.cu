@@ -8,9 +8,11 @@
 // rows 128..255 are W_UV[h] (v x c).  Products accumulate in fp32 (tensor
 // memory) and are rounded to bf16 once.
 //
-// One CTA per (head, chunk of up to 64 sequences).  The head's weights are
-// the MMA's A operand (M = 128 rows: 128 latent columns c of W_UK^T per MMA
-// row block, or the 128 value rows v of W_UV), the chunk's sequences its N
+// One CTA per (head, chunk of up to 64 sequences) -- and, for the query
+// absorption, per 128-column block of q_latent, so that a head's 128 KB of
+// weights is pulled in by four SMs.  The weights are the MMA's A operand
+// (M = 128 rows: 128 latent columns c of W_UK^T, or the 128 value rows v of
+// W_UV), the chunk's sequences its N
 // (64, rows past B zero-filled by TMA): a decode batch is far narrower than
 // any MMA M, so the weights take that side.  W_UK^T is read straight from
 // W_UK's [n][c] layout as an MN-major A operand; W_UV and the activations are
@@ -36,7 +38,6 @@ namespace {
 using namespace ptx;
 
 constexpr int kChunk = 64;                   // sequences per CTA (MMA N)
-constexpr int kWBytes = 8 * kSwBlk;          // one head's W_UK or W_UV: 8 blocks of 64 c
 constexpr int kXBlk = kChunk * 128;          // 64 sequence rows x 64 columns, bf16
 constexpr long kSpin = 1L << 26;
 
@@ -54,18 +55,21 @@ __device__ bool wait_bounded(uint64_t* b, uint32_t parity) {
   return false;
 }
 
-// kQ = true: q_latent = q_nope . W_UK (K = 128, four 128-row blocks of c)
+// kQ = true: q_latent = q_nope . W_UK (K = 128; the CTA's 128-column block of
+//            c is blockIdx.z)
 // kQ = false: o = W_UV . x (K = 512, one block of 128 v)
 template <bool kQ>
-__global__ void __launch_bounds__(128, 1) absorb_kernel(const __grid_constant__ AbsorbParams ap) {
+__global__ void __launch_bounds__(128) absorb_kernel(const __grid_constant__ AbsorbParams ap) {
   constexpr int kK = kQ ? 128 : 512;               // contraction length
-  constexpr int kMBlocks = kQ ? 4 : 1;             // 128-row output blocks
+  constexpr int kMBlocks = 1;                      // 128-row output blocks per CTA
   constexpr int kXBlocks = kK / 64;                // activation blocks of 64 columns
   constexpr uint32_t kCols = kMBlocks * kChunk;    // tensor-memory columns
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* wsm = sm;                   // 8 blocks of 16 KB
-  uint8_t* xsm = sm + kWBytes;         // kXBlocks blocks of 8 KB
+  uint8_t* wsm = sm;                   // 2 (query) or 8 (projection) blocks of 16 KB
+  constexpr int kWBlocks = kQ ? 2 : 8;
+  uint8_t* xsm = sm + kWBlocks * kSwBlk;   // kXBlocks blocks of 8 KB
+  const int mb = kQ ? blockIdx.z : 0;      // output block: c in [128 mb, 128 mb + 128)
   __shared__ __align__(8) uint64_t full, done;
   __shared__ uint32_t tslot;
   const int h = blockIdx.x, b0 = blockIdx.y * kChunk;
@@ -90,9 +94,10 @@ __global__ void __launch_bounds__(128, 1) absorb_kernel(const __grid_constant__ 
 
   __shared__ int s_ok;
   if (threadIdx.x == 0) {
-    bar_expect_tx(&full, kWBytes + kXBlocks * kXBlk);
+    bar_expect_tx(&full, kWBlocks * kSwBlk + kXBlocks * kXBlk);
     const int row0 = kQ ? 0 : 128;     // W_UK or W_UV rows of head h
-    for (int cb = 0; cb < 8; ++cb) tma3(wsm + cb * kSwBlk, &ap.m_w, 64 * cb, row0, h, &full);
+    for (int cb = 0; cb < kWBlocks; ++cb)
+      tma3(wsm + cb * kSwBlk, &ap.m_w, 64 * (cb + 2 * mb), row0, h, &full);
     for (int k = 0; k < kXBlocks; ++k) tma3(xsm + k * kXBlk, &ap.m_x, 64 * k, h, b0, &full);
     const bool landed = wait_bounded(&full, 0);
     if (landed) {
@@ -103,7 +108,7 @@ __global__ void __launch_bounds__(128, 1) absorb_kernel(const __grid_constant__ 
       for (int m = 0; m < kMBlocks; ++m) {
 #pragma unroll 1
         for (int kk = 0; kk < kK / 16; ++kk) {
-          // A: W_UK^T is MN-major (c contiguous): blocks 2m and 2m+1 (LBO apart),
+          // A: W_UK^T is MN-major (c contiguous): blocks 0 and 1 (LBO apart),
           //    16 rows of n per step; W_UV is K-major: block kk/4, 32 B per step
           const uint64_t a = kQ ? sdesc(wa + 2 * m * kSwBlk + 2048 * kk, kSwBlk, 1024)
                                 : sdesc(wa + (kk >> 2) * kSwBlk + (kk & 3) * 32, 16, 1024);
@@ -131,7 +136,7 @@ __global__ void __launch_bounds__(128, 1) absorb_kernel(const __grid_constant__ 
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll 1
     for (int m = 0; m < kMBlocks; ++m) {
-      const int row = m * 128 + warp * 32 + lane;   // c (query) or v (output)
+      const int row = (mb + m) * 128 + warp * 32 + lane;   // c (query) or v (output)
 #pragma unroll 1
       for (int c = 0; c < kChunk / 16; ++c) {
         uint32_t r[16];
@@ -199,10 +204,11 @@ cudaError_t launch(const void* x, const void* wkv_b, int B, int H, void* y, uint
   ap.status = status;
   ap.B = B;
   ap.H = H;
-  const size_t smem = kWBytes + (kK / 64) * kXBlk + 1024;
+  const size_t smem = (kQ ? 2 : 8) * kSwBlk + (kK / 64) * kXBlk + 1024;
   cudaError_t e = ensure_smem<absorb_kernel<kQ>>(smem);
   if (e != cudaSuccess) return e;
-  return launch_pdl(absorb_kernel<kQ>, dim3(H, (B + kChunk - 1) / kChunk), dim3(128), smem, s, ap);
+  return launch_pdl(absorb_kernel<kQ>, dim3(H, (B + kChunk - 1) / kChunk, kQ ? 4 : 1), dim3(128), smem, s,
+                    ap);
 }
 
 }  // namespace
