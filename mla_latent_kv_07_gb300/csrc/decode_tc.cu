@@ -542,6 +542,8 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     const int p0 = 16 * sh, p1 = 32 + 8 * sh;   // first position of each run
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const float sl2 = p.scale_log2;
+    const bool pos_scale = sl2 > 0.f;
+    const float ps = pos_scale ? sl2 : 1.f;   // the factor still to apply to sc in P
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int i = 0; i < ntiles; ++i) {
@@ -577,16 +579,27 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         // registers, so no release ordering is needed
         if (lane == 0) bar_arrive_remote_relaxed(mapa(&bars->xempty[xb], peer));
       }
-      // masked, scaled scores; the tile maximum of the pair
+      // masked scores and the tile maximum of the pair.  With a positive
+      // scale the scores stay unscaled here: round-to-nearest is monotone, so
+      // the maximum of the scaled scores is the scaled maximum, and P below
+      // takes scale and reference in one fused multiply-add.  (A scale <= 0
+      // scales first.)
       const int valid = min(kN, u.t1 - (u.t0 + i * kN));
+      if (!pos_scale) {
 #pragma unroll
-      for (int k = 0; k < 24; ++k)
-        sc[k] = (k < 16 ? p0 + k : p1 + k - 16) < valid ? sc[k] * sl2 : -INFINITY;
+        for (int k = 0; k < 24; ++k) sc[k] *= sl2;
+      }
+      if (valid < kN) {   // the unit's last tile
+#pragma unroll
+        for (int k = 0; k < 24; ++k)
+          if ((k < 16 ? p0 + k : p1 + k - 16) >= valid) sc[k] = -INFINITY;
+      }
       float mx[4] = {sc[0], sc[1], sc[2], sc[3]};
 #pragma unroll
       for (int k = 4; k < 24; ++k) mx[k & 3] = fmaxf(mx[k & 3], sc[k]);
       float* pm = bars->pair_max[i & 1];
-      pm[sh * 128 + h] = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+      pm[sh * 128 + h] = pos_scale ? mloc * sl2 : mloc;
       pair_sync(warp & 3);
       const float mt = fmaxf(pm[h], pm[128 + h]);
       // lazy rescale of the running reference max
@@ -631,8 +644,9 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         float part = 0.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const __nv_bfloat162 two = __floats2bfloat162_rn(ex2_approx(sc[8 * c + 2 * k] - m_ref),
-                                                           ex2_approx(sc[8 * c + 2 * k + 1] - m_ref));
+          const __nv_bfloat162 two =
+              __floats2bfloat162_rn(ex2_approx(__fmaf_rn(sc[8 * c + 2 * k], ps, -m_ref)),
+                                    ex2_approx(__fmaf_rn(sc[8 * c + 2 * k + 1], ps, -m_ref)));
           const float2 back = __bfloat1622float2(two);
           part += back.x + back.y;
           pk[k] = *reinterpret_cast<const uint32_t*>(&two);
