@@ -204,7 +204,8 @@ __device__ __forceinline__ void dequant16(uint4 v, float sc, uint4& lo, uint4& h
     const __nv_fp8x2_storage_t pair = (__nv_fp8x2_storage_t)((w[i >> 1] >> ((i & 1) * 16)) & 0xffffu);
     const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
     const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
-    const __nv_bfloat162 bb = __floats2bfloat162_rn(__fmul_rn(f.x, sc), __fmul_rn(f.y, sc));
+    // a pair of IEEE fp32 products, each rounded to nearest, then to bf16
+    const __nv_bfloat162 bb = __float22bfloat162_rn(__fmul2_rn(f, make_float2(sc, sc)));
     o[i] = *reinterpret_cast<const uint32_t*>(&bb);
   }
   lo = make_uint4(o[0], o[1], o[2], o[3]);
@@ -572,7 +573,9 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 6; ++k) {
           const float4 v = xr[128 * (k < 4 ? p0 / 4 + k : p1 / 4 + k - 4)];
-          sc[4 * k] += v.x; sc[4 * k + 1] += v.y; sc[4 * k + 2] += v.z; sc[4 * k + 3] += v.w;
+          const float2 a = __fadd2_rn(make_float2(sc[4 * k], sc[4 * k + 1]), make_float2(v.x, v.y));
+          const float2 c2 = __fadd2_rn(make_float2(sc[4 * k + 2], sc[4 * k + 3]), make_float2(v.z, v.w));
+          sc[4 * k] = a.x; sc[4 * k + 1] = a.y; sc[4 * k + 2] = c2.x; sc[4 * k + 3] = c2.y;
         }
         __syncwarp();
         // my buffer b may be refilled: the values read above are already in
@@ -637,26 +640,23 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       // p0/8 + 1 and p1/8; l sums the rounded values
       ok = ok && wt.wait(&bars->pfree[b], par ^ 1);
       uint8_t* prow = pbuf(b);
-      float ls[3];
+      float2 ls = make_float2(0.f, 0.f);
+      const float2 ps2 = make_float2(ps, ps), nm2 = make_float2(-m_ref, -m_ref);
 #pragma unroll
       for (int c = 0; c < 3; ++c) {
         uint32_t pk[4];
-        float part = 0.f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-          const __nv_bfloat162 two =
-              __floats2bfloat162_rn(ex2_approx(__fmaf_rn(sc[8 * c + 2 * k], ps, -m_ref)),
-                                    ex2_approx(__fmaf_rn(sc[8 * c + 2 * k + 1], ps, -m_ref)));
-          const float2 back = __bfloat1622float2(two);
-          part += back.x + back.y;
+          const float2 t = __ffma2_rn(make_float2(sc[8 * c + 2 * k], sc[8 * c + 2 * k + 1]), ps2, nm2);
+          const __nv_bfloat162 two = __floats2bfloat162_rn(ex2_approx(t.x), ex2_approx(t.y));
+          ls = __fadd2_rn(ls, __bfloat1622float2(two));
           pk[k] = *reinterpret_cast<const uint32_t*>(&two);
         }
-        ls[c] = part;
         const int chunk = c < 2 ? p0 / 8 + c : p1 / 8;
         *reinterpret_cast<uint4*>(prow + (chunk >> 3) * kSwBlk + swz_chunk(h, chunk & 7)) =
             make_uint4(pk[0], pk[1], pk[2], pk[3]);
       }
-      l += (ls[0] + ls[1]) + ls[2];
+      l += ls.x + ls.y;
       if (!C::kConv && valid < kN) {
         // dense bf16 tail: rows past the unit hold whatever the cache holds
         // there; zero them so P = 0 never meets a non-finite value
