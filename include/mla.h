@@ -156,7 +156,8 @@ MLA_API mla_status mla_decode(const mla_cache* cache, const void* q_latent, cons
  *
  *   q_latent    device bf16 [B, s, H, 512];  q_pe  device bf16 [B, s, H, 64]
  *   end_pos     device int32 [B]
- *   s           1 <= s <= 16 (s = 1 is mla_decode)
+ *   s           1 <= s <= 1024 (s = 1 is mla_decode; a large s is a prefill
+ *               chunk over the cached prefix, with the same causal mask)
  *   out         device bf16 [B, s, H, 512];  lse  NULL or device fp32 [B, s, H]
  *   workspace   >= mla_workspace_size(B * s, H, max_end_pos, 0) bytes
  *   other arguments as for mla_decode (B <= cache->max_batch)

@@ -179,10 +179,11 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
                                                        int mtp_s) {
   __shared__ int scan_smem[33];
   __shared__ unsigned long long total_len;
-  __shared__ int count_smem;
+  __shared__ int count_smem, max_len_smem;
   pdl_wait();   // the previous call's kernels may still read this workspace
   if (threadIdx.x == 0) {
     total_len = 0;
+    max_len_smem = 0;
     if (end_pos) *ws.status = 0u;   // dense: first kernel of the call
   }
   __syncthreads();
@@ -190,6 +191,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
   const int per = (B + blockDim.x - 1) / blockDim.x;
   const int b0 = threadIdx.x * per;
   unsigned long long mine = 0;
+  int longest = 0;
   for (int b = b0; b < b0 + per && b < B; ++b) {
     int len;
     if (end_pos) {
@@ -205,14 +207,30 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
       len = ws.lengths[b];
     }
     mine += (unsigned long long)len;
+    longest = len > longest ? len : longest;
   }
-  atomicAdd(&total_len, mine);
+  // one shared atomic per warp (a block-wide pile-up on one word serialises)
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mine += __shfl_xor_sync(0xffffffffu, mine, o);
+    longest = max(longest, __shfl_xor_sync(0xffffffffu, longest, o));
+  }
+  if ((threadIdx.x & 31) == 0) {
+    atomicAdd(&total_len, mine);
+    atomicMax(&max_len_smem, longest);
+  }
   __syncthreads();
+  // a chunk of the longest length gives every non-empty sequence one unit; no
+  // larger chunk lowers the count (which may then stay above the target when
+  // there are more sequences than units in a wave)
+  const long long cap = max_len_smem > granule ? ((long long)max_len_smem + granule - 1) / granule * granule
+                                               : (long long)granule;
   // smallest granule multiple with sum_b ceil(len_b / chunk) <= target, so
   // the units fit the launch (and, on the pair path, one wave of the GPU)
   long long chunk = ((long long)total_len + target - 1) / target;
   chunk = ((chunk + granule - 1) / granule) * granule;
   if (chunk < granule) chunk = granule;
+  if (chunk > cap) chunk = cap;
   int nmine = 0;
   for (int iter = 0; iter < 64; ++iter) {
     nmine = 0;
@@ -220,14 +238,16 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
       nmine += (int)((ws.lengths[b] + chunk - 1) / chunk);
     if (threadIdx.x == 0) count_smem = 0;
     __syncthreads();
-    atomicAdd(&count_smem, nmine);
+    const int wsum = __reduce_add_sync(0xffffffffu, nmine);
+    if ((threadIdx.x & 31) == 0) atomicAdd(&count_smem, wsum);
     __syncthreads();
     const int n = count_smem;
     __syncthreads();
-    if (n <= target) break;
+    if (n <= target || chunk >= cap) break;
     long long grown = (chunk * n + target - 1) / target;
     grown = ((grown + granule - 1) / granule) * granule;
     chunk = grown > chunk + granule ? grown : chunk + granule;
+    if (chunk > cap) chunk = cap;
   }
   int total_units;
   int u = block_exclusive_scan(nmine, scan_smem, &total_units);
@@ -249,17 +269,15 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
 }
 
 // ---------------------------------------------------------------- combine
-// One CTA per (h, b); 128 threads x 4 latent columns.  out = sum_i w_i O_i,
-// w_i = exp(lse_i - lse), lse = log sum_i exp(lse_i).  The partial rows are
-// fetched eight units at a time, loads first, so their latencies overlap.
-__global__ void __launch_bounds__(128) combine_kernel(Workspace ws, int H,
-                                                     __nv_bfloat16* __restrict__ out,
-                                                     float* __restrict__ lse_out) {
-  pdl_wait();
-  pdl_trigger();
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int2 sq = ws.seq[b];
-  if (sq.y < 0) return;   // a single unit: the decode kernel wrote the result
+// CTA (h, y) combines head h of sequences y, y + gridDim.y, ...; 128 threads x
+// 4 latent columns.  out = sum_i w_i O_i, w_i = exp(lse_i - lse),
+// lse = log sum_i exp(lse_i).  The first warp fetches the descriptors of 32 of
+// the CTA's sequences at once, so sequences the decode kernel finished itself
+// (a single unit) cost one load between them, not a CTA each.  The partial
+// rows are fetched eight units at a time, loads first, so their latencies
+// overlap.
+__device__ __forceinline__ void combine_one(const Workspace& ws, int H, int h, int b, int2 sq,
+                                            __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
   const int n = sq.y;
   const int c = threadIdx.x * 4;
   const float* pl = ws.part_lse + (size_t)sq.x * H + h;            // unit stride H
@@ -304,6 +322,31 @@ __global__ void __launch_bounds__(128) combine_kernel(Workspace ws, int H,
   pk.y = *reinterpret_cast<uint32_t*>(&hi);
   *reinterpret_cast<uint2*>(out + ((size_t)b * H + h) * kDc + c) = pk;
   if (lse_out && threadIdx.x == 0) lse_out[(size_t)b * H + h] = lse;
+}
+
+__global__ void __launch_bounds__(128) combine_kernel(Workspace ws, int H, int B,
+                                                     __nv_bfloat16* __restrict__ out,
+                                                     float* __restrict__ lse_out) {
+  __shared__ int2 seq_smem[32];
+  __shared__ uint32_t live_smem;
+  pdl_wait();
+  pdl_trigger();
+  const int h = blockIdx.x, step = gridDim.y;
+  for (int base = blockIdx.y; base < B; base += 32 * step) {
+    if (threadIdx.x < 32) {
+      const int b = base + threadIdx.x * step;
+      const int2 sq = b < B ? ws.seq[b] : make_int2(0, -1);
+      seq_smem[threadIdx.x] = sq;
+      const uint32_t live = __ballot_sync(0xffffffffu, sq.y >= 0);
+      if (threadIdx.x == 0) live_smem = live;
+    }
+    __syncthreads();
+    for (uint32_t live = live_smem; live; live &= live - 1u) {
+      const int k = __ffs(live) - 1;
+      combine_one(ws, H, h, base + k * step, seq_smem[k], out, lse_out);
+    }
+    __syncthreads();
+  }
 }
 
 // ----------------------------------------------------------- read ceiling
@@ -369,7 +412,8 @@ cudaError_t launch_schedule(const int* end_pos, int max_end_pos, const Workspace
 
 cudaError_t launch_combine(const Workspace& ws, int B, int H, void* out, float* lse,
                            cudaStream_t s) {
-  return launch_pdl(combine_kernel, dim3(H, B), dim3(128), 0, s, ws, H,
+  // up to 32 sequences per head in flight; a CTA walks the rest
+  return launch_pdl(combine_kernel, dim3(H, B < 32 ? B : 32), dim3(128), 0, s, ws, H, B,
                     static_cast<__nv_bfloat16*>(out), lse);
 }
 

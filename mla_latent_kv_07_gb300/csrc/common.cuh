@@ -17,7 +17,7 @@ constexpr int kBlk = 128;         // FP8 block width
 constexpr int kNblk = kDc / kBlk; // 4 scales per row
 constexpr int kMaxAppendB = 2048; // rows one append call may write
 constexpr int kMaxTopK = 8192;
-constexpr int kMaxMtp = 16;       // new tokens per sequence in one multi-token decode
+constexpr int kMaxMtp = 1024;     // new tokens per sequence in one multi-token call (a prefill chunk)
 
 constexpr uint32_t kDevEndPosClamped = 0x1u;
 constexpr uint32_t kDevAppendSkipped = 0x2u;

@@ -62,6 +62,10 @@ WORKLOADS = {
     # beyond the headline table: workload 2 with two new tokens per sequence
     6: Workload(6, "mtp2_b8_h128_t4096_bf16", B=8, H=128, S=4096, fmt=0, softmax_scale=SCALE_YARN,
                 T=4096, mtp=2),
+    # a prefill chunk: 512 new tokens of one sequence over its 4096-position
+    # prefix (causal among the chunk's tokens; the chunk's rows are in the cache)
+    8: Workload(8, "prefill_chunk_b1_s512_h128_t4096_bf16", B=1, H=128, S=4096, fmt=0,
+                softmax_scale=SCALE_YARN, T=4096, mtp=512),
     # workload 2 as a whole attention step: q_nope -> q_latent -> decode -> o
     7: Workload(7, "attn_b8_h128_t4096_bf16", B=8, H=128, S=4096, fmt=0, softmax_scale=SCALE_YARN,
                 T=4096, absorb=True),

@@ -146,7 +146,7 @@ def test_multi_token_decode_rejects_bad_arguments(L):
         return L.mla_decode_mtp(ctypes.byref(c), f, f, f, 64, B, s, H, 0.1, f, None, f, 1 << 30, None)
 
     assert mtp(s=0) == 1
-    assert mtp(s=17) == 1
+    assert mtp(s=1025) == 1
     assert mtp(B=3) == 1                                    # more slots than the cache holds
     assert mtp(H=24) == 3
 

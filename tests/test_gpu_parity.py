@@ -172,7 +172,8 @@ def test_read_ceiling_reads_every_word():
 
 # ------------------------------------------------------ multi-token decode
 
-@pytest.mark.parametrize("fmt,H,s", [(0, 128, 2), (1, 128, 3), (0, 16, 2), (1, 64, 4)])
+@pytest.mark.parametrize("fmt,H,s", [(0, 128, 2), (1, 128, 3), (0, 16, 2), (1, 64, 4), (0, 128, 40),
+                                     (1, 16, 24)])
 def test_multi_token_decode_all_outputs(fmt, H, s):
     B, S = 3, 300
     oc = oracle_cache(_rand_bf16((B, S, 512), 101), _rand_bf16((B, S, 64), 102), fmt)
@@ -181,6 +182,26 @@ def test_multi_token_decode_all_outputs(fmt, H, s):
     ends = np.array([300, 97, 2], np.int32)      # the last: the first tokens see nothing or one row
     out, lse = mla.decode_mtp(dc, ql.cuda(), qp.cuda(), torch.from_numpy(ends).cuda(), S, 0.14)
     ref, ref_lse = orc.decode_absorbed_mtp(oc, bits(ql), bits(qp), ends, 0.14)
+    check_close(f64(out).reshape(-1, 512), ref.reshape(-1, 512), "out")
+    check_close(f64(lse).reshape(-1), ref_lse.reshape(-1), "lse")
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_prefill_chunk_more_tokens_than_units(fmt):
+    # 200 causal tokens over a 520-position prefix: more (token) sequences than
+    # CTA pairs in a wave, so every sequence is one unit and the schedule's
+    # unit count is the count of sequences
+    B, S, H, s = 1, 520, 128, 200
+    oc = oracle_cache(_rand_bf16((B, S, 512), 121), _rand_bf16((B, S, 64), 122), fmt)
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((B, s, H, 512), 123), _rand_bf16((B, s, H, 64), 124)
+    ends = np.array([S], np.int32)
+    ws = mla.alloc_workspace(B * s, H, S)
+    out, lse = mla.decode_mtp(dc, ql.cuda(), qp.cuda(), torch.from_numpy(ends).cuda(), S, 0.1, workspace=ws)
+    torch.cuda.synchronize()
+    header = ws[:8].cpu().numpy().view(np.int32)
+    assert header[0] == 0 and header[1] == B * s
+    ref, ref_lse = orc.decode_absorbed_mtp(oc, bits(ql), bits(qp), ends, 0.1)
     check_close(f64(out).reshape(-1, 512), ref.reshape(-1, 512), "out")
     check_close(f64(lse).reshape(-1), ref_lse.reshape(-1), "lse")
 
