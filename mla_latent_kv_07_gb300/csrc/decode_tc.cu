@@ -449,6 +449,12 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc(128, kN, false);
       constexpr uint32_t id_pv = idesc(128, kHalf, true);
+      // descriptors of stage 0 and P buffer 0; a tile's are these plus
+      // constant offsets (one add per MMA on this thread)
+      const uint64_t d_k0 = sdesc(sa(opl(0)), 16, 1024);          // K-major operand tiles
+      const uint64_t d_v0 = sdesc(sa(opl(0)), kBlkBytes, 1024);   // the latent tile read MN-major (V)
+      const uint64_t d_p0 = sdesc(sa(pbuf(0)), 16, 1024);
+      const uint32_t t_q = tmem + kTmemQ, t_o = tmem + kTmemO;
       int nq = 0, np = 0;
       long idle = 0;
       if (live && wt.wait(&bars->qready, 0)) tc_after();
@@ -460,11 +466,15 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           const int i = np, j = i % C::kStages, b = bsel(i);
           if (bar_try(&bars->pfull[b], bpar(i))) {
             tc_after();
-            const uint32_t pa = sa(pbuf(b)), va = sa(opl(j));
+            const uint64_t pd = sdesc_at(d_p0, b * C::kPBytes), vd = sdesc_at(d_v0, j * C::kStage);
+            if (i == 0)
+              mma_ss_c<false>(t_o, pd, vd, id_pv);
+            else
+              mma_ss_c<true>(t_o, pd, vd, id_pv);
 #pragma unroll
-            for (int kk = 0; kk < kN / 16; ++kk)
-              mma_ss(tmem + kTmemO, sdesc(pa + (kk >> 2) * kSwBlk + (kk & 3) * 32, 16, 1024),
-                     sdesc(va + 2048 * kk, kBlkBytes, 1024), id_pv, (i > 0 || kk > 0) ? 1 : 0);
+            for (int kk = 1; kk < kN / 16; ++kk)
+              mma_ss_c<true>(t_o, sdesc_at(pd, (kk >> 2) * kSwBlk + (kk & 3) * 32), sdesc_at(vd, 2048 * kk),
+                             id_pv);
             mma_commit(&bars->pfree[b]);
             mma_commit(&bars->empty[j]);
             ++np;
@@ -478,14 +488,15 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
               bar_try(&bars->sfree[b], bpar(k) ^ 1)) {
             tc_after();
             const uint32_t sd = tmem + kTmemS + b * kN;
-            const uint32_t la = sa(opl(j)), pe = sa(ope(j)) + rank * (kPeHalf * 2);
+            const uint64_t kd = sdesc_at(d_k0, j * C::kStage);
+            const uint64_t ped = sdesc_at(kd, kOplBytes + rank * (kPeHalf * 2));
+            mma_ts_c<false>(sd, t_q, kd, id_qk);
 #pragma unroll
-            for (int kk = 0; kk < kHalf / 16; ++kk)
-              mma_ts(sd, tmem + kTmemQ + 8 * kk,
-                     sdesc(la + (kk >> 2) * kBlkBytes + (kk & 3) * 32, 16, 1024), id_qk, kk > 0 ? 1 : 0);
+            for (int kk = 1; kk < kHalf / 16; ++kk)
+              mma_ts_c<true>(sd, t_q + 8 * kk, sdesc_at(kd, (kk >> 2) * kBlkBytes + (kk & 3) * 32), id_qk);
 #pragma unroll
             for (int kk = 0; kk < kPeHalf / 16; ++kk)
-              mma_ts(sd, tmem + kTmemQ + kHalf / 2 + 8 * kk, sdesc(pe + 32 * kk, 16, 1024), id_qk, 1);
+              mma_ts_c<true>(sd, t_q + kHalf / 2 + 8 * kk, sdesc_at(ped, 32 * kk), id_qk);
             mma_commit(&bars->sfull[b]);
             ++nq;
             did = true;

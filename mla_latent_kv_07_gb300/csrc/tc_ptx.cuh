@@ -89,6 +89,31 @@ __device__ __forceinline__ void mma_ts(uint32_t d, uint32_t a, uint64_t b, uint3
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d),
       "r"(a), "l"(b), "r"(id), "r"(acc));
 }
+// Descriptor of a tile `bytes` further into shared memory: the start-address
+// field is the low 14 bits (address >> 4, shared addresses below 256 KB), so
+// the offset adds without a carry into the other fields.  A descriptor built
+// once per stage plus a constant offset keeps the issuing thread's work per
+// MMA at one add.
+__device__ __forceinline__ uint64_t sdesc_at(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+// MMA with a compile-time accumulate flag (kAcc = false overwrites D)
+template <bool kAcc>
+__device__ __forceinline__ void mma_ss_c(uint32_t d, uint64_t a, uint64_t b, uint32_t id) {
+  if constexpr (kAcc)
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, 1, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+                 ::"r"(d), "l"(a), "l"(b), "r"(id));
+  else
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, 0, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+                 ::"r"(d), "l"(a), "l"(b), "r"(id));
+}
+template <bool kAcc>
+__device__ __forceinline__ void mma_ts_c(uint32_t d, uint32_t a, uint64_t b, uint32_t id) {
+  if constexpr (kAcc)
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, 1, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
+                 ::"r"(d), "r"(a), "l"(b), "r"(id));
+  else
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, 0, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }"
+                 ::"r"(d), "r"(a), "l"(b), "r"(id));
+}
 __device__ __forceinline__ void mma_commit(uint64_t* b) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    sa(b))
