@@ -218,7 +218,8 @@ def decode_absorbed(cache: dict, q_latent, q_pe, end_pos, softmax_scale: float,
     return (out, lse, w) if w is not None else (out, lse)
 
 
-def decode_absorbed_mtp(cache: dict, q_latent, q_pe, end_pos, softmax_scale: float):
+def decode_absorbed_mtp(cache: dict, q_latent, q_pe, end_pos, softmax_scale: float,
+                        token=None, pairs=None):
     """fp64 absorbed decode of s new tokens per sequence (multi-token decode).
 
     q_latent [B, s, H, 512], q_pe [B, s, H, 64].  The s new tokens of sequence
@@ -227,12 +228,18 @@ def decode_absorbed_mtp(cache: dict, q_latent, q_pe, end_pos, softmax_scale: flo
     mask over the current step's tokens) prescribes, to the cache positions up
     to and including its own: 0 .. end_pos[b]-s+j.  That is the single-token
     decode with end_pos[b] - (s-1-j) (a token with no position attends to
-    nothing: out 0, lse -inf).  Returns (out [B, s, H, 512], lse [B, s, H]).
+    nothing: out 0, lse -inf).  Returns (out [B, s, H, 512], lse [B, s, H]);
+    with ``token`` = j, only token j, for the (b, h) ``pairs`` (default all):
+    (out [n, 512], lse [n]).
     """
     ql = np.asarray(q_latent)
     qp = np.asarray(q_pe)
     B, s, H = ql.shape[:3]
     ep = np.asarray(end_pos, np.int64)
+    if token is not None:
+        e = np.maximum(ep - (s - 1 - token), 0).astype(np.int32)
+        return decode_absorbed(cache, np.ascontiguousarray(ql[:, token]), np.ascontiguousarray(qp[:, token]),
+                               e, softmax_scale, pairs=pairs)
     out = np.empty((B, s, H, DC), np.float64)
     lse = np.empty((B, s, H), np.float64)
     for j in range(s):

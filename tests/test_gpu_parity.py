@@ -1,8 +1,9 @@
 """GPU parity: the CUDA library against the CPU oracle on the same seeded
 inputs, called through the C ABI (ctypes binding).  Small cases compare every
-output and span several tiles with ragged tails; the five workloads run at
-their full sizes in the launch configuration the benchmark times and compare
-sampled (sequence, head) outputs the oracle computes one by one.
+output and span several tiles with ragged tails; every benchmark workload
+runs at its full size in the launch configuration the benchmark times and
+compares sampled (sequence, token, head) outputs the oracle computes one by
+one.
 """
 import numpy as np
 import pytest
@@ -362,3 +363,56 @@ def test_workload5_sparse_with_fused_append():
     o, l = f64(out), f64(lse)
     check_close(np.stack([o[b, h] for b, h in pairs]), ref, "out")
     check_close(np.array([l[b, h] for b, h in pairs]), ref_lse, "lse")
+
+
+def _check_tokens_sampled(w, oc, ql, qp, ends, out, lse, tokens, per_seq):
+    o, l = f64(out), f64(lse)
+    for j in tokens:
+        pairs = sample_pairs(w.B, w.H, per_seq, 1000 * w.index + j)
+        ref, ref_lse = orc.decode_absorbed_mtp(oc, bits(ql), bits(qp), ends.numpy(), w.softmax_scale,
+                                               token=j, pairs=pairs)
+        check_close(np.stack([o[b, j, h] for b, h in pairs]), ref, f"{w.name} token {j} out")
+        check_close(np.array([l[b, j, h] for b, h in pairs]), ref_lse, f"{w.name} token {j} lse")
+
+
+def test_workload6_multi_token_decode():
+    w = inputs.WORKLOADS[6]
+    oc, dc = workload_cache(w)
+    ql, qp = inputs.queries(w)
+    ends = inputs.end_positions(w)
+    ws = mla.alloc_workspace(w.B * w.mtp, w.H, w.S)
+    out, lse = mla.decode_mtp(dc, ql.cuda(), qp.cuda(), ends.cuda(), w.S, w.softmax_scale, workspace=ws)
+    _check_tokens_sampled(w, oc, ql, qp, ends, out, lse, range(w.mtp), 4)
+
+
+def test_workload8_prefill_chunk():
+    # first, second, middle and last tokens of the 512-token chunk
+    w = inputs.WORKLOADS[8]
+    oc, dc = workload_cache(w)
+    ql, qp = inputs.queries(w)
+    ends = inputs.end_positions(w)
+    ws = mla.alloc_workspace(w.B * w.mtp, w.H, w.S)
+    out, lse = mla.decode_mtp(dc, ql.cuda(), qp.cuda(), ends.cuda(), w.S, w.softmax_scale, workspace=ws)
+    _check_tokens_sampled(w, oc, ql, qp, ends, out, lse, [0, 1, 255, 510, 511], 4)
+
+
+def test_workload7_attention_step():
+    # q_nope -> absorption -> latent decode -> value projection, against the
+    # oracle's fp64 chain of the same three steps (its own q_latent and x)
+    w = inputs.WORKLOADS[7]
+    oc, dc = workload_cache(w)
+    qn, wkv = inputs.absorb_inputs(w)
+    _, qp = inputs.queries(w)
+    ends = inputs.end_positions(w)
+    ql = mla.absorb_q(qn.cuda(), wkv.cuda())
+    out, _ = mla.decode(dc, ql, qp.cuda(), ends.cuda(), w.S, w.softmax_scale)
+    o = f64(mla.project_out(out, wkv.cuda()))
+    ql_ref = orc.absorb_q(bits(qn), bits(wkv))
+    pairs = sample_pairs(w.B, w.H, 6, w.index)
+    x_ref, _ = orc.decode_absorbed(oc, ql_ref, bits(qp), ends.numpy(), w.softmax_scale, pairs=pairs)
+    x = np.zeros((w.B, w.H, 512))
+    for k, (b, h) in enumerate(pairs):
+        x[b, h] = x_ref[k]
+    o_ref = orc.project_out(x, bits(wkv))
+    check_close(f64(ql).reshape(-1, 512), ql_ref.reshape(-1, 512), "q_latent")
+    check_close(np.stack([o[b, h] for b, h in pairs]), np.stack([o_ref[b, h] for b, h in pairs]), "o")
