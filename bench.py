@@ -480,63 +480,147 @@ def run_gpu(args, rank, world, local_rank):
     print(json.dumps(line), flush=True)
 
 
+def _pack(named, align=256):
+    """Byte offsets of the named tensors laid end to end, each `align`-aligned."""
+    offs, total = {}, 0
+    for k, t in named.items():
+        offs[k] = total
+        total += -(-t.numel() * t.element_size() // align) * align
+    return offs, total
+
+
+def _views(buf, offs, like):
+    return {k: buf.narrow(0, offs[k], t.numel() * t.element_size()).view(t.dtype).view(t.shape)
+            for k, t in like.items()}
+
+
 def run_e2e(st: Setup, K: int, W: int):
-    """Public API per step with host buffers: H2D of the step's inputs from
-    pinned memory, the calls, D2H of the outputs, all inside the timing."""
+    """Public API per step with host buffers: the step's inputs leave pinned
+    host memory in one copy (laid end to end) and its results come back in
+    one copy, all inside the timing; the steps' calls and copies are captured
+    in one CUDA graph, as a serving loop replays them.  Two device slots and
+    three streams let the copies of one step overlap the kernels of the
+    previous one (the pipelined number); the serial number runs copy,
+    kernels, copy on one stream."""
     w = st.w
-    host_in = {("qn" if w.absorb else "ql"): (st.q_nope if w.absorb else st.ql).cpu().pin_memory(),
-               "qp": st.qp.cpu().pin_memory(),
-               "ends": st.ends.cpu().pin_memory()}
+    src = {("qn" if w.absorb else "ql"): (st.q_nope if w.absorb else st.ql), "qp": st.qp, "ends": st.ends}
     if w.topk or st.start_pos:   # the step's new cache rows
-        host_in["kv_new"], host_in["pe_new"] = st.kv_new.cpu().pin_memory(), st.pe_new.cpu().pin_memory()
+        src["kv_new"], src["pe_new"] = st.kv_new, st.pe_new
     if w.topk:
-        host_in["topk"] = st.topks[0].cpu().pin_memory()
-    dev = {k: torch.empty_like(v, device=st.device) for k, v in host_in.items()}
-    res = st.o if w.absorb else st.out   # the step's result
-    out_h = torch.empty(res.shape, dtype=res.dtype).pin_memory()
-    lse_h = torch.empty(st.lse.shape, dtype=st.lse.dtype).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+        src["topk"] = st.topks[0]
+    res = {"res": st.o if w.absorb else st.out, "lse": st.lse}   # the step's results
+    in_offs, in_total = _pack(src)
+    out_offs, out_total = _pack(res)
+    host_in = torch.empty(in_total, dtype=torch.uint8).pin_memory()
+    for k, v in _views(host_in, in_offs, src).items():
+        v.copy_(src[k].cpu())
+    host_out = torch.empty(out_total, dtype=torch.uint8).pin_memory()
+    dev_in = [torch.empty(in_total, dtype=torch.uint8, device=st.device) for _ in range(2)]
+    dev_out = [torch.empty(out_total, dtype=torch.uint8, device=st.device) for _ in range(2)]
+    vin = [_views(b, in_offs, src) for b in dev_in]
+    vout = [_views(b, out_offs, res) for b in dev_out]
+    h2d = sum(v.numel() * v.element_size() for v in src.values())
+    d2h = sum(v.numel() * v.element_size() for v in res.values())
     n = min(K, 2000)
 
-    def one(i):
-        for k, v in host_in.items():
-            dev[k].copy_(v, non_blocking=True)
+    def kernels(i, d, o):
         if w.topk:
-            mla.decode_sparse(st.caches[0], dev["ql"], dev["qp"], dev["ends"], w.S, w.softmax_scale,
-                              dev["topk"], kv_new=dev["kv_new"], pe_new=dev["pe_new"], out=st.out,
-                              lse=st.lse, workspace=st.ws)
+            mla.decode_sparse(st.caches[0], d["ql"], d["qp"], d["ends"], w.S, w.softmax_scale, d["topk"],
+                              kv_new=d["kv_new"], pe_new=d["pe_new"], out=o["res"], lse=o["lse"],
+                              workspace=st.ws)
+            return
+        c = st.caches[i % st.rot]
+        for sp in st.start_pos:
+            mla.cache_append(c, d["kv_new"], d["pe_new"], sp)
+        ql = mla.absorb_q(d["qn"], st.wkv_b, out=st.ql) if w.absorb else d["ql"]
+        x = st.out if w.absorb else o["res"]
+        if w.mtp > 1:
+            mla.decode_mtp(c, ql, d["qp"], d["ends"], w.S, w.softmax_scale, out=x, lse=o["lse"],
+                           workspace=st.ws)
         else:
-            c = st.caches[i % st.rot]
-            for sp in st.start_pos:
-                mla.cache_append(c, dev["kv_new"], dev["pe_new"], sp)
-            ql = mla.absorb_q(dev["qn"], st.wkv_b, out=st.ql) if w.absorb else dev["ql"]
-            if w.mtp > 1:
-                mla.decode_mtp(c, ql, dev["qp"], dev["ends"], w.S, w.softmax_scale, out=st.out,
-                               lse=st.lse, workspace=st.ws)
-            else:
-                mla.decode(c, ql, dev["qp"], dev["ends"], w.S, w.softmax_scale, out=st.out,
-                           lse=st.lse, workspace=st.ws)
-            if w.absorb:
-                mla.project_out(st.out, st.wkv_b, out=st.o)
-        out_h.copy_(res, non_blocking=True)
-        lse_h.copy_(st.lse, non_blocking=True)
+            mla.decode(c, ql, d["qp"], d["ends"], w.S, w.softmax_scale, out=x, lse=o["lse"],
+                       workspace=st.ws)
+        if w.absorb:
+            mla.project_out(x, st.wkv_b, out=o["res"])
 
-    for i in range(min(W, 10)):
-        one(i)
+    comp, up, down = torch.cuda.Stream(st.device), torch.cuda.Stream(st.device), torch.cuda.Stream(st.device)
+    ev = lambda: torch.cuda.Event()
+    in_ready, in_free, out_ready, out_free = ([ev() for _ in range(2)] for _ in range(4))
+    used = [False, False]
+
+    def pipelined(i):
+        k = i % 2
+        if used[k]:
+            up.wait_event(in_free[k])       # the kernels of step i-2 are done with slot k's inputs
+            comp.wait_event(out_free[k])    # and its results are home
+        with torch.cuda.stream(up):
+            dev_in[k].copy_(host_in, non_blocking=True)
+            in_ready[k].record(up)
+        comp.wait_event(in_ready[k])
+        with torch.cuda.stream(comp):
+            kernels(i, vin[k], vout[k])
+            in_free[k].record(comp)
+            out_ready[k].record(comp)
+        down.wait_event(out_ready[k])
+        with torch.cuda.stream(down):
+            host_out.copy_(dev_out[k], non_blocking=True)
+            out_free[k].record(down)
+        used[k] = True
+
+    def serial(i):
+        dev_in[0].copy_(host_in, non_blocking=True)
+        kernels(i, vin[0], vout[0])
+        host_out.copy_(dev_out[0], non_blocking=True)
+
+    def graph_of(body):
+        # n steps, each with its own upload and read-back, in one CUDA graph
+        # (the other streams fork from and join the capturing one)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=comp):
+            fork = ev()
+            fork.record(comp)
+            up.wait_event(fork)
+            down.wait_event(fork)
+            for i in range(n):
+                body(i)
+            for s_ in (up, down):
+                j = ev()
+                j.record(s_)
+                comp.wait_event(j)
+        return g
+
+    def timed(g):
+        with torch.cuda.stream(comp):
+            g.replay()   # warm-up
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(comp):
+            e0.record(comp)
+            g.replay()
+            e1.record(comp)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / n
+
+    for i in range(min(W, 10)):   # eager warm-up of every call on the path
+        with torch.cuda.stream(comp):
+            serial(i)
     torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(n):
-        one(i)
-    e1.record()
-    torch.cuda.synchronize()
-    step_s = e0.elapsed_time(e1) / 1e3 / n
+    g_pipe = graph_of(pipelined)
+    step_s = timed(g_pipe)
+    del g_pipe
+    g_serial = graph_of(serial)
+    serial_s = timed(g_serial)
+    del g_serial
     cache_bytes = st.tokens * layout.cache_bytes_per_token(w.fmt)
     return {"value": round(cache_bytes / step_s / 1e12, 4), "unit": "TB/s", "steps": n,
             "ms_per_step": round(step_s * 1e3, 6), "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h,
-            "path": "python binding -> C ABI, pinned host buffers, per-step H2D inputs and D2H outputs"}
+            "serial_value": round(cache_bytes / serial_s / 1e12, 4),
+            "serial_ms_per_step": round(serial_s * 1e3, 6),
+            "path": "python binding -> C ABI, captured with the copies in one CUDA graph of the steps; per "
+                    "step one H2D of the step's inputs (pinned, laid end to end) and one D2H of its out "
+                    "and lse; two device slots, so the copies of a step overlap the kernels of the "
+                    "previous one (serial_*: copy, kernels, copy in one stream)"}
 
 
 # ------------------------------------------------------------ CPU oracle

@@ -49,3 +49,21 @@ def test_single_process_is_identity():
     import bench
     assert bench.slowest(4.25, "cpu") == 4.25
     assert bench.whole_job_rate(10.0, 1, 2.0) == 5.0
+
+
+def test_e2e_packing_round_trips_and_aligns():
+    # the end-to-end leg moves a step's inputs in one copy: every tensor gets a
+    # 256-byte-aligned, non-overlapping slice and reads back unchanged
+    import torch
+    import bench
+    named = {"a": torch.arange(7, dtype=torch.int32), "b": torch.randn(3, 5).to(torch.bfloat16),
+             "c": torch.randn(2, 2, 3)}
+    offs, total = bench._pack(named)
+    spans = sorted((offs[k], offs[k] + t.numel() * t.element_size()) for k, t in named.items())
+    assert all(o % 256 == 0 for o, _ in spans) and spans[-1][1] <= total
+    assert all(spans[i][1] <= spans[i + 1][0] for i in range(len(spans) - 1))
+    buf = torch.zeros(total, dtype=torch.uint8)
+    for k, v in bench._views(buf, offs, named).items():
+        v.copy_(named[k])
+    for k, v in bench._views(buf.clone(), offs, named).items():
+        assert v.dtype == named[k].dtype and v.shape == named[k].shape and torch.equal(v, named[k])
