@@ -274,8 +274,8 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
 // lse = log sum_i exp(lse_i).  The first warp fetches the descriptors of 32 of
 // the CTA's sequences at once, so sequences the decode kernel finished itself
 // (a single unit) cost one load between them, not a CTA each.  The partial
-// rows are fetched eight units at a time, loads first, so their latencies
-// overlap.
+// rows are fetched sixteen units at a time, loads first, so their latencies
+// overlap; the first sixteen are issued before the maximum of the lse values.
 __device__ __forceinline__ void combine_one(const Workspace& ws, int H, int h, int b, int2 sq,
                                             __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
   const int n = sq.y;
@@ -283,24 +283,36 @@ __device__ __forceinline__ void combine_one(const Workspace& ws, int H, int h, i
   const float* pl = ws.part_lse + (size_t)sq.x * H + h;            // unit stride H
   const float* po = ws.part_o + ((size_t)sq.x * H + h) * kDc + c;  // unit stride H * 512
   const size_t ostride = (size_t)H * kDc;
+  // the first kBatch partial rows are in flight while the maximum is formed
+  // (the loads do not depend on it)
+  constexpr int kBatch = 16;
+  float4 o[kBatch];
+  float l[kBatch];
+#pragma unroll
+  for (int k = 0; k < kBatch; ++k) {
+    if (k < n) {
+      o[k] = *reinterpret_cast<const float4*>(po + (size_t)k * ostride);
+      l[k] = pl[(size_t)k * H];
+    }
+  }
   float m = -INFINITY;
   for (int i = threadIdx.x & 31; i < n; i += 32) m = fmaxf(m, pl[(size_t)i * H]);
   m = warp_max(m);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
   if (m > -INFINITY) {
-    for (int i0 = 0; i0 < n; i0 += 8) {
-      float4 o[8];
-      float l[8];
+    for (int i0 = 0; i0 < n; i0 += kBatch) {
+      if (i0 > 0) {
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        if (i0 + k < n) {
-          o[k] = *reinterpret_cast<const float4*>(po + (size_t)(i0 + k) * ostride);
-          l[k] = pl[(size_t)(i0 + k) * H];
+        for (int k = 0; k < kBatch; ++k) {
+          if (i0 + k < n) {
+            o[k] = *reinterpret_cast<const float4*>(po + (size_t)(i0 + k) * ostride);
+            l[k] = pl[(size_t)(i0 + k) * H];
+          }
         }
       }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
+      for (int k = 0; k < kBatch; ++k) {
         if (i0 + k < n) {
           const float w = expf(l[k] - m);
           acc.x += w * o[k].x; acc.y += w * o[k].y; acc.z += w * o[k].z; acc.w += w * o[k].w;
