@@ -274,8 +274,9 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
 // lse = log sum_i exp(lse_i).  The first warp fetches the descriptors of 32 of
 // the CTA's sequences at once, so sequences the decode kernel finished itself
 // (a single unit) cost one load between them, not a CTA each.  The partial
-// rows are fetched sixteen units at a time, loads first, so their latencies
-// overlap; the first sixteen are issued before the maximum of the lse values.
+// rows are fetched eight units at a time, loads first, so their latencies
+// overlap; the first eight are issued before the maximum of the lse values
+// (sixteen at a time cost occupancy: slower on most workloads).
 __device__ __forceinline__ void combine_one(const Workspace& ws, int H, int h, int b, int2 sq,
                                             __nv_bfloat16* __restrict__ out, float* __restrict__ lse_out) {
   const int n = sq.y;
@@ -285,7 +286,7 @@ __device__ __forceinline__ void combine_one(const Workspace& ws, int H, int h, i
   const size_t ostride = (size_t)H * kDc;
   // the first kBatch partial rows are in flight while the maximum is formed
   // (the loads do not depend on it)
-  constexpr int kBatch = 16;
+  constexpr int kBatch = 8;
   float4 o[kBatch];
   float l[kBatch];
 #pragma unroll
