@@ -146,6 +146,24 @@ MLA_API mla_status mla_decode(const mla_cache* cache, const void* q_latent, cons
                       size_t ws_bytes, void* stream);
 
 /*
+ * mla_selftest_decode_timeout -- self-test of the kernels' bounded waits
+ *
+ * Runs mla_decode (same arguments, same checks; H = 128, the tensor-memory
+ * kernel) with two changes: the first unit's first tile of cache rows is
+ * never loaded, and every wait in the decode kernel gives up after 2^16 polls
+ * (milliseconds).  The waits on the missing tile run out, the unit's CTA pair
+ * records MLA_DEV_PIPELINE_TIMEOUT in the workspace status word, drains what
+ * it issued, frees its tensor memory and exits; the call completes.  Outputs
+ * are unspecified; the device stays usable.  Returns MLA_ERR_UNSUPPORTED if
+ * the tensor-memory kernel is not the one that would run.
+ */
+MLA_API mla_status mla_selftest_decode_timeout(const mla_cache* cache, const void* q_latent,
+                                               const void* q_pe, const int32_t* end_pos,
+                                               int32_t max_end_pos, int32_t B, int32_t H,
+                                               float softmax_scale, void* out, float* lse,
+                                               void* workspace, size_t ws_bytes, void* stream);
+
+/*
  * mla_decode_mtp -- absorbed decode of s new tokens per sequence at once
  * (multi-token decode: speculative or multi-token-prediction steps).  The s
  * new rows of cache slot b are its positions end_pos[b]-s .. end_pos[b]-1

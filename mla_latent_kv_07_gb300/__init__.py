@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
             L.mla_workspace_size.restype = SZ
             L.mla_decode.argtypes = [P, P, P, P, I32, I32, I32, F, P, P, P, SZ, P]
             L.mla_decode.restype = I32
+            L.mla_selftest_decode_timeout.argtypes = [P, P, P, P, I32, I32, I32, F, P, P, P, SZ, P]
+            L.mla_selftest_decode_timeout.restype = I32
             L.mla_decode_mtp.argtypes = [P, P, P, P, I32, I32, I32, I32, F, P, P, P, SZ, P]
             L.mla_decode_mtp.restype = I32
             L.mla_decode_sparse.argtypes = [P, P, P, P, I32, I32, I32, F, P, I32, P, P, P, P, P,
@@ -178,6 +180,22 @@ def decode(cache: Cache, q_latent, q_pe, end_pos, max_end_pos: int, softmax_scal
                             B, H, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
                             workspace.numel(), _stream(stream)), "mla_decode")
     return out, lse
+
+
+def selftest_decode_timeout(cache: Cache, q_latent, q_pe, end_pos, max_end_pos: int,
+                            softmax_scale: float, workspace, stream=None) -> int:
+    """mla_decode with the first unit's first tile withheld and short waits:
+    returns the workspace status word (MLA_DEV_PIPELINE_TIMEOUT expected)."""
+    B, H, _ = q_latent.shape
+    _need(q_latent, torch.bfloat16, (B, H, 512), "q_latent")
+    _need(q_pe, torch.bfloat16, (B, H, 64), "q_pe")
+    _need(end_pos, torch.int32, (B,), "end_pos")
+    out, lse = _outputs(B, H, q_latent.device, None, None, True)
+    _check(lib().mla_selftest_decode_timeout(cache.ref, _ptr(q_latent), _ptr(q_pe), _ptr(end_pos),
+                                             int(max_end_pos), B, H, float(softmax_scale), _ptr(out),
+                                             _ptr(lse), _ptr(workspace), workspace.numel(),
+                                             _stream(stream)), "mla_selftest_decode_timeout")
+    return workspace_status(workspace, stream)
 
 
 def decode_mtp(cache: Cache, q_latent, q_pe, end_pos, max_end_pos: int, softmax_scale: float,

@@ -117,6 +117,8 @@ struct DecodeParams {
   Workspace ws;
   int K;                  // sparse list length (0 = dense)
   int mtp_s;              // new tokens per cache slot: sequence b reads slot b / mtp_s (1: plain decode)
+  long long spin_limit = 0;   // polls a bounded wait makes before it gives up (0: the default)
+  int withhold_tile = -1;     // self-test of the bounded waits: this tile of the first unit is never loaded (-1: none)
 };
 
 // Raise a kernel's dynamic shared memory limit once per device.  The kernel

@@ -132,6 +132,8 @@ mla::DecodeParams make_params(const DecodeArgs& a, const mla::Workspace& ws, int
   p.ws = ws;
   p.K = K;
   p.mtp_s = a.mtp_s;
+  p.spin_limit = 0;
+  p.withhold_tile = -1;
   return p;
 }
 
@@ -148,7 +150,8 @@ bool use_tc_path(int H) {
 }
 
 // schedule -> decode -> combine, after the lengths are known on the device.
-mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cudaStream_t s) {
+mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cudaStream_t s,
+                      long long spin_limit = 0, int withhold_tile = -1) {
   int sms = 0;
   num_sms(&sms);
   const bool tc = use_tc_path(a.H);
@@ -159,8 +162,10 @@ mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cuda
       s);
   if (e != cudaSuccess) return cuda_fail(e, "schedule");
   const bool traced = trace_start(s);
-  e = tc ? mla::launch_decode_tc(make_params(a, ws, K), s)
-         : mla::launch_decode_mma(make_params(a, ws, K), s);
+  mla::DecodeParams p = make_params(a, ws, K);
+  p.spin_limit = spin_limit;
+  p.withhold_tile = withhold_tile;
+  e = tc ? mla::launch_decode_tc(p, s) : mla::launch_decode_mma(p, s);
   trace_stop(s, traced);
   if (e != cudaSuccess) return cuda_fail(e, "decode");
   e = mla::launch_combine(ws, a.B, a.H, a.out, a.lse, s);
@@ -226,6 +231,22 @@ mla_status mla_decode(const mla_cache* cache, const void* q_latent, const void* 
   if (st != MLA_OK) return st;
   // the schedule kernel, first of the dense call, clears the status word
   return run_decode(a, ws, 0, static_cast<cudaStream_t>(stream));
+}
+
+mla_status mla_selftest_decode_timeout(const mla_cache* cache, const void* q_latent, const void* q_pe,
+                                       const int32_t* end_pos, int32_t max_end_pos, int32_t B, int32_t H,
+                                       float softmax_scale, void* out, float* lse, void* workspace,
+                                       size_t ws_bytes, void* stream) {
+  g_last_error[0] = 0;
+  DecodeArgs a{cache, q_latent, q_pe, end_pos, max_end_pos, B, H, softmax_scale, out, lse,
+               workspace, ws_bytes, 1};
+  mla::Workspace ws;
+  mla_status st = check_decode(a, 0, &ws);
+  if (st != MLA_OK) return st;
+  if (!use_tc_path(H)) return MLA_ERR_UNSUPPORTED;
+  // the first unit's first tile is never loaded; every wait gives up after
+  // 2^16 polls (milliseconds)
+  return run_decode(a, ws, 0, static_cast<cudaStream_t>(stream), 1LL << 16, 0);
 }
 
 mla_status mla_decode_mtp(const mla_cache* cache, const void* q_latent, const void* q_pe,

@@ -149,6 +149,26 @@ def test_empty_and_clamped_sequences():
     assert mla.workspace_status(ws) == 0
 
 
+@pytest.mark.parametrize("fmt", [0, 1])
+def test_bounded_wait_runs_out_and_reports(fmt):
+    # the self-test withholds the first unit's first tile: its waits run out
+    # (milliseconds), the status word says so, the call completes, and the
+    # next decode on the same device and workspace is correct
+    B, S, H = 2, 300, 128
+    oc = oracle_cache(_rand_bf16((B, S, 512), 131), _rand_bf16((B, S, 64), 132), fmt)
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((B, H, 512), 133).cuda(), _rand_bf16((B, H, 64), 134).cuda()
+    ends = torch.tensor([300, 200], dtype=torch.int32).cuda()
+    ws = mla.alloc_workspace(B, H, S)
+    flags = mla.selftest_decode_timeout(dc, ql, qp, ends, S, 0.2, ws)
+    assert flags & mla.DEV_PIPELINE_TIMEOUT
+    out, lse = mla.decode(dc, ql, qp, ends, S, 0.2, workspace=ws)
+    assert mla.workspace_status(ws) == 0
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql.cpu()), bits(qp.cpu()), ends.cpu().numpy(), 0.2)
+    check_close(f64(out).reshape(-1, 512), ref, "out")
+    check_close(f64(lse).reshape(-1), ref_lse, "lse")
+
+
 def test_workspace_too_small_is_refused():
     oc = oracle_cache(_rand_bf16((1, 32, 512), 41), _rand_bf16((1, 32, 64), 42), 0)
     dc = device_cache(oc)
