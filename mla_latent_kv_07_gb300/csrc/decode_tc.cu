@@ -80,7 +80,11 @@ template <int kFmt, bool kSparse>
 struct Cfg {
   static constexpr bool kConv = kFmt == 1 || kSparse;       // converter warps present
   static constexpr int kN = 48;    // positions per tile
-  static constexpr int kBufs = 2;  // S and P buffers
+  static constexpr int kSBufs = 2;  // S buffers (tensor memory)
+  // P buffers (shared memory): three where there is room (bf16), so the
+  // softmax writes P of tile i once PV of tile i-3 is done -- PV of tile i-2
+  // runs behind the QK of tile i in the in-order tensor pipe
+  static constexpr int kPBufs = kFmt == 0 ? 3 : 2;
   // exchange buffers: two, except with FP8 caches, whose fourth operand stage
   // takes the room of the second (the softmax reads a tile's exchange buffer
   // well before the peer's partial of the next tile is due)
@@ -112,7 +116,7 @@ struct Cfg {
   static constexpr int kRawSlots = kConv ? 2 : 0;
   static constexpr int kRawOff = kStages * kStage;
   static constexpr int kPOff = kRawOff + kRawSlots * kRaw;
-  static constexpr int kXOff = kPOff + kBufs * kPBytes;
+  static constexpr int kXOff = kPOff + kPBufs * kPBytes;
   static constexpr int kBarOff = kXOff + kXBufs * kXBytes;
   // query staging (5 swizzled blocks): the P and exchange buffers, or with
   // FP8 caches operand stages 1-3, which the converter fills only once the
@@ -121,10 +125,10 @@ struct Cfg {
   static constexpr int kSmem = kBarOff + 4096 + 1024;      // barriers/flags + base alignment slack
   static_assert(kSmem <= 232448, "shared memory budget");
   static_assert(kStage % 1024 == 0 && kRaw % 1024 == 0, "1 KB alignment of swizzled tiles");
-  static_assert(kN % 16 == 0 && kTmemS + kBufs * kN <= 512, "tile width");
+  static_assert(kN % 16 == 0 && kTmemS + kSBufs * kN <= 512, "tile width");
   // the output half is staged from offset 0 (8 blocks of 32 fp32 columns)
   static_assert(kFmt == 1 ? (kStages - 1) * kStage >= 5 * kSwBlk
-                          : kBufs * kPBytes + kXBufs * kXBytes >= 5 * kSwBlk,
+                          : kPBufs * kPBytes + kXBufs * kXBytes >= 5 * kSwBlk,
                 "query staging fits");
   static_assert(kQOff % 1024 == 0 && kPOff % 1024 == 0, "1 KB alignment of the query staging");
   static_assert(kBarOff >= 8 * kSwBlk, "output staging fits the idle buffers");
@@ -163,7 +167,7 @@ struct Bars {
   uint64_t deq[4];     // operand stage converted
   uint64_t empty[4];   // PV done: operand stage free
   uint64_t rfree[2];   // raw slot read by the converter
-  uint64_t sfull[2], sfree[2], pfull[2], pfree[2], xfull[2], xempty[2];
+  uint64_t sfull[2], sfree[2], pfull[3], pfree[3], xfull[2], xempty[2];
   uint64_t drain;   // final commit of the MMA issuer
   uint64_t qbar;    // query rows staged in shared memory
   uint64_t qready;  // query half in tensor memory
@@ -287,10 +291,12 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   auto rpe = [&](int r) { return raw(r) + kN * C::kRawRow + C::kScBytes; };
   auto pbuf = [&](int b) { return sm + C::kPOff + b * C::kPBytes; };
   auto xbuf = [&](int b) { return reinterpret_cast<float*>(sm + C::kXOff + b * C::kXBytes); };
-  // tile i uses S, P and exchange buffer bsel(i); bpar(i) is the parity of
-  // the phase that tile completes on that buffer's barriers
-  auto bsel = [](int i) { return i % C::kBufs; };
-  auto bpar = [](int i) { return (uint32_t)((i / C::kBufs) & 1); };
+  // tile i uses S buffer ssel(i) and P buffer psel(i); spar(i) / ppar(i) is
+  // the parity of the phase that tile completes on that buffer's barriers
+  auto ssel = [](int i) { return i % C::kSBufs; };
+  auto spar = [](int i) { return (uint32_t)((i / C::kSBufs) & 1); };
+  auto psel = [](int i) { return i % C::kPBufs; };
+  auto ppar = [](int i) { return (uint32_t)((i / C::kPBufs) & 1); };
   auto xsel = [](int i) { return i % C::kXBufs; };   // the same for exchange buffers
   auto xpar = [](int i) { return (uint32_t)((i / C::kXBufs) & 1); };
 
@@ -302,11 +308,13 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       bar_init(&bars->empty[j], 1);
     }
     for (int r = 0; r < 2; ++r) bar_init(&bars->rfree[r], kConvWarps);
+    for (int b = 0; b < C::kPBufs; ++b) {
+      bar_init(&bars->pfull[b], 8);
+      bar_init(&bars->pfree[b], 1);
+    }
     for (int b = 0; b < 2; ++b) {
       bar_init(&bars->sfull[b], 1);
       bar_init(&bars->sfree[b], 12);   // softmax (8) and exchange (4) warps read S
-      bar_init(&bars->pfull[b], 8);
-      bar_init(&bars->pfree[b], 1);
       bar_init(&bars->xfull[b], 4);
       bar_init(&bars->xempty[b], 8);   // the peer's softmax warps
     }
@@ -449,7 +457,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer
     // Event-driven: QK of the next tile is issued as soon as its stage, its
-    // converted operand and its S buffer are ready (at most kBufs tiles ahead
+    // converted operand and its S buffer are ready (at most kSBufs tiles ahead
     // of the softmax); PV of the next tile as soon as its P is written.
     // Neither waits behind the other's inputs.
     if (lane == 0) {
@@ -469,8 +477,8 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         // PV first: it is on the critical path (the softmax waits for it), and
         // issuing the 18 QK instructions takes about as long as running them
         if (np < nq) {
-          const int i = np, j = i % C::kStages, b = bsel(i);
-          if (bar_try(&bars->pfull[b], bpar(i))) {
+          const int i = np, j = i % C::kStages, b = psel(i);
+          if (bar_try(&bars->pfull[b], ppar(i))) {
             tc_after();
             const uint64_t pd = sdesc_at(d_p0, b * C::kPBytes), vd = sdesc_at(d_v0, j * C::kStage);
             if (i == 0)
@@ -488,10 +496,10 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           }
         }
         if (nq < ntiles && nq < np + C::kQkAhead) {
-          const int k = nq, j = k % C::kStages, b = bsel(k);
+          const int k = nq, j = k % C::kStages, b = ssel(k);
           const uint32_t use = k / C::kStages;
           if (bar_try(C::kConv ? &bars->deq[j] : &bars->full[j], use & 1) &&
-              bar_try(&bars->sfree[b], bpar(k) ^ 1)) {
+              bar_try(&bars->sfree[b], spar(k) ^ 1)) {
             tc_after();
             const uint32_t sd = tmem + kTmemS + b * kN;
             const uint64_t kd = sdesc_at(d_k0, j * C::kStage);
@@ -526,8 +534,8 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     const int h = threadIdx.x - 256;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     for (int i = 0; i < ntiles; ++i) {
-      const int b = bsel(i);
-      if (!wt.wait(&bars->sfull[b], bpar(i))) break;
+      const int b = ssel(i);
+      if (!wt.wait(&bars->sfull[b], spar(i))) break;
       tc_after();
       const uint32_t sb = lane_base + kTmemS + b * kN;
       uint32_t r[kN];
@@ -565,13 +573,13 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int i = 0; i < ntiles; ++i) {
-      const int j = i % C::kStages, b = bsel(i);
-      const uint32_t par = bpar(i);
+      const int j = i % C::kStages, sb_i = ssel(i), b = psel(i);
+      const uint32_t par = ppar(i);
       float sc[24];
-      ok = ok && wt.wait(&bars->sfull[b], par);
+      ok = ok && wt.wait(&bars->sfull[sb_i], spar(i));
       {
         tc_after();
-        const uint32_t sb = lane_base + kTmemS + b * kN;
+        const uint32_t sb = lane_base + kTmemS + sb_i * kN;
         uint32_t r[24];
         TC_LD16(sb + p0, r);
         TC_LD8(sb + p1, (r + 16));
@@ -580,7 +588,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         for (int k = 0; k < 24; ++k) sc[k] = __uint_as_float(r[k]);
         tc_before();
         __syncwarp();
-        if (lane == 0) bar_arrive(&bars->sfree[b]);   // QK of tile i + kBufs may overwrite
+        if (lane == 0) bar_arrive(&bars->sfree[sb_i]);   // QK of tile i + kSBufs may overwrite
       }
       // + the peer's partial (fp32 addition commutes: both CTAs get the same S)
       const int xb = xsel(i);
@@ -632,7 +640,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           // the previous use of that buffer is known complete, so the parity
           // wait cannot be fooled by a phase two steps back), then scale this
           // thread's half of the lane's row
-          ok = ok && wt.wait(&bars->pfree[bsel(i - 1)], bpar(i - 1));
+          ok = ok && wt.wait(&bars->pfree[psel(i - 1)], ppar(i - 1));
           tc_after();
 #pragma unroll 1
           for (int c = 4 * sh; c < 4 * sh + 4; ++c) {
@@ -690,7 +698,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     }
     // ------------------------------------------------------------ epilogue
     if (live) {
-      if (ntiles > 0) ok = ok && wt.wait(&bars->pfree[bsel(ntiles - 1)], bpar(ntiles - 1));
+      if (ntiles > 0) ok = ok && wt.wait(&bars->pfree[psel(ntiles - 1)], ppar(ntiles - 1));
       tc_after();
       // O half (128 heads x 256 fp32) -> workspace, normalised by the head's
       // l (the sum of the pair's halves).  With the last PV complete, every
