@@ -102,9 +102,12 @@ struct Cfg {
   static constexpr int kOplBytes = 4 * kBlkBytes;  // latent half operand
   static constexpr int kOpeBytes = kBlkBytes;      // rotary operand (full 64 columns)
   static constexpr int kPBytes = ((kN + 63) / 64) * kSwBlk;  // P: 128 heads x kN bf16, swizzled
-  // exchange buffer: float4 chunk c (positions 4c..4c+3) of head h at index
-  // c * 128 + h, so a warp's remote store is one contiguous 512-byte run
-  static constexpr int kXBytes = (kN / 4) * 128 * 16;
+  // exchange buffer: a head's kN partial scores as 24-bit codes (the fp32
+  // value rounded to its top 24 bits), four positions in three words, so
+  // 3 kN / 4 words = kXRows 16-byte rows per head; row q of head h at index
+  // q * 128 + h, so a warp's remote store is one contiguous 512-byte run
+  static constexpr int kXRows = 3 * kN / 16;
+  static constexpr int kXBytes = kXRows * 128 * 16;
   static constexpr int kStage = kOplBytes + kOpeBytes;
   static constexpr int kStages = kConv ? (kFmt == 1 ? 4 : 2) : 4;
   static constexpr int kRawRow = kFmt == 1 ? kHalf : kHalf * 2;  // bytes of a raw latent half row
@@ -151,6 +154,29 @@ __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;"
 __device__ __forceinline__ void pair_sync(int q) {
   asm volatile("bar.sync %0, 64;" ::"r"(2 + q) : "memory");
 }
+// Partial scores cross between the pair as the top 24 bits of the fp32 value,
+// rounded (add half the dropped unit, truncate): relative error at most 2^-16
+// for normal values; both CTAs round their own partial the same way before
+// adding, so the pair still computes bit-identical scores.
+__device__ __forceinline__ float round24(float x) {
+  return __uint_as_float((__float_as_uint(x) + 0x80u) & 0xFFFFFF00u);
+}
+// four fp32 bit patterns -> three words of 24-bit codes
+__device__ __forceinline__ void pack24(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t& w0,
+                                       uint32_t& w1, uint32_t& w2) {
+  a = (a + 0x80u) >> 8;
+  b = (b + 0x80u) >> 8;
+  c = (c + 0x80u) >> 8;
+  d = (d + 0x80u) >> 8;
+  w0 = a | (b << 24);
+  w1 = (b >> 8) | (c << 16);
+  w2 = (c >> 16) | (d << 8);
+}
+__device__ __forceinline__ float4 unpack24(uint32_t w0, uint32_t w1, uint32_t w2) {
+  return make_float4(__uint_as_float(w0 << 8), __uint_as_float(__funnelshift_r(w0, w1, 24) << 8),
+                     __uint_as_float(__funnelshift_r(w1, w2, 16) << 8), __uint_as_float(w2 & 0xFFFFFF00u));
+}
+
 // 2^x with the hardware approximation (relative error far below the bf16
 // rounding P receives); 0 for -inf
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -548,10 +574,14 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       const int xb = xsel(i);
       if (!wt.wait(&bars->xempty[xb], xpar(i))) break;   // phase 0: the peer's query staging is done
       const uint32_t xd = mapa(xbuf(xb) + 4 * h, peer);
+      uint32_t w[C::kXRows * 4];
 #pragma unroll
-      for (int c = 0; c < kN / 4; ++c)
-        asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(xd + 16 * 128 * c),
-                     "r"(r[4 * c]), "r"(r[4 * c + 1]), "r"(r[4 * c + 2]), "r"(r[4 * c + 3])
+      for (int g = 0; g < kN / 4; ++g)
+        pack24(r[4 * g], r[4 * g + 1], r[4 * g + 2], r[4 * g + 3], w[3 * g], w[3 * g + 1], w[3 * g + 2]);
+#pragma unroll
+      for (int q = 0; q < C::kXRows; ++q)
+        asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(xd + 16 * 128 * q),
+                     "r"(w[4 * q]), "r"(w[4 * q + 1]), "r"(w[4 * q + 2]), "r"(w[4 * q + 3])
                      : "memory");
       __syncwarp();
       if (lane == 0) bar_arrive_remote(mapa(&bars->xfull[xb], peer));
@@ -590,16 +620,32 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         __syncwarp();
         if (lane == 0) bar_arrive(&bars->sfree[sb_i]);   // QK of tile i + kSBufs may overwrite
       }
-      // + the peer's partial (fp32 addition commutes: both CTAs get the same S)
+      // + the peer's partial, both rounded to 24 bits (fp32 addition commutes:
+      // both CTAs get the same S).  This half's positions p0..p0+15 are code
+      // words 12 sh .. 12 sh + 11 (rows 3 sh .. 3 sh + 2), p1..p1+7 words
+      // 24 + 6 sh .. 24 + 6 sh + 5 (within rows 6 + sh, 7 + sh).
       const int xb = xsel(i);
       ok = ok && wt.wait(&bars->xfull[xb], xpar(i));
       {
-        const float4* xr = reinterpret_cast<const float4*>(xbuf(xb)) + h;
+        const uint4* xr = reinterpret_cast<const uint4*>(xbuf(xb)) + h;
+        uint32_t w[20];
+#pragma unroll
+        for (int q = 0; q < 5; ++q) {
+          const uint4 v = xr[128 * (q < 3 ? 3 * sh + q : 6 + sh + q - 3)];
+          w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+        }
 #pragma unroll
         for (int k = 0; k < 6; ++k) {
-          const float4 v = xr[128 * (k < 4 ? p0 / 4 + k : p1 / 4 + k - 4)];
-          const float2 a = __fadd2_rn(make_float2(sc[4 * k], sc[4 * k + 1]), make_float2(v.x, v.y));
-          const float2 c2 = __fadd2_rn(make_float2(sc[4 * k + 2], sc[4 * k + 3]), make_float2(v.z, v.w));
+          float4 v;
+          if (k < 4) {
+            v = unpack24(w[3 * k], w[3 * k + 1], w[3 * k + 2]);
+          } else {
+            const int t = 3 * (k - 4);
+            v = unpack24(sh ? w[14 + t] : w[12 + t], sh ? w[15 + t] : w[13 + t], sh ? w[16 + t] : w[14 + t]);
+          }
+          const float2 a = __fadd2_rn(make_float2(round24(sc[4 * k]), round24(sc[4 * k + 1])), make_float2(v.x, v.y));
+          const float2 c2 =
+              __fadd2_rn(make_float2(round24(sc[4 * k + 2]), round24(sc[4 * k + 3])), make_float2(v.z, v.w));
           sc[4 * k] = a.x; sc[4 * k + 1] = a.y; sc[4 * k + 2] = c2.x; sc[4 * k + 3] = c2.y;
         }
         __syncwarp();
