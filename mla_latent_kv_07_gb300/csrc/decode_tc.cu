@@ -115,7 +115,10 @@ struct Cfg {
   // gather lands 4 rows per 128-byte slot (a tensor copy's shared-memory
   // destination is 128-byte aligned)
   static constexpr int kScBytes = kFmt == 1 ? (kSparse ? 2048 : 1024) : 0;
-  static constexpr int kRaw = kConv ? kN * kRawRow + kScBytes + kN * 128 : 0;
+  // rotary bytes per raw row: dense FP8 loads only the CTA's 32 columns (the
+  // 32 its QK reads); gathers land whole 128-byte rows
+  static constexpr int kRawPe = (kFmt == 1 && !kSparse) ? kPeHalf * 2 : 128;
+  static constexpr int kRaw = kConv ? kN * kRawRow + kScBytes + kN * kRawPe : 0;
   static constexpr int kRawSlots = kConv ? 2 : 0;
   static constexpr int kRawOff = kStages * kStage;
   static constexpr int kPOff = kRawOff + kRawSlots * kRaw;
@@ -442,10 +445,10 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
               tma3(opl(j) + blk * kBlkBytes, &tp.m_kv, rank * kHalf + blk * 64, e0, slot, &bars->full[j]);
             tma3(ope(j), &tp.m_pe, 0, e0, slot, &bars->full[j]);
           } else {
-            bar_expect_tx(&bars->full[j], kN * kHalf + kN * 16 + kN * 128);
+            bar_expect_tx(&bars->full[j], kN * kHalf + kN * 16 + kN * C::kRawPe);
             tma3(raw(j), &tp.m_kv, rank * kHalf, e0, slot, &bars->full[j]);
             tma3(rsc(j), &tp.m_sc, 0, e0, slot, &bars->full[j]);
-            tma3(rpe(j), &tp.m_pe, 0, e0, slot, &bars->full[j]);
+            tma3(rpe(j), &tp.m_pe, rank * kPeHalf, e0, slot, &bars->full[j]);
           }
         }
       } else {
@@ -820,12 +823,16 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           *reinterpret_cast<uint4*>(dst + (q >> 3) * kBlkBytes + swz_chunk(row, q & 7)) = v;
         }
       }
-      // rotary rows -> swizzled operand
-      for (int idx = t; idx < kN * 8; idx += 32 * kConvWarps) {
-        const int row = idx >> 3, q = idx & 7;
+      // rotary rows -> swizzled operand (with half rows, the CTA's 16-byte
+      // chunks 4 rank .. 4 rank + 3 of the 64-column operand row, the only
+      // ones its QK reads)
+      constexpr int kPeChunks = C::kRawPe / 16;
+      const int pe_chunk0 = kPeChunks == 8 ? 0 : 4 * (int)rank;
+      for (int idx = t; idx < kN * kPeChunks; idx += 32 * kConvWarps) {
+        const int row = idx / kPeChunks, q = idx % kPeChunks;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < valid) v = *reinterpret_cast<const uint4*>(rpe(r) + row * 128 + q * 16);
-        *reinterpret_cast<uint4*>(ope(j) + swz_chunk(row, q)) = v;
+        if (row < valid) v = *reinterpret_cast<const uint4*>(rpe(r) + row * C::kRawPe + q * 16);
+        *reinterpret_cast<uint4*>(ope(j) + swz_chunk(row, pe_chunk0 + q)) = v;
       }
       fence_async_smem();
       __syncwarp();
@@ -987,8 +994,10 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s) {
            encode3(&tp.m_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.kv_scale, kNblk, S, slots, kNblk, n,
                    CU_TENSOR_MAP_SWIZZLE_NONE);
     }
-    // bf16: straight into the operand layout; FP8: plain rows for the converter
-    ok = ok && encode3(&tp.m_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.pe, kDr, S, slots, 64, n,
+    // bf16: straight into the operand layout; FP8: plain half rows (the
+    // CTA's 32 columns) for the converter
+    ok = ok && encode3(&tp.m_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.pe, kDr, S, slots,
+                       p.fmt == 0 ? 64 : kPeHalf, n,
                        p.fmt == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   ok = ok &&
