@@ -15,9 +15,10 @@
 // and rotary columns [32r, 32r+32):
 //   * QK: each CTA contracts its 288-wide half (Q half as the A operand held in
 //     tensor memory, K half from shared memory) into a partial S; the two
-//     partials are exchanged through distributed shared memory and summed.
-//     fp32 addition commutes, so both CTAs hold bit-identical S and take the
-//     same softmax decisions.
+//     partials are exchanged through distributed shared memory as 24-bit
+//     codes (each fp32 partial rounded to its top 24 bits, by both CTAs
+//     alike) and summed.  fp32 addition commutes, so both CTAs hold
+//     bit-identical S and take the same softmax decisions.
 //   * PV: each CTA multiplies P (shared memory) by its latent half V (the same
 //     shared-memory tile, read as an MN-major operand) into its own O half.
 // Every cache byte is fetched by exactly one CTA and there is no redundant
@@ -34,9 +35,10 @@
 //              online softmax (lazy rescale), P, epilogue
 //   warps 8-11 exchange: partial S of each tile from TMEM -> peer (DSMEM),
 //              as soon as it is computed.  Distributed shared memory moves
-//              ~40 GB/s per SM with ~0.3 us latency on this part, so sending
-//              runs as its own pipeline stage, ahead of the softmax; the
-//              softmax adds the peer's partial when it reads its own.
+//              ~20-35 GB/s per SM with ~0.3 us latency on this part (its
+//              delivery is on the tile's critical path), so sending runs as
+//              its own pipeline stage, ahead of the softmax; the softmax adds
+//              the peer's partial when it reads its own.
 //   warps 2-3 and 12-15 converter (FP8 caches and gathers): raw rows -> bf16
 //              operand tile bf16(fp32(e4m3 * scale)) in the 128-byte
 //              swizzled layout
