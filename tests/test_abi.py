@@ -72,6 +72,9 @@ def test_append_rejects_bad_arguments(L):
     assert L.mla_cache_append(ctypes.byref(c8), ok_args[1], ok_args[2], pos, 2, None) == 1
     cx = _cache(fmt=7)
     assert L.mla_cache_append(ctypes.byref(cx), ok_args[1], ok_args[2], pos, 2, None) == 3
+    wide = _cache(B=4096)                                  # more rows than one call may write
+    many = (ctypes.c_int32 * 2049)(*([0] * 2049))
+    assert L.mla_cache_append(ctypes.byref(wide), ok_args[1], ok_args[2], many, 2049, None) == 1
 
 
 def test_decode_rejects_bad_arguments(L):

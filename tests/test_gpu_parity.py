@@ -436,3 +436,56 @@ def test_workload7_attention_step():
     o_ref = orc.project_out(x, bits(wkv))
     check_close(f64(ql).reshape(-1, 512), ql_ref.reshape(-1, 512), "q_latent")
     check_close(np.stack([o[b, h] for b, h in pairs]), np.stack([o_ref[b, h] for b, h in pairs]), "o")
+
+
+# ---------------------------------------------------------------- limits
+
+def test_limits_longest_list_most_tokens_most_rows():
+    # the largest top-k list (8192 entries, with repeats and a ragged length),
+    # the largest multi-token call (1024 tokens) and the largest append (2048
+    # rows), each against the oracle
+    B, S, H, K = 2, 9000, 128, 8192
+    oc = oracle_cache(_rand_bf16((B, S, 512), 141), _rand_bf16((B, S, 64), 142), 1)
+    dc = device_cache(oc)
+    ends = np.array([9000, 8500], np.int32)
+    rng = np.random.default_rng(143)
+    topk = np.stack([rng.permutation(int(T))[:K] for T in ends]).astype(np.int32)
+    topk[1, :100] = topk[1, 100]                            # repeats count once
+    ql, qp = _rand_bf16((B, H, 512), 144), _rand_bf16((B, H, 64), 145)
+    gidx = torch.empty((B, K), dtype=torch.int32, device="cuda")
+    gcnt = torch.empty((B,), dtype=torch.int32, device="cuda")
+    out, lse = mla.decode_sparse(dc, ql.cuda(), qp.cuda(), torch.from_numpy(ends).cuda(), S, 0.13,
+                                 torch.from_numpy(topk).cuda(), gidx=gidx, gcount=gcnt)
+    ref_g, ref_c = orc.sparse_gather_lists(topk, ends)
+    assert np.array_equal(gidx.cpu().numpy(), ref_g) and np.array_equal(gcnt.cpu().numpy(), ref_c)
+    pairs = sample_pairs(B, H, 6, 146)
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), ends, 0.13, pairs=pairs, topk=topk)
+    o, l = f64(out), f64(lse)
+    check_close(np.stack([o[b, h] for b, h in pairs]), ref, "sparse out")
+    check_close(np.array([l[b, h] for b, h in pairs]), ref_lse, "sparse lse")
+
+    s, T = 1024, 1100
+    oc0 = oracle_cache(_rand_bf16((1, T, 512), 147), _rand_bf16((1, T, 64), 148), 0)
+    dc0 = device_cache(oc0)
+    qm, qpm = _rand_bf16((1, s, H, 512), 149), _rand_bf16((1, s, H, 64), 150)
+    e = np.array([T], np.int32)
+    om, lm = mla.decode_mtp(dc0, qm.cuda(), qpm.cuda(), torch.from_numpy(e).cuda(), T, 0.13,
+                            workspace=mla.alloc_workspace(s, H, T))
+    om, lm = f64(om), f64(lm)
+    for j in (0, 511, 1023):
+        pairs = sample_pairs(1, H, 4, 151 + j)
+        ref, ref_lse = orc.decode_absorbed_mtp(oc0, bits(qm), bits(qpm), e, 0.13, token=j, pairs=pairs)
+        check_close(np.stack([om[b, j, h] for b, h in pairs]), ref, f"token {j} out")
+        check_close(np.array([lm[b, j, h] for b, h in pairs]), ref_lse, f"token {j} lse")
+
+    R = 2048
+    oc1 = oracle_cache(_rand_bf16((R, 4, 512), 152), _rand_bf16((R, 4, 64), 153), 1)
+    dc1 = device_cache(oc1)
+    kv_new, pe_new = _rand_bf16((R, 512), 154), _rand_bf16((R, 64), 155)
+    start = np.random.default_rng(156).integers(0, 4, R).astype(np.int32)
+    mla.cache_append(dc1, kv_new.cuda(), pe_new.cuda(), start)
+    orc.cache_append(oc1, bits(kv_new), bits(pe_new), start)
+    torch.cuda.synchronize()
+    assert np.array_equal(dc1.kv.cpu().numpy(), oc1["kv"])
+    assert np.array_equal(dc1.kv_scale.cpu().numpy().view(np.uint32), oc1["kv_scale"].view(np.uint32))
+    assert np.array_equal(bits(dc1.pe.cpu()), oc1["pe"])
