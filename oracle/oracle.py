@@ -170,6 +170,30 @@ def sparse_gather_lists(topk, end_pos) -> tuple[np.ndarray, np.ndarray]:
     return gidx, gcount
 
 
+def topk_select(scores, end_pos, K: int) -> np.ndarray:
+    """Top-k position selection per sequence (the ``topk_indices`` the V3.2
+    sparse decode consumes, "DeepSeek-V3.2-Exp . KV cache", MQA-decode
+    excerpt: an index list per sequence that the mask keeps).  The pages show
+    only the call, not the scoring; the selection taken here is its plainest
+    reading: among positions 0 .. end_pos[b]-1 of row b of ``scores`` [B, S]
+    (fp32), the K with the largest score; equal scores go to the lower
+    position; -0 equals +0; NaN ranks below -inf.  Returns int32 [B, K]: the
+    selected positions in increasing order, then -1 (fewer than K valid)."""
+    s = np.asarray(scores, np.float32)
+    B, S = s.shape
+    ep = np.asarray(end_pos).reshape(-1)
+    out = np.full((B, K), -1, np.int32)
+    for b in range(B):
+        T = int(min(max(int(ep[b]), 0), S))
+        row = s[b, :T].astype(np.float64)
+        nan = np.isnan(row)
+        neg = np.where(nan, 0.0, -row)            # score descending; -0 == +0
+        order = np.lexsort((np.arange(T), neg, nan))   # last key first: non-NaN, score, position
+        sel = np.sort(order[:K])
+        out[b, :sel.size] = sel
+    return out
+
+
 # ------------------------------------------------------ absorbed decode
 
 def decode_absorbed(cache: dict, q_latent, q_pe, end_pos, softmax_scale: float,
