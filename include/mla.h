@@ -146,6 +146,29 @@ MLA_API mla_status mla_decode(const mla_cache* cache, const void* q_latent, cons
                       size_t ws_bytes, void* stream);
 
 /*
+ * mla_topk_select -- top-k position selection per sequence: the index lists
+ * that mla_decode_sparse consumes ("DeepSeek-V3.2-Exp . KV cache",
+ * MQA-decode excerpt: topk_indices, one list per sequence, shared by its
+ * heads).  The pages show the indexer only as a call; the selection is its
+ * plainest reading, and the scores that feed it are an input here.
+ *
+ *   scores      device fp32 [B][max_end_pos] (row b = sequence b's score per
+ *               position; row stride max_end_pos)
+ *   end_pos     device int32 [B]: positions 0 .. end_pos[b]-1 compete
+ *               (clamped to [0, max_end_pos])
+ *   K           1 <= K <= 8192
+ *   topk_idx    device int32 [B][K] (out): the K positions with the largest
+ *               score, ties to the lower position, -0 equal to +0, NaN below
+ *               -inf; in increasing order; fewer than K valid positions: all
+ *               of them, then -1
+ *
+ * Errors: MLA_ERR_INVALID_ARG for null or misaligned pointers, B < 1,
+ * max_end_pos < 1, K outside 1..8192.  One kernel launch on `stream`.
+ */
+MLA_API mla_status mla_topk_select(const float* scores, const int32_t* end_pos, int32_t B,
+                                   int32_t max_end_pos, int32_t K, int32_t* topk_idx, void* stream);
+
+/*
  * mla_selftest_decode_timeout -- self-test of the kernels' bounded waits
  *
  * Runs mla_decode (same arguments, same checks; H = 128, the tensor-memory

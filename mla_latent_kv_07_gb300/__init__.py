@@ -61,6 +61,8 @@ def lib() -> ctypes.CDLL:
             L.mla_workspace_size.restype = SZ
             L.mla_decode.argtypes = [P, P, P, P, I32, I32, I32, F, P, P, P, SZ, P]
             L.mla_decode.restype = I32
+            L.mla_topk_select.argtypes = [P, P, I32, I32, I32, P, P]
+            L.mla_topk_select.restype = I32
             L.mla_selftest_decode_timeout.argtypes = [P, P, P, P, I32, I32, I32, F, P, P, P, SZ, P]
             L.mla_selftest_decode_timeout.restype = I32
             L.mla_decode_mtp.argtypes = [P, P, P, P, I32, I32, I32, I32, F, P, P, P, SZ, P]
@@ -180,6 +182,21 @@ def decode(cache: Cache, q_latent, q_pe, end_pos, max_end_pos: int, softmax_scal
                             B, H, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
                             workspace.numel(), _stream(stream)), "mla_decode")
     return out, lse
+
+
+def topk_select(scores, end_pos, K: int, out=None, stream=None):
+    """Top-k positions per sequence from fp32 scores [B, max_end_pos]:
+    int32 [B, K], increasing, -1 padded (the index lists decode_sparse takes)."""
+    B, S = scores.shape
+    if scores.dtype != torch.float32 or not scores.is_contiguous() or not scores.is_cuda:
+        raise ValueError(f"scores: want contiguous cuda float32 [B, S], got {scores.dtype} on {scores.device}")
+    _need(end_pos, torch.int32, (B,), "end_pos")
+    if out is None:
+        out = torch.empty((B, K), dtype=torch.int32, device=scores.device)
+    _need(out, torch.int32, (B, K), "out")
+    _check(lib().mla_topk_select(_ptr(scores), _ptr(end_pos), B, S, int(K), _ptr(out), _stream(stream)),
+           "mla_topk_select")
+    return out
 
 
 def selftest_decode_timeout(cache: Cache, q_latent, q_pe, end_pos, max_end_pos: int,

@@ -394,6 +394,116 @@ __global__ void __launch_bounds__(512) read_ceiling_kernel(const uint4* __restri
   }
 }
 
+
+// ----------------------------------------------------------- top-k select
+// One CTA per sequence selects, among positions 0 .. end_pos-1 of its score
+// row, the K with the largest score (equal scores: the lower position; -0
+// equals +0; NaN ranks lowest) and writes them in increasing order, then -1.
+// Scores map to order-preserving 32-bit keys; a radix select over the key's
+// four bytes (most significant first, a shared 256-bin histogram per pass,
+// increments aggregated per warp) finds the K-th largest key t and how many
+// keys equal to t belong to the selection; a last pass over contiguous runs
+// of positions (one per thread, offsets from two block scans) writes the
+// selected positions in order.
+__device__ __forceinline__ uint32_t score_key(float x) {
+  if (x != x) return 0u;                             // NaN: below every number
+  const uint32_t u = x == 0.f ? 0u : __float_as_uint(x);   // -0 -> +0
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__global__ void __launch_bounds__(1024) topk_select_kernel(const float* __restrict__ scores, int ld,
+                                                          const int* __restrict__ end_pos,
+                                                          int max_end_pos, int K,
+                                                          int* __restrict__ out) {
+  __shared__ uint32_t hist[256];
+  __shared__ int scan_smem[33];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_krem;
+  pdl_wait();
+  pdl_trigger();
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  int T = end_pos[b];
+  T = T < 0 ? 0 : (T > max_end_pos ? max_end_pos : T);
+  const float* row = scores + (size_t)b * ld;
+  int* o = out + (size_t)b * K;
+  if (T <= K) {   // every valid position is selected
+    for (int k = tid; k < K; k += blockDim.x) o[k] = k < T ? k : -1;
+    return;
+  }
+  uint32_t prefix = 0u, mask = 0u;
+  int krem = K;   // selected positions still to place at or below the current prefix
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0u;
+    __syncthreads();
+    for (int p0 = 0; p0 < T; p0 += blockDim.x) {
+      const int p = p0 + tid;
+      const uint32_t key = p < T ? score_key(row[p]) : 0u;
+      const bool in = p < T && (key & mask) == prefix;
+      const uint32_t digit = in ? (key >> shift) & 255u : 256u;
+      const uint32_t same = __match_any_sync(0xffffffffu, digit);
+      if (in && lane == __ffs(same) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(same));
+    }
+    __syncthreads();
+    if (tid < 32) {
+      // lane l holds bins 255 - 8 l .. 248 - 8 l (largest first)
+      uint32_t cnt[8], sum = 0;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        cnt[e] = hist[255 - 8 * lane - e];
+        sum += cnt[e];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int o2 = 1; o2 < 32; o2 <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o2);
+        if (lane >= o2) incl += y;
+      }
+      const uint32_t before = incl - sum;   // keys in the bins above this lane's
+      if (before < (uint32_t)krem && (uint32_t)krem <= incl) {
+        uint32_t acc = before;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          if (acc + cnt[e] >= (uint32_t)krem) {
+            s_prefix = prefix | ((uint32_t)(255 - 8 * lane - e) << shift);
+            s_krem = krem - (int)acc;
+            break;
+          }
+          acc += cnt[e];
+        }
+      }
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    krem = s_krem;
+    mask |= 255u << shift;
+    __syncthreads();   // hist and the shared results are reused by the next pass
+  }
+  // prefix = the K-th largest key; krem of the keys equal to it are selected
+  const int run = (T + blockDim.x - 1) / blockDim.x;
+  const int p0 = tid * run, p1 = min(p0 + run, T);
+  int ngt = 0, neq = 0;
+  for (int p = p0; p < p1; ++p) {
+    const uint32_t key = score_key(row[p]);
+    ngt += key > prefix;
+    neq += key == prefix;
+  }
+  int tot;
+  int gt = block_exclusive_scan(ngt, scan_smem, &tot);
+  int eq = block_exclusive_scan(neq, scan_smem, &tot);
+  for (int p = p0; p < p1; ++p) {
+    const uint32_t key = score_key(row[p]);
+    if (key > prefix) {
+      o[gt + min(eq, krem)] = p;
+      ++gt;
+    } else if (key == prefix) {
+      if (eq < krem) o[gt + eq] = p;
+      ++eq;
+    }
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_read_ceiling(const void* buf, size_t bytes, uint32_t* sink, int sms, cudaStream_t s) {
@@ -428,6 +538,12 @@ cudaError_t launch_combine(const Workspace& ws, int B, int H, void* out, float* 
   // up to 32 sequences per head in flight; a CTA walks the rest
   return launch_pdl(combine_kernel, dim3(H, B < 32 ? B : 32), dim3(128), 0, s, ws, H, B,
                     static_cast<__nv_bfloat16*>(out), lse);
+}
+
+cudaError_t launch_topk_select(const float* scores, const int* end_pos, int B, int max_end_pos, int K,
+                               int* out, cudaStream_t s) {
+  return launch_pdl(topk_select_kernel, dim3(B), dim3(1024), 0, s, scores, max_end_pos, end_pos, max_end_pos,
+                    K, out);
 }
 
 }  // namespace mla

@@ -199,5 +199,8 @@ cudaError_t launch_project_out(const void* x, const void* wkv_b, int B, int H, v
                                uint32_t* status, cudaStream_t s);
 // streams `bytes` (a multiple of 16) of device memory, XOR-folding into *sink
 cudaError_t launch_read_ceiling(const void* buf, size_t bytes, uint32_t* sink, int sms, cudaStream_t s);
+// top-k position selection: scores [B][max_end_pos] fp32 -> out [B][K] int32
+cudaError_t launch_topk_select(const float* scores, const int* end_pos, int B, int max_end_pos, int K,
+                               int* out, cudaStream_t s);
 
 }  // namespace mla

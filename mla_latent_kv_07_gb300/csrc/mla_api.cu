@@ -233,6 +233,19 @@ mla_status mla_decode(const mla_cache* cache, const void* q_latent, const void* 
   return run_decode(a, ws, 0, static_cast<cudaStream_t>(stream));
 }
 
+mla_status mla_topk_select(const float* scores, const int32_t* end_pos, int32_t B, int32_t max_end_pos,
+                           int32_t K, int32_t* topk_idx, void* stream) {
+  g_last_error[0] = 0;
+  if (!scores || !end_pos || !topk_idx || !aligned4(scores) || !aligned4(end_pos) || !aligned4(topk_idx))
+    return MLA_ERR_INVALID_ARG;
+  if (B < 1 || max_end_pos < 1 || K < 1 || K > mla::kMaxTopK) return MLA_ERR_INVALID_ARG;
+  cudaError_t e = mla::launch_topk_select(scores, end_pos, B, max_end_pos, K, topk_idx,
+                                          static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "topk_select");
+  trace_launches(1);
+  return MLA_OK;
+}
+
 mla_status mla_selftest_decode_timeout(const mla_cache* cache, const void* q_latent, const void* q_pe,
                                        const int32_t* end_pos, int32_t max_end_pos, int32_t B, int32_t H,
                                        float softmax_scale, void* out, float* lse, void* workspace,

@@ -110,6 +110,17 @@ def test_sparse_rejects_bad_arguments(L):
                                f, None, None, None, f, 1 << 30, None) == 3
 
 
+def test_topk_select_rejects_bad_arguments(L):
+    f = ctypes.c_void_p(FAKE)
+    assert L.mla_topk_select(None, f, 2, 64, 8, f, None) == 1
+    assert L.mla_topk_select(f, f, 2, 64, 8, None, None) == 1
+    assert L.mla_topk_select(ctypes.c_void_p(FAKE + 2), f, 2, 64, 8, f, None) == 1   # misaligned
+    assert L.mla_topk_select(f, f, 0, 64, 8, f, None) == 1
+    assert L.mla_topk_select(f, f, 2, 0, 8, f, None) == 1
+    assert L.mla_topk_select(f, f, 2, 64, 0, f, None) == 1
+    assert L.mla_topk_select(f, f, 2, 64, 8193, f, None) == 1
+
+
 def test_workspace_size_rejects_bad_arguments(L):
     assert L.mla_workspace_size(0, 128, 64, 0) == 0
     assert L.mla_workspace_size(4, 24, 64, 0) == 0

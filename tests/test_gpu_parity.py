@@ -489,3 +489,56 @@ def test_limits_longest_list_most_tokens_most_rows():
     assert np.array_equal(dc1.kv.cpu().numpy(), oc1["kv"])
     assert np.array_equal(dc1.kv_scale.cpu().numpy().view(np.uint32), oc1["kv_scale"].view(np.uint32))
     assert np.array_equal(bits(dc1.pe.cpu()), oc1["pe"])
+
+
+# ---------------------------------------------------------- top-k select
+
+def _adversarial_scores(B, S, seed):
+    rng = np.random.default_rng(seed)
+    s = rng.standard_normal((B, S)).astype(np.float32)
+    s[0, 10:60] = 0.75                                      # a run of equal scores
+    s[1, ::5] = -0.0
+    s[1, 2::5] = 0.0
+    s[2, rng.integers(0, S, 20)] = np.inf
+    s[2, rng.integers(0, S, 20)] = -np.inf
+    s[3, rng.integers(0, S, 30)] = np.nan
+    s[3, :5] = np.float32(3.0e38)
+    return s
+
+
+@pytest.mark.parametrize("K", [1, 7, 64, 250, 299, 300, 500])
+def test_topk_select_bit_exact(K):
+    B, S = 5, 300
+    scores = _adversarial_scores(B, S, 161)
+    ends = np.array([300, 257, 0, 299, 40], np.int32)
+    got = mla.topk_select(torch.from_numpy(scores).cuda(), torch.from_numpy(ends).cuda(), K)
+    assert np.array_equal(got.cpu().numpy(), orc.topk_select(scores, ends, K))
+
+
+def test_topk_select_sparse_workload_shape():
+    # 16 sequences of 32768 scores, 2048 selected (ties included)
+    B, S, K = 16, 32768, 2048
+    rng = np.random.default_rng(162)
+    scores = rng.standard_normal((B, S)).astype(np.float32)
+    scores[:, ::97] = np.round(scores[:, ::97], 1)
+    ends = np.array([S] * 12 + [S - 1, 3000, 2048, 100], np.int32)
+    got = mla.topk_select(torch.from_numpy(scores).cuda(), torch.from_numpy(ends).cuda(), K)
+    assert np.array_equal(got.cpu().numpy(), orc.topk_select(scores, ends, K))
+
+
+def test_topk_select_feeds_the_sparse_decode():
+    # per-position scores -> selection -> gathered decode, on the device and
+    # in the oracle (each side selects its own lists from the same scores)
+    B, S, H, K = 3, 700, 128, 256
+    oc = oracle_cache(_rand_bf16((B, S, 512), 163), _rand_bf16((B, S, 64), 164), 1)
+    dc = device_cache(oc)
+    scores = np.random.default_rng(165).standard_normal((B, S)).astype(np.float32)
+    ends = np.array([700, 301, 120], np.int32)
+    ql, qp = _rand_bf16((B, H, 512), 166), _rand_bf16((B, H, 64), 167)
+    e_dev = torch.from_numpy(ends).cuda()
+    idx = mla.topk_select(torch.from_numpy(scores).cuda(), e_dev, K)
+    out, lse = mla.decode_sparse(dc, ql.cuda(), qp.cuda(), e_dev, S, 0.11, idx)
+    ref_idx = orc.topk_select(scores, ends, K)
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), ends, 0.11, topk=ref_idx)
+    check_close(f64(out).reshape(-1, 512), ref, "out")
+    check_close(f64(lse).reshape(-1), ref_lse, "lse")
