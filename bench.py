@@ -315,6 +315,44 @@ def run_warm(st, stream, steps: int = 200):
             "note": "one cache resident in L2 (warm); the headline is the cold, rotated number"}
 
 
+def run_select(st, stream, reps: int = 200):
+    """The top-k position selection timed on its own, at the sparse
+    workload's shape: seeded N(0,1) fp32 scores for every position of every
+    sequence, K of them selected per sequence; `reps` launches in a CUDA graph,
+    cycling through score buffers that together exceed twice the L2.
+    Algorithmic bytes: the scores read once and the lists written."""
+    w = st.w
+    pk, src = peaks()
+    one = w.B * w.S * 4
+    n = max(1, math.ceil(2 * st.l2_bytes / one))
+    scores = [inputs.randn_bf16((w.B, w.S), 1000 * w.index + 97 + k, st.device).float() for k in range(n)]
+    ends = st.ends
+    out = torch.empty((w.B, w.topk), dtype=torch.int32, device=st.device)
+    call = lambda k: mla.topk_select(scores[k % n], ends, w.topk, out=out, stream=stream)
+    with torch.cuda.stream(stream):
+        for k in range(3):
+            call(k)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for k in range(reps):
+            call(k)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t = e0.elapsed_time(e1) / 1e3 / reps
+    nbytes = sum(int(e) for e in st.ends_host) * 4 + w.B * w.topk * 4
+    return {"kernel": "topk_select_kernel", "us": round(t * 1e6, 3), "bytes": nbytes,
+            "gbs": round(nbytes / t / 1e9, 1), "frac": round(nbytes / t / 1e9 / pk["hbm_gbs"], 4),
+            "peak_source": f"of {src}",
+            "sample": f"{w.B} x {w.S} fp32 scores, top {w.topk} each; {n} rotating score buffers "
+                      f"({n * one / 1e6:.0f} MB), cold in L2"}
+
+
 def run_gemms(st, stream, reps: int = 200):
     """The query absorption and value projection timed on their own: `reps`
     launches of each captured in a CUDA graph (launches back to back), CUDA
@@ -443,6 +481,7 @@ def run_gpu(args, rank, world, local_rank):
 
     warm = run_warm(st, stream)
     gemms = run_gemms(st, stream) if w.absorb else None
+    select = run_select(st, stream) if w.topk else None
     e2e = run_e2e(st, K, W) if not args.no_e2e else None
     cpu = run_cpu_baseline(w) if (rank == 0 and world == 1 and not args.no_cpu) else None
     if rank != 0:
@@ -469,6 +508,7 @@ def run_gpu(args, rank, world, local_rank):
         "roofline": roofline,
         "warm": warm,
         "gemms": gemms,
+        "select": select,
         "read_ceiling": {"gbs": round(ceil_gbs, 1), "kernel": "read_ceiling_kernel",
                          "bytes_per_pass": int(ceil_bytes),
                          "sample": "the step's rotated cache tensors, streamed with 16-byte loads"},

@@ -7,13 +7,21 @@
 //            zeros into -inf, so repeats act once and order does not matter)
 //   schedule split every sequence's positions into units of about equal size
 //   combine  log-sum-exp merge of the per-unit partial outputs
+//   select   top-k positions per sequence from per-position scores (the
+//            index lists the sparse decode takes)
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include <cuda.h>
+
 #include "common.cuh"
+#include "tc_ptx.cuh"
 
 namespace mla {
 namespace {
+
+using ptx::cluster_sync;
+using ptx::mapa;
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -396,54 +404,109 @@ __global__ void __launch_bounds__(512) read_ceiling_kernel(const uint4* __restri
 
 
 // ----------------------------------------------------------- top-k select
-// One CTA per sequence selects, among positions 0 .. end_pos-1 of its score
-// row, the K with the largest score (equal scores: the lower position; -0
-// equals +0; NaN ranks lowest) and writes them in increasing order, then -1.
-// Scores map to order-preserving 32-bit keys; a radix select over the key's
-// four bytes (most significant first, a shared 256-bin histogram per pass,
-// increments aggregated per warp) finds the K-th largest key t and how many
-// keys equal to t belong to the selection; a last pass over contiguous runs
-// of positions (one per thread, offsets from two block scans) writes the
-// selected positions in order.
+// A cluster of kTopkCtas CTAs per sequence selects, among positions
+// 0 .. end_pos-1 of its score row, the K with the largest score (equal
+// scores: the lower position; -0 equals +0; NaN ranks lowest) and writes them
+// in increasing order, then -1.  Scores map to order-preserving 32-bit keys;
+// CTA r of the cluster holds the keys of the r-th of kTopkCtas equal runs of
+// positions in shared memory (read once, 16-byte loads when aligned).  A
+// radix select over the key's four bytes (most significant first) finds the
+// K-th largest key t and how many keys equal to t belong to the selection:
+// per pass every CTA builds a 256-bin histogram of its run, and after one
+// cluster barrier each CTA sums the kTopkCtas histograms through distributed
+// shared memory and takes the same decision (histograms alternate between
+// two buffers by pass, so none is cleared while a peer still reads it).  A
+// last pass counts, per CTA and per warp, the keys above and equal to t,
+// turns the counts into offsets (the peers' through distributed shared
+// memory) and writes the selected positions in order.
+constexpr int kTopkCtas = 8;
+constexpr int kTopkThreads = 256;
+constexpr int kTopkSmemKeys = 55296;   // runs up to this many positions are staged (216 KB)
+
 __device__ __forceinline__ uint32_t score_key(float x) {
   if (x != x) return 0u;                             // NaN: below every number
   const uint32_t u = x == 0.f ? 0u : __float_as_uint(x);   // -0 -> +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__global__ void __launch_bounds__(1024) topk_select_kernel(const float* __restrict__ scores, int ld,
-                                                          const int* __restrict__ end_pos,
-                                                          int max_end_pos, int K,
-                                                          int* __restrict__ out) {
-  __shared__ uint32_t hist[256];
-  __shared__ int scan_smem[33];
+__device__ __forceinline__ uint32_t ld_cluster_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+template <bool kSmem>
+__global__ void __launch_bounds__(kTopkThreads, 1) topk_select_kernel(const float* __restrict__ scores,
+                                                                     int ld, const int* __restrict__ end_pos,
+                                                                     int max_end_pos, int K,
+                                                                     int* __restrict__ out) {
+  extern __shared__ uint32_t keys_smem[];   // kSmem: this CTA's run of keys
+  __shared__ uint32_t hist[2][256];
+  __shared__ uint32_t ghist[256];
+  __shared__ int wgt[kTopkThreads / 32], weq[kTopkThreads / 32];
+  __shared__ int cta_cnt[2];   // this CTA's keys above / equal to t (read by the peers)
   __shared__ uint32_t s_prefix;
   __shared__ int s_krem;
   pdl_wait();
   pdl_trigger();
-  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+  uint32_t rank;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
+  const int b = blockIdx.x / kTopkCtas, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = kTopkThreads / 32;
   int T = end_pos[b];
   T = T < 0 ? 0 : (T > max_end_pos ? max_end_pos : T);
   const float* row = scores + (size_t)b * ld;
   int* o = out + (size_t)b * K;
-  if (T <= K) {   // every valid position is selected
-    for (int k = tid; k < K; k += blockDim.x) o[k] = k < T ? k : -1;
+  if (T <= K) {   // every valid position is selected (the same test in every CTA of the cluster)
+    if (rank == 0)
+      for (int k = tid; k < K; k += kTopkThreads) o[k] = k < T ? k : -1;
     return;
   }
+  // this CTA's run [c0, c1): a multiple of 4 positions long except the last
+  const int per = ((T + kTopkCtas - 1) / kTopkCtas + 3) & ~3;
+  const int c0 = min((int)rank * per, T), c1 = min(c0 + per, T), n = c1 - c0;
+  if (kSmem) {
+    const float* src = row + c0;
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+      const int n4 = n >> 2;
+      const float4* src4 = reinterpret_cast<const float4*>(src);
+      for (int q0 = tid; q0 < n4; q0 += 8 * kTopkThreads) {
+        float4 v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          v[k] = q0 + k * kTopkThreads < n4 ? src4[q0 + k * kTopkThreads] : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          if (q0 + k * kTopkThreads < n4)
+            reinterpret_cast<uint4*>(keys_smem)[q0 + k * kTopkThreads] =
+                make_uint4(score_key(v[k].x), score_key(v[k].y), score_key(v[k].z), score_key(v[k].w));
+      }
+      for (int i = 4 * n4 + tid; i < n; i += kTopkThreads) keys_smem[i] = score_key(src[i]);
+    } else {
+      for (int i = tid; i < n; i += kTopkThreads) keys_smem[i] = score_key(src[i]);
+    }
+  }
+  // key of the run's i-th position
+  auto key_at = [&](int i) -> uint32_t { return kSmem ? keys_smem[i] : score_key(row[c0 + i]); };
+
   uint32_t prefix = 0u, mask = 0u;
   int krem = K;   // selected positions still to place at or below the current prefix
 #pragma unroll 1
   for (int pass = 0; pass < 4; ++pass) {
     const int shift = 24 - 8 * pass;
-    for (int i = tid; i < 256; i += blockDim.x) hist[i] = 0u;
+    uint32_t* h = hist[pass & 1];
+    for (int i = tid; i < 256; i += kTopkThreads) h[i] = 0u;
     __syncthreads();
-    for (int p0 = 0; p0 < T; p0 += blockDim.x) {
-      const int p = p0 + tid;
-      const uint32_t key = p < T ? score_key(row[p]) : 0u;
-      const bool in = p < T && (key & mask) == prefix;
-      const uint32_t digit = in ? (key >> shift) & 255u : 256u;
-      const uint32_t same = __match_any_sync(0xffffffffu, digit);
-      if (in && lane == __ffs(same) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(same));
+    for (int i = tid; i < n; i += kTopkThreads) {
+      const uint32_t key = key_at(i);
+      if ((key & mask) == prefix) atomicAdd(&h[(key >> shift) & 255u], 1u);
+    }
+    cluster_sync();   // every CTA's histogram of this pass is complete
+    for (int i = tid; i < 256; i += kTopkThreads) {
+      uint32_t sum = 0;
+#pragma unroll
+      for (int r = 0; r < kTopkCtas; ++r) sum += ld_cluster_u32(mapa(&h[i], r));
+      ghist[i] = sum;
     }
     __syncthreads();
     if (tid < 32) {
@@ -451,7 +514,7 @@ __global__ void __launch_bounds__(1024) topk_select_kernel(const float* __restri
       uint32_t cnt[8], sum = 0;
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        cnt[e] = hist[255 - 8 * lane - e];
+        cnt[e] = ghist[255 - 8 * lane - e];
         sum += cnt[e];
       }
       uint32_t incl = sum;
@@ -478,32 +541,66 @@ __global__ void __launch_bounds__(1024) topk_select_kernel(const float* __restri
     prefix = s_prefix;
     krem = s_krem;
     mask |= 255u << shift;
-    __syncthreads();   // hist and the shared results are reused by the next pass
   }
-  // prefix = the K-th largest key; krem of the keys equal to it are selected
-  const int run = (T + blockDim.x - 1) / blockDim.x;
-  const int p0 = tid * run, p1 = min(p0 + run, T);
+
+  // prefix = the K-th largest key; krem of the keys equal to it are selected.
+  // Warp w owns run positions [w R, w R + R), R a multiple of 32.
+  const int R = ((n + kWarps - 1) / kWarps + 31) & ~31;
+  const int q0 = warp * R, q1 = min(q0 + R, n);
   int ngt = 0, neq = 0;
-  for (int p = p0; p < p1; ++p) {
-    const uint32_t key = score_key(row[p]);
+  for (int i = q0 + lane; i < q1; i += 32) {
+    const uint32_t key = key_at(i);
     ngt += key > prefix;
     neq += key == prefix;
   }
-  int tot;
-  int gt = block_exclusive_scan(ngt, scan_smem, &tot);
-  int eq = block_exclusive_scan(neq, scan_smem, &tot);
-  for (int p = p0; p < p1; ++p) {
-    const uint32_t key = score_key(row[p]);
-    if (key > prefix) {
-      o[gt + min(eq, krem)] = p;
-      ++gt;
-    } else if (key == prefix) {
-      if (eq < krem) o[gt + eq] = p;
-      ++eq;
+  ngt = __reduce_add_sync(0xffffffffu, ngt);
+  neq = __reduce_add_sync(0xffffffffu, neq);
+  if (lane == 0) {
+    wgt[warp] = ngt;
+    weq[warp] = neq;
+  }
+  __syncthreads();
+  if (warp == 0) {   // exclusive scans of the warps' counts; this CTA's totals
+    const int g = lane < kWarps ? wgt[lane] : 0, e = lane < kWarps ? weq[lane] : 0;
+    int gi = g, ei = e;
+#pragma unroll
+    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+      const int yg = __shfl_up_sync(0xffffffffu, gi, o2), ye = __shfl_up_sync(0xffffffffu, ei, o2);
+      if (lane >= o2) {
+        gi += yg;
+        ei += ye;
+      }
+    }
+    if (lane < kWarps) {
+      wgt[lane] = gi - g;
+      weq[lane] = ei - e;
+    }
+    if (lane == kWarps - 1) {
+      cta_cnt[0] = gi;
+      cta_cnt[1] = ei;
     }
   }
+  cluster_sync();   // every CTA's totals are in place
+  int gbase = 0, ebase = 0;   // keys above / equal to t in the runs of the lower ranks
+  for (int r = 0; r < (int)rank; ++r) {
+    gbase += (int)ld_cluster_u32(mapa(&cta_cnt[0], r));
+    ebase += (int)ld_cluster_u32(mapa(&cta_cnt[1], r));
+  }
+  int gt = gbase + wgt[warp], eq = ebase + weq[warp];   // before this warp's next step
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int i0 = q0; i0 < q1; i0 += 32) {
+    const int i = i0 + lane;
+    const uint32_t key = i < q1 ? key_at(i) : 0u;
+    const bool is_gt = i < q1 && key > prefix, is_eq = i < q1 && key == prefix;
+    const uint32_t bg = __ballot_sync(0xffffffffu, is_gt), be = __ballot_sync(0xffffffffu, is_eq);
+    const int g_before = gt + __popc(bg & lt), e_before = eq + __popc(be & lt);
+    if (is_gt) o[g_before + min(e_before, krem)] = c0 + i;
+    if (is_eq && e_before < krem) o[g_before + e_before] = c0 + i;
+    gt += __popc(bg);
+    eq += __popc(be);
+  }
+  cluster_sync();   // no peer reads this CTA's counts any more
 }
-
 }  // namespace
 
 cudaError_t launch_read_ceiling(const void* buf, size_t bytes, uint32_t* sink, int sms, cudaStream_t s) {
@@ -542,8 +639,28 @@ cudaError_t launch_combine(const Workspace& ws, int B, int H, void* out, float* 
 
 cudaError_t launch_topk_select(const float* scores, const int* end_pos, int B, int max_end_pos, int K,
                                int* out, cudaStream_t s) {
-  return launch_pdl(topk_select_kernel, dim3(B), dim3(1024), 0, s, scores, max_end_pos, end_pos, max_end_pos,
-                    K, out);
+  const int per = ((max_end_pos + kTopkCtas - 1) / kTopkCtas + 3) & ~3;   // longest run of a CTA
+  const bool staged = per <= kTopkSmemKeys;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  cfg.gridDim = dim3(B * kTopkCtas);
+  cfg.blockDim = dim3(kTopkThreads);
+  cfg.dynamicSmemBytes = staged ? (size_t)per * 4 : 0;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kTopkCtas;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (staged) {
+    cudaError_t e = ensure_smem<topk_select_kernel<true>>((size_t)kTopkSmemKeys * 4);
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, topk_select_kernel<true>, scores, max_end_pos, end_pos, max_end_pos, K, out);
+  }
+  return cudaLaunchKernelEx(&cfg, topk_select_kernel<false>, scores, max_end_pos, end_pos, max_end_pos, K, out);
 }
 
 }  // namespace mla
