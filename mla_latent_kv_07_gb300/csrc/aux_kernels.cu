@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(512) read_ceiling_kernel(const uint4* __restri
 // turns the counts into offsets (the peers' through distributed shared
 // memory) and writes the selected positions in order.
 constexpr int kTopkCtas = 8;
-constexpr int kTopkThreads = 256;
+constexpr int kTopkThreads = 512;
 constexpr int kTopkSmemKeys = 55296;   // runs up to this many positions are staged (216 KB)
 
 __device__ __forceinline__ uint32_t score_key(float x) {
