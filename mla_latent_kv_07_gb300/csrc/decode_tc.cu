@@ -121,7 +121,7 @@ struct Cfg {
   // 32 its QK reads); gathers land whole 128-byte rows
   static constexpr int kRawPe = (kFmt == 1 && !kSparse) ? kPeHalf * 2 : 128;
   static constexpr int kRaw = kConv ? kN * kRawRow + kScBytes + kN * kRawPe : 0;
-  static constexpr int kRawSlots = kConv ? 2 : 0;
+  static constexpr int kRawSlots = kConv ? (kFmt == 1 && !kSparse ? 3 : 2) : 0;
   static constexpr int kRawOff = kStages * kStage;
   static constexpr int kPOff = kRawOff + kRawSlots * kRaw;
   static constexpr int kXOff = kPOff + kPBufs * kPBytes;
@@ -197,7 +197,7 @@ struct Bars {
   uint64_t full[4];    // tile landed: stage (dense bf16) or raw slot
   uint64_t deq[4];     // operand stage converted
   uint64_t empty[4];   // PV done: operand stage free
-  uint64_t rfree[2];   // raw slot read by the converter
+  uint64_t rfree[3];   // raw slot read by the converter
   uint64_t sfull[2], sfree[2], pfull[3], pfree[3], xfull[2], xempty[2];
   uint64_t drain;   // final commit of the MMA issuer
   uint64_t qbar;    // query rows staged in shared memory
@@ -338,7 +338,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       bar_init(&bars->deq[j], kConvWarps);
       bar_init(&bars->empty[j], 1);
     }
-    for (int r = 0; r < 2; ++r) bar_init(&bars->rfree[r], kConvWarps);
+    for (int r = 0; r < C::kRawSlots; ++r) bar_init(&bars->rfree[r], kConvWarps);
     for (int b = 0; b < C::kPBufs; ++b) {
       bar_init(&bars->pfull[b], 8);
       bar_init(&bars->pfree[b], 1);
