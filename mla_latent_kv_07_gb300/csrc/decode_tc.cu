@@ -17,7 +17,8 @@
 //     tensor memory, K half from shared memory) into a partial S; the two
 //     partials are exchanged through distributed shared memory as 24-bit
 //     codes (each fp32 partial rounded to its top 24 bits, by both CTAs
-//     alike) and summed.  fp32 addition commutes, so both CTAs hold
+//     alike; asynchronous remote stores, counted on the receiver's barrier)
+//     and summed.  fp32 addition commutes, so both CTAs hold
 //     bit-identical S and take the same softmax decisions.
 //   * PV: each CTA multiplies P (shared memory) by its latent half V (the same
 //     shared-memory tile, read as an MN-major operand) into its own O half.
@@ -346,7 +347,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     for (int b = 0; b < 2; ++b) {
       bar_init(&bars->sfull[b], 1);
       bar_init(&bars->sfree[b], 12);   // softmax (8) and exchange (4) warps read S
-      bar_init(&bars->xfull[b], 4);
+      bar_init(&bars->xfull[b], 1);    // one arrival (with the tile's bytes) from the peer
       bar_init(&bars->xempty[b], 8);   // the peer's softmax warps
     }
     bar_init(&bars->drain, 1);
@@ -578,18 +579,17 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       if (lane == 0) bar_arrive(&bars->sfree[b]);
       const int xb = xsel(i);
       if (!wt.wait(&bars->xempty[xb], xpar(i))) break;   // phase 0: the peer's query staging is done
-      const uint32_t xd = mapa(xbuf(xb) + 4 * h, peer);
+      const uint32_t xd = mapa(xbuf(xb) + 4 * h, peer), xf = mapa(&bars->xfull[xb], peer);
       uint32_t w[C::kXRows * 4];
 #pragma unroll
       for (int g = 0; g < kN / 4; ++g)
         pack24(r[4 * g], r[4 * g + 1], r[4 * g + 2], r[4 * g + 3], w[3 * g], w[3 * g + 1], w[3 * g + 2]);
+      // the peer's phase completes on one arrival carrying the tile's bytes
+      // and on those bytes landing, in either order
+      if (h == 0) bar_arrive_expect_tx_remote(xf, C::kXBytes);
 #pragma unroll
       for (int q = 0; q < C::kXRows; ++q)
-        asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(xd + 16 * 128 * q),
-                     "r"(w[4 * q]), "r"(w[4 * q + 1]), "r"(w[4 * q + 2]), "r"(w[4 * q + 3])
-                     : "memory");
-      __syncwarp();
-      if (lane == 0) bar_arrive_remote(mapa(&bars->xfull[xb], peer));
+        st_async_v4(xd + 16 * 128 * q, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3], xf);
     }
   } else if ((warp >= 4 && warp < 8) || (warp >= C::kHiWarp && warp < C::kHiWarp + 4)) {
     // ------------------------------------------------------------ softmax
@@ -848,7 +848,22 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   // ---------------------------------------------------------------- teardown
   tc_before();
   __syncthreads();
-  cluster_sync();  // no remote access into this CTA's shared memory remains
+  cluster_sync();  // neither CTA issues remote stores any more
+  if (bars->abort) {
+    // The partial scores arrive by asynchronous remote stores, which the
+    // cluster barrier does not wait for.  On the normal path every one has
+    // landed (this CTA waited for each tile's); after an abort some the peer
+    // issued may still be in flight into this CTA's shared memory, so it
+    // stays alive for a bound far above their delivery time (microseconds).
+    if (threadIdx.x == 0) {
+      uint64_t t0, t;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+      do {
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+      } while (t - t0 < 100000u);
+    }
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));

@@ -30,6 +30,22 @@ __device__ __forceinline__ void bar_arrive_remote_relaxed(uint32_t remote_addr) 
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_addr)
                : "memory");
 }
+// arrive on a peer CTA's barrier, adding `bytes` to the transaction count its
+// phase waits for
+__device__ __forceinline__ void bar_arrive_expect_tx_remote(uint32_t remote_addr, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(remote_addr),
+               "r"(bytes)
+               : "memory");
+}
+// 16 bytes into a peer CTA's shared memory, counted on the peer's barrier when
+// they land (no acknowledgement travels back to this thread)
+__device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   remote_addr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
+               : "memory");
+}
 __device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa(b)), "r"(bytes)
                : "memory");
