@@ -28,9 +28,11 @@
 // Tensor memory (512 columns): O half [0,256) fp32; Q half [256,400) bf16 (2
 // per column); S double buffer [400,448) and [448,496) fp32.
 //
-// Warp roles (512 threads; 640 when a converter is needed):
+// Warp roles (512 threads; 672 with a converter, 640 for gathers):
 //   warp 0  producer: TMA tiles (dense) or four-row TMA gathers (gather)
-//   warp 1  MMA issuer (one thread) and tensor-memory owner
+//   warp 1  MMA issuer (one thread; of QK only in the dense variants) and
+//           tensor-memory owner
+//   dense variants: PV issuer (one thread), warp 2 (bf16) or warp 20 (FP8)
 //   warps 4-7 and 12-15 (16-19 with a converter)  softmax: two threads per
 //              head h <-> TMEM lane h, each half of the tile's positions;
 //              online softmax (lazy rescale), P, epilogue
@@ -100,7 +102,14 @@ struct Cfg {
   // of a tile, no more -- the pipe runs its queue in order, so each queued QK
   // delays the PV behind it (measured: 2 starves the pipe, 3 is best).
   static constexpr int kQkAhead = 3;
-  static constexpr int kThreads = 32 * (kHiWarp + 4);
+  // Dense variants issue PV from a thread of its own (warp 2, idle without a
+  // converter; with one, a warp of its own after the softmax's second half),
+  // so a PV whose P is ready never waits behind the issue of a QK (which
+  // blocks on the tensor pipe's queue for about as long as it runs).  The
+  // gather variants keep one issuer: the extra warp costs them registers.
+  static constexpr bool kSplitIssue = !kSparse;
+  static constexpr int kPvWarp = kConv ? kHiWarp + 4 : 2;
+  static constexpr int kThreads = 32 * (kHiWarp + 4 + (kConv && kSplitIssue ? 1 : 0));
   static constexpr int kBlkBytes = kN * 128;       // one 64-column swizzled block of a tile
   static constexpr int kOplBytes = 4 * kBlkBytes;  // latent half operand
   static constexpr int kOpeBytes = kBlkBytes;      // rotary operand (full 64 columns)
@@ -200,7 +209,9 @@ struct Bars {
   uint64_t empty[4];   // PV done: operand stage free
   uint64_t rfree[3];   // raw slot read by the converter
   uint64_t sfull[2], sfree[2], pfull[3], pfree[3], xfull[2], xempty[2];
-  uint64_t drain;   // final commit of the MMA issuer
+  uint64_t drain;   // final commit of the MMA issuer (of QK, when PV has its own)
+  uint64_t drain_pv;  // final commit of the PV issuer
+  volatile int pv_issued;   // PV issuer: tiles whose PV is issued (paces QK)
   uint64_t qbar;    // query rows staged in shared memory
   uint64_t qready;  // query half in tensor memory
   uint32_t tmem;
@@ -351,6 +362,8 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       bar_init(&bars->xempty[b], 8);   // the peer's softmax warps
     }
     bar_init(&bars->drain, 1);
+    bar_init(&bars->drain_pv, 1);
+    bars->pv_issued = 0;
     bar_init(&bars->qbar, 1);
     bar_init(&bars->qready, 4);
     bars->abort = 0;
@@ -417,7 +430,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   }
   // the second-half softmax warps count towards that phase too (it completes
   // only with the first half's arrivals, after the staged rows were read)
-  if (live && warp >= C::kHiWarp && lane == 0) {
+  if (live && warp >= C::kHiWarp && warp < C::kHiWarp + 4 && lane == 0) {
     bar_arrive_remote(mapa(&bars->xempty[0], peer));
     bar_arrive_remote(mapa(&bars->xempty[1], peer));
   }
@@ -485,6 +498,72 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     if (lane == 0 && bars->abort) {
       for (int i = issued > kSlots ? issued - kSlots : 0; i < issued; ++i)
         if (!(unit_id == 0 && i == p.withhold_tile)) wt.drain(&bars->full[i % kSlots], (i / kSlots) & 1);
+    }
+  } else if (C::kSplitIssue && warp == C::kPvWarp) {
+    // ------------------------------------------------------------ PV issuer
+    if (lane == 0) {
+      constexpr uint32_t id_pv = idesc(128, kHalf, true);
+      const uint64_t d_v0 = sdesc(sa(opl(0)), kBlkBytes, 1024);
+      const uint64_t d_p0 = sdesc(sa(pbuf(0)), 16, 1024);
+      const uint32_t t_o = tmem + kTmemO;
+      for (int i = 0; i < ntiles; ++i) {
+        const int j = i % C::kStages, b = psel(i);
+        if (!wt.wait(&bars->pfull[b], ppar(i))) break;
+        tc_after();
+        const uint64_t pd = sdesc_at(d_p0, b * C::kPBytes), vd = sdesc_at(d_v0, j * C::kStage);
+        if (i == 0)
+          mma_ss_c<false>(t_o, pd, vd, id_pv);
+        else
+          mma_ss_c<true>(t_o, pd, vd, id_pv);
+#pragma unroll
+        for (int kk = 1; kk < kN / 16; ++kk)
+          mma_ss_c<true>(t_o, sdesc_at(pd, (kk >> 2) * kSwBlk + (kk & 3) * 32), sdesc_at(vd, 2048 * kk), id_pv);
+        mma_commit(&bars->pfree[b]);
+        mma_commit(&bars->empty[j]);
+        bars->pv_issued = i + 1;
+      }
+      mma_commit(&bars->drain_pv);
+      wt.drain(&bars->drain_pv, 0);
+    }
+  } else if (C::kSplitIssue && warp == 1) {
+    // ------------------------------------------------------------ QK issuer
+    if (lane == 0) {
+      constexpr uint32_t id_qk = idesc(128, kN, false);
+      const uint64_t d_k0 = sdesc(sa(opl(0)), 16, 1024);
+      const uint32_t t_q = tmem + kTmemQ;
+      if (live && wt.wait(&bars->qready, 0)) tc_after();
+      for (int k = 0; k < ntiles && !bars->abort; ++k) {
+        const int j = k % C::kStages, b = ssel(k);
+        bool paced = false;
+        for (long it = 0; it < wt.lim && !bars->abort; ++it)
+          if (bars->pv_issued > k - C::kQkAhead) {
+            paced = true;
+            break;
+          }
+        if (!paced) {
+          if (!bars->abort) {
+            bars->abort = 1;
+            atomicOr(p.ws.status, kDevTimeout);
+          }
+          break;
+        }
+        if (!wt.wait(C::kConv ? &bars->deq[j] : &bars->full[j], (k / C::kStages) & 1)) break;
+        if (!wt.wait(&bars->sfree[b], spar(k) ^ 1)) break;
+        tc_after();
+        const uint32_t sd = tmem + kTmemS + b * kN;
+        const uint64_t kd = sdesc_at(d_k0, j * C::kStage);
+        const uint64_t ped = sdesc_at(kd, kOplBytes + rank * (kPeHalf * 2));
+        mma_ts_c<false>(sd, t_q, kd, id_qk);
+#pragma unroll
+        for (int kk = 1; kk < kHalf / 16; ++kk)
+          mma_ts_c<true>(sd, t_q + 8 * kk, sdesc_at(kd, (kk >> 2) * kBlkBytes + (kk & 3) * 32), id_qk);
+#pragma unroll
+        for (int kk = 0; kk < kPeHalf / 16; ++kk)
+          mma_ts_c<true>(sd, t_q + kHalf / 2 + 8 * kk, sdesc_at(ped, 32 * kk), id_qk);
+        mma_commit(&bars->sfull[b]);
+      }
+      mma_commit(&bars->drain);
+      wt.drain(&bars->drain, 0);
     }
   } else if (warp == 1) {
     // -------------------------------------------------------- MMA issuer
