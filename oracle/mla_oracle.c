@@ -23,6 +23,11 @@
  *     all-zero codes.
  *   - The dequantised latent is bf16(fp32(e4m3_value * scale)), which is what
  *     the cache-write excerpt stores into the bf16 cache.
+ *   - The cache-write excerpt passes a scale format to act_quant without
+ *     defining it.  The power-of-two ("ue8m0", exponent-only) format taken
+ *     here: scale = the smallest power of two >= fp32(amax / 448), so every
+ *     x / scale is exact and the block still fits the e4m3 range; the codes
+ *     follow as above.
  *   - Top-k entries that are negative or >= end_pos are skipped; duplicates
  *     act once (the mask is built by a scatter of zeros, which is idempotent);
  *     one index list per sequence is shared by all heads.
@@ -114,8 +119,18 @@ uint8_t orc_e4m3_encode(float y) {
 /* Cache-write step: FP8 block quantisation and its round trip [KVC]   */
 /* ------------------------------------------------------------------ */
 
-/* One latent row (512 bf16) -> 512 codes + 4 fp32 scales. */
-static void quantize_row(const uint16_t* x, uint8_t* q, float* scales) {
+/* Smallest power of two >= s, for a finite s > 0 (fp32 subnormals included):
+ * frexp writes s = m * 2^e with m in [0.5, 1); s is itself a power of two
+ * exactly when m == 0.5. */
+static float pow2_at_least(float s) {
+  int e;
+  double m = frexp((double)s, &e);
+  return (float)(m == 0.5 ? (double)s : ldexp(1.0, e));
+}
+
+/* One latent row (512 bf16) -> 512 codes + 4 fp32 scales; pow2 != 0 rounds
+ * each scale up to a power of two. */
+static void quantize_row(const uint16_t* x, uint8_t* q, float* scales, int pow2) {
   for (int j = 0; j < ORC_NBLK; ++j) {
     const uint16_t* xb = x + j * ORC_BLK;
     float amax = 0.0f;
@@ -124,6 +139,7 @@ static void quantize_row(const uint16_t* x, uint8_t* q, float* scales) {
       if (v > amax) amax = v;
     }
     float scale = amax / 448.0f;                 /* fp32 division */
+    if (pow2 && amax > 0.0f) scale = pow2_at_least(scale);
     scales[j] = scale;
     for (int i = 0; i < ORC_BLK; ++i) {
       if (amax == 0.0f) { q[j * ORC_BLK + i] = 0; continue; }
@@ -140,10 +156,10 @@ static uint16_t dequant_elem(uint8_t code, float scale) {
   return f32_to_bf16(p);
 }
 
-void orc_quantize_rows(const uint16_t* x, int64_t nrows, uint8_t* q, float* scales) {
+void orc_quantize_rows(const uint16_t* x, int64_t nrows, uint8_t* q, float* scales, int pow2) {
 #pragma omp parallel for schedule(static)
   for (int64_t r = 0; r < nrows; ++r)
-    quantize_row(x + r * ORC_DC, q + r * ORC_DC, scales + r * ORC_NBLK);
+    quantize_row(x + r * ORC_DC, q + r * ORC_DC, scales + r * ORC_NBLK, pow2);
 }
 
 void orc_dequant_rows(const uint8_t* q, const float* scales, int64_t nrows, uint16_t* out) {
@@ -201,9 +217,10 @@ void orc_sparse_gather_lists(const int32_t* topk, int B, int K, const int32_t* e
 /* Absorbed decode [KVC MQA-decode excerpt; ABS sections 3-4]           */
 /* ------------------------------------------------------------------ */
 
-/* Cache view.  fmt 0: kv is bf16 bits [Bmax, S, 512]; fmt 1: kv is e4m3
- * codes [Bmax, S, 512] with kv_scale fp32 [Bmax, S, 4].  pe is bf16 bits
- * [Bmax, S, 64] in both formats. */
+/* Cache view.  fmt 0: kv is bf16 bits [Bmax, S, 512]; fmt 1 and 2: kv is
+ * e4m3 codes [Bmax, S, 512] with kv_scale fp32 [Bmax, S, 4] (fmt 2's scales
+ * are powers of two; reading them is the same).  pe is bf16 bits
+ * [Bmax, S, 64] in every format. */
 typedef struct {
   int fmt;
   int64_t S;

@@ -56,7 +56,7 @@ def _load():
             lib.orc_e4m3_encode_array.argtypes = [P, I64, P]
             lib.orc_e4m3_value_array.argtypes = [P, I64, P]
             lib.orc_f32_to_bf16_array.argtypes = [P, I64, P]
-            lib.orc_quantize_rows.argtypes = [P, I64, P, P]
+            lib.orc_quantize_rows.argtypes = [P, I64, P, P, I32]
             lib.orc_dequant_rows.argtypes = [P, P, I64, P]
             lib.orc_sparse_gather_lists.argtypes = [P, I32, I32, P, P, P]
             lib.orc_decode_absorbed.argtypes = [I32, I64, P, P, P, P, P, I32, P, P, I32, D,
@@ -113,14 +113,19 @@ def bf16_bits_to_f64(bits) -> np.ndarray:
 
 # ------------------------------------------------------ cache-write step
 
-def quantize_rows(x_bits) -> tuple[np.ndarray, np.ndarray]:
-    """Latent rows [..., 512] (bf16 bits) -> (codes [..., 512] u8, scales [..., 4] f32)."""
+def quantize_rows(x_bits, pow2: bool = False) -> tuple[np.ndarray, np.ndarray]:
+    """Latent rows [..., 512] (bf16 bits) -> (codes [..., 512] u8, scales [..., 4] f32).
+
+    ``pow2`` selects the power-of-two scale format: each block's scale is the
+    smallest power of two >= fp32(amax / 448) (the cache-write excerpt of
+    "DeepSeek-V3.2-Exp . KV cache" passes a scale format to act_quant without
+    defining it; this is the exponent-only reading)."""
     x = _c(x_bits, np.uint16)
     assert x.shape[-1] == DC
     n = x.size // DC
     q = np.empty(x.shape, np.uint8)
     s = np.empty(x.shape[:-1] + (NBLK,), np.float32)
-    _load().orc_quantize_rows(_p(x), n, _p(q), _p(s))
+    _load().orc_quantize_rows(_p(x), n, _p(q), _p(s), 1 if pow2 else 0)
     return q, s
 
 
@@ -138,8 +143,9 @@ def dequant_rows(q, scales) -> np.ndarray:
 def cache_append(cache: dict, kv_new_bits, pe_new_bits, start_pos) -> None:
     """Write row start_pos[b] of every sequence b < B, in place.
 
-    ``cache`` holds numpy arrays: 'fmt' (0 bf16, 1 fp8), 'kv', 'pe' and, for
-    fmt 1, 'kv_scale'.  bf16 rows are copied; FP8 rows are block-quantised.
+    ``cache`` holds numpy arrays: 'fmt' (0 bf16, 1 fp8, 2 fp8 with
+    power-of-two scales), 'kv', 'pe' and, for fmt 1 and 2, 'kv_scale'.  bf16
+    rows are copied; FP8 rows are block-quantised.
     A start_pos outside [0, max_seq_len) raises (the library refuses it too).
     """
     kv_new = _c(kv_new_bits, np.uint16).reshape(-1, DC)
@@ -151,7 +157,7 @@ def cache_append(cache: dict, kv_new_bits, pe_new_bits, start_pos) -> None:
         if cache["fmt"] == 0:
             cache["kv"][b, t] = kv_new[b]
         else:
-            q, s = quantize_rows(kv_new[b:b + 1])
+            q, s = quantize_rows(kv_new[b:b + 1], pow2=cache["fmt"] == 2)
             cache["kv"][b, t] = q[0]
             cache["kv_scale"][b, t] = s[0]
         cache["pe"][b, t] = pe_new[b]
@@ -223,7 +229,7 @@ def decode_absorbed(cache: dict, q_latent, q_pe, end_pos, softmax_scale: float,
     pe = _c(cache["pe"], np.uint16)
     S = kv.shape[1]
     scale = None
-    if cache["fmt"] == 1:
+    if cache["fmt"] in (1, 2):
         scale = _c(cache["kv_scale"], np.float32)
     ep = _c(end_pos, np.int32)
     K = 0
@@ -312,7 +318,7 @@ def decode_naive(cache: dict, wkv_b, q_nope, q_pe, end_pos, softmax_scale: float
     B, H, _ = qn.shape
     kv = np.ascontiguousarray(cache["kv"])
     pe = _c(cache["pe"], np.uint16)
-    scale = _c(cache["kv_scale"], np.float32) if cache["fmt"] == 1 else None
+    scale = _c(cache["kv_scale"], np.float32) if cache["fmt"] in (1, 2) else None
     ep = _c(end_pos, np.int32)
     o = np.empty((B, H, 128), np.float64)
     lse = np.empty((B, H), np.float64)

@@ -43,8 +43,8 @@ def _rand_cache(rng, B, S, fmt=0):
     pe = orc.bf16_round(rng.standard_normal((B, S, DR)).astype(np.float32))
     if fmt == 0:
         return {"fmt": 0, "kv": kv, "pe": pe}
-    q, s = orc.quantize_rows(kv)
-    return {"fmt": 1, "kv": q, "kv_scale": s, "pe": pe}
+    q, s = orc.quantize_rows(kv, pow2=fmt == 2)
+    return {"fmt": fmt, "kv": q, "kv_scale": s, "pe": pe}
 
 
 def _latents(cache):
@@ -115,7 +115,7 @@ def test_rotary_term_alone():
     assert lse[0] == pytest.approx(4096.0, rel=1e-12)
 
 
-@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("fmt", [0, 1, 2])
 def test_absorbed_equals_naive_mha(fmt):
     rng = np.random.default_rng(20 + fmt)
     B, H, S = 2, 3, 9
@@ -186,11 +186,12 @@ def test_empty_sequence():
     assert np.isfinite(lse[2:]).all()
 
 
-def test_fp8_cache_attends_to_round_trip_values():
+@pytest.mark.parametrize("fmt", [1, 2])
+def test_fp8_cache_attends_to_round_trip_values(fmt):
     # Decoding the FP8 cache equals decoding a bf16 cache that holds the
     # dequantised latents (the bf16 cache of the cache-write excerpt).
     rng = np.random.default_rng(34)
-    c8 = _rand_cache(rng, 2, 30, 1)
+    c8 = _rand_cache(rng, 2, 30, fmt)
     c16 = {"fmt": 0, "kv": orc.dequant_rows(c8["kv"], c8["kv_scale"]), "pe": c8["pe"]}
     ql, qp = _rand_q(rng, 2, 3)
     a = orc.decode_absorbed(c8, ql, qp, [30, 11], 0.13)

@@ -172,6 +172,79 @@ def test_round_trip_error_bound():
     assert (np.abs(c - xv) <= bound).all()
 
 
+# ------------------------------------------- power-of-two scale format
+
+def _pow2_at_least_brute(s: float) -> float:
+    """Smallest 2^k (k from -149 up, every fp32 power of two) that is >= s."""
+    k = -149
+    while 2.0 ** k < s:
+        k += 1
+    return 2.0 ** k
+
+
+def test_quantise_pow2_hand_blocks():
+    row = np.zeros(512, np.float32)
+    row[:4] = [448.0, 1.0, -2.0, 2.0 ** -9]   # block 0: amax 448 -> scale exactly 1
+    row[128:256] = 1.0                        # block 1: 1/448 -> 2^-8; 1 / 2^-8 = 256 = 0x78
+    row[256] = 450.0                          # block 2: 450/448 -> 2; 225 -> 224 = 0x76
+    row[257] = -0.5                           #          -0.25 -> 2^-2 = 0xA8
+    row[384] = 2.0 ** -132                    # block 3: fp32(amax/448) = 293 * 2^-149 is
+    row[385] = -(2.0 ** -133)                 #          subnormal, rounds up to 2^-140
+    q, s = orc.quantize_rows(_bf16(row)[None], pow2=True)
+    q, s = q[0], s[0]
+    assert s[0] == 1.0 and list(q[:4]) == [0x7E, 0x38, 0xC0, 0x01]
+    assert s[1] == 2.0 ** -8 and (q[128:256] == 0x78).all()
+    assert s[2] == 2.0 and q[256] == 0x76 and q[257] == 0xA8 and (q[258:384] == 0).all()
+    assert s[3] == np.float32(2.0 ** -140) and q[384] == 0x78 and q[385] == 0xF0
+    zero = np.zeros((1, 512), np.uint16)
+    qz, sz = orc.quantize_rows(zero, pow2=True)
+    assert (sz == 0).all() and (qz == 0).all()
+
+
+def test_quantise_pow2_matches_brute_force():
+    # scale: brute-force smallest power of two >= fp32(amax / 448); codes:
+    # brute-force nearest table value of x / scale, which is exact here
+    g = torch.Generator().manual_seed(6)
+    x = (torch.randn(96, 512, generator=g) * torch.exp(torch.randn(96, 1, generator=g) * 6)).to(torch.bfloat16)
+    bits = x.view(torch.int16).numpy().view(np.uint16)
+    q, s = orc.quantize_rows(bits, pow2=True)
+    xv = orc.bf16_bits_to_f64(bits).reshape(-1, 4, 128)
+    amax = np.abs(xv).max(-1).astype(np.float32)
+    base = amax / np.float32(448.0)
+    want_s = np.array([_pow2_at_least_brute(float(v)) if v > 0 else 0.0 for v in base.ravel()])
+    assert np.array_equal(s.ravel().astype(np.float64), want_s)
+    for r in range(0, 96, 7):
+        for j in range(4):
+            for i in range(0, 128, 5):
+                y = xv[r, j, i] / float(s[r, j])
+                assert q[r, j * 128 + i] == _brute_encode(y), (r, j, i)
+
+
+def test_dequant_pow2_is_exact():
+    # e4m3 values carry 4 significant bits, so value * 2^k is exact in fp32
+    # and in bf16: the round trip adds no rounding beyond the e4m3 code's
+    g = torch.Generator().manual_seed(7)
+    x = (torch.randn(256, 512, generator=g) * 3).to(torch.bfloat16)
+    q, s = orc.quantize_rows(x.view(torch.int16).numpy().view(np.uint16), pow2=True)
+    got = orc.bf16_bits_to_f64(orc.dequant_rows(q, s))
+    want = orc.e4m3_value(q) * np.repeat(s.astype(np.float64), 128, axis=1)
+    assert np.array_equal(got, want)
+
+
+def test_cache_append_pow2_format():
+    g = torch.Generator().manual_seed(8)
+    kv = torch.randn(2, 512, generator=g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    pe = torch.randn(2, 64, generator=g).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    cache = {"fmt": 2, "kv": np.zeros((2, 8, 512), np.uint8), "kv_scale": np.zeros((2, 8, 4), np.float32),
+             "pe": np.zeros((2, 8, 64), np.uint16)}
+    orc.cache_append(cache, kv, pe, [3, 5])
+    q, s = orc.quantize_rows(kv, pow2=True)
+    assert np.array_equal(cache["kv"][0, 3], q[0]) and np.array_equal(cache["kv"][1, 5], q[1])
+    assert np.array_equal(cache["kv_scale"][1, 5], s[1])
+    m, _ = np.frexp(s)
+    assert (m == 0.5).all()
+
+
 def test_footprint_golden():
     # latent-only bytes of one layer; pins the byte accounting used by the bench
     from mla_latent_kv_07_gb300 import layout
