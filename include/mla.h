@@ -59,17 +59,22 @@ typedef enum {
 
 typedef enum {
   MLA_KV_BF16 = 0,           /* kv: bf16 [max_batch, max_seq_len, 512]          */
-  MLA_KV_FP8_E4M3_B128 = 1   /* kv: e4m3 bytes [max_batch, max_seq_len, 512] and
+  MLA_KV_FP8_E4M3_B128 = 1,  /* kv: e4m3 bytes [max_batch, max_seq_len, 512] and
                                 kv_scale: fp32 [max_batch, max_seq_len, 4]      */
+  MLA_KV_FP8_E4M3_B128_POW2 = 2  /* the layout of format 1; every scale is a
+                                power of two (the exponent-only "ue8m0" scale
+                                format), still stored as fp32                   */
 } mla_kv_format;
 
 /* Cache descriptor (caller-owned device buffers, row-major, one slot per
  * sequence, as the register_buffer calls of "DeepSeek-V3.2-Exp . KV cache"
  * lay them out: [max_batch_size, max_seq_len, width]).
  *   kv       latent c_KV: bf16 or e4m3 codes, see mla_kv_format
- *   kv_scale fp32 block scales [max_batch, max_seq_len, 4] (FP8 only; NULL
- *            for bf16).  Scale j covers latent columns 128j..128j+127 and the
- *            stored value is bf16(fp32(e4m3(code) * scale)).
+ *   kv_scale fp32 block scales [max_batch, max_seq_len, 4] (FP8 formats
+ *            only; NULL for bf16).  Scale j covers latent columns
+ *            128j..128j+127 and the stored value is
+ *            bf16(fp32(e4m3(code) * scale)).  The decode calls read formats 1
+ *            and 2 alike; only the cache write differs.
  *   pe       rotary key k_R, bf16 [max_batch, max_seq_len, 64]            */
 typedef struct {
   int32_t fmt;               /* mla_kv_format */
@@ -93,8 +98,11 @@ typedef struct {
  * kv_new[b] into row start_pos[b] of sequence slot b, and pe_new[b] into the
  * same row of pe.  bf16 caches store the row unchanged.  FP8 caches store
  * e4m3 codes and 4 fp32 scales: per 128-wide block, amax = max |x|, scale =
- * fp32(amax / 448), code = e4m3(fp32(x / scale)) with round-to-nearest-even
- * and saturation to +-448; an all-zero block stores scale 0 and code 0.
+ * fp32(amax / 448) -- for MLA_KV_FP8_E4M3_B128_POW2 rounded up to the
+ * smallest power of two not below it (the page passes a scale format to the
+ * quantiser without defining it; this is the exponent-only reading) -- and
+ * code = e4m3(fp32(x / scale)) with round-to-nearest-even and saturation to
+ * +-448; an all-zero block stores scale 0 and code 0.
  *
  *   kv_new     device bf16 [B, 512]
  *   pe_new     device bf16 [B, 64]

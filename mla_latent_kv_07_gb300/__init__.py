@@ -22,6 +22,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libmla.so")
 
 MLA_KV_BF16 = 0
 MLA_KV_FP8_E4M3_B128 = 1
+MLA_KV_FP8_E4M3_B128_POW2 = 2
 DEV_END_POS_CLAMPED = 0x1
 DEV_APPEND_SKIPPED = 0x2
 DEV_PIPELINE_TIMEOUT = 0x4
@@ -113,7 +114,9 @@ def _need(t, dtype, shape, name):
 
 class Cache:
     """Caller-owned latent cache: kv [Bmax, S, 512] (bf16 or e4m3 bytes),
-    kv_scale fp32 [Bmax, S, 4] (FP8 only), pe bf16 [Bmax, S, 64]."""
+    kv_scale fp32 [Bmax, S, 4] (FP8 formats only), pe bf16 [Bmax, S, 64].
+    fmt: MLA_KV_BF16, MLA_KV_FP8_E4M3_B128, or MLA_KV_FP8_E4M3_B128_POW2
+    (FP8 whose appends round every block scale up to a power of two)."""
 
     def __init__(self, max_batch: int, max_seq_len: int, fmt: int = MLA_KV_BF16,
                  device="cuda", kv=None, kv_scale=None, pe=None):
@@ -122,13 +125,13 @@ class Cache:
         if kv is None:
             kv = torch.zeros(shape + (512,), dtype=torch.bfloat16 if fmt == 0 else torch.uint8,
                              device=device)
-        if fmt == MLA_KV_FP8_E4M3_B128 and kv_scale is None:
+        if fmt != MLA_KV_BF16 and kv_scale is None:
             kv_scale = torch.zeros(shape + (4,), dtype=torch.float32, device=device)
         if pe is None:
             pe = torch.zeros(shape + (64,), dtype=torch.bfloat16, device=device)
         _need(kv, torch.bfloat16 if fmt == 0 else torch.uint8, shape + (512,), "kv")
         _need(pe, torch.bfloat16, shape + (64,), "pe")
-        if fmt == MLA_KV_FP8_E4M3_B128:
+        if fmt != MLA_KV_BF16:
             _need(kv_scale, torch.float32, shape + (4,), "kv_scale")
         self.kv, self.kv_scale, self.pe = kv, kv_scale, pe
         self._c = _CCache(fmt, max_batch, max_seq_len, kv.data_ptr(),

@@ -29,10 +29,23 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Smallest power of two >= s, for s > 0 or +inf (returned unchanged).  A
+// normal s with a zero fraction is already one; otherwise the next exponent.
+// A subnormal s is m * 2^-149 with m in [1, 2^23): the answer is 2^ceil(log2 m)
+// units of 2^-149, whose bit pattern is that single bit (2^23 units = the
+// smallest normal, bit 23, comes out the same way).
+__device__ __forceinline__ float pow2_at_least(float s) {
+  const uint32_t u = __float_as_uint(s);
+  const uint32_t e = u >> 23, m = u & 0x7fffffu;
+  if (e == 0) return __uint_as_float(1u << (32 - __clz(m - 1)));
+  return (m == 0 || e == 0xffu) ? s : __uint_as_float((e + 1) << 23);
+}
+
 // ---------------------------------------------------------------- append
 // One CTA (4 warps) per row.  Warp j owns latent block j (128 values, 4 per
-// lane): amax by shuffle, scale = amax / 448 (IEEE fp32 division), codes =
-// e4m3 of x / scale with round-to-nearest-even and saturation.
+// lane): amax by shuffle, scale = amax / 448 (IEEE fp32 division; format 2
+// rounds it up to a power of two), codes = e4m3 of x / scale with
+// round-to-nearest-even and saturation.
 template <bool kDevicePos>
 __global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
   pdl_wait();   // earlier kernels may still read the cache rows written here
@@ -61,7 +74,8 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
     float2 x23 = __bfloat1622float2(h2[1]);
     float amax = fmaxf(fmaxf(fabsf(x01.x), fabsf(x01.y)), fmaxf(fabsf(x23.x), fabsf(x23.y)));
     amax = warp_max(amax);
-    const float scale = __fdiv_rn(amax, 448.0f);
+    float scale = __fdiv_rn(amax, 448.0f);
+    if (p.fmt == 2 && amax > 0.0f) scale = pow2_at_least(scale);
     uint32_t packed = 0;
     if (amax > 0.0f) {
       float2 y01 = make_float2(__fdiv_rn(x01.x, scale), __fdiv_rn(x01.y, scale));

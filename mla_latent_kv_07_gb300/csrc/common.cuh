@@ -87,8 +87,12 @@ inline Workspace carve_workspace(void* base, int B, int H, int K, int num_sms) {
 }
 
 // Parameters of the append kernels.
+// The decode kernels read formats 1 and 2 alike (fp32 scales); only the
+// cache write tells them apart.
+inline int decode_fmt(int fmt) { return fmt == 2 ? 1 : fmt; }
+
 struct AppendParams {
-  int fmt;
+  int fmt;                // 0 bf16, 1 FP8, 2 FP8 with power-of-two scales
   int max_seq_len;
   void* kv;
   float* kv_scale;

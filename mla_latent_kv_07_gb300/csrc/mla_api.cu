@@ -74,10 +74,11 @@ bool supported_heads(int H) { return H == 16 || H == 32 || H == 64 || H == 128; 
 
 mla_status check_cache(const mla_cache* c) {
   if (!c || !c->kv || !c->pe) return MLA_ERR_INVALID_ARG;
-  if (c->fmt != MLA_KV_BF16 && c->fmt != MLA_KV_FP8_E4M3_B128) return MLA_ERR_UNSUPPORTED;
+  if (c->fmt != MLA_KV_BF16 && c->fmt != MLA_KV_FP8_E4M3_B128 && c->fmt != MLA_KV_FP8_E4M3_B128_POW2)
+    return MLA_ERR_UNSUPPORTED;
   if (c->max_batch <= 0 || c->max_seq_len <= 0) return MLA_ERR_INVALID_ARG;
   if (!aligned16(c->kv) || !aligned16(c->pe)) return MLA_ERR_INVALID_ARG;
-  if (c->fmt == MLA_KV_FP8_E4M3_B128 && (!c->kv_scale || !aligned16(c->kv_scale)))
+  if (c->fmt != MLA_KV_BF16 && (!c->kv_scale || !aligned16(c->kv_scale)))
     return MLA_ERR_INVALID_ARG;
   return MLA_OK;
 }
@@ -117,7 +118,7 @@ mla_status check_decode(const DecodeArgs& a, int K, mla::Workspace* ws) {
 
 mla::DecodeParams make_params(const DecodeArgs& a, const mla::Workspace& ws, int K) {
   mla::DecodeParams p{};
-  p.fmt = a.cache->fmt;
+  p.fmt = mla::decode_fmt(a.cache->fmt);
   p.max_seq_len = a.cache->max_seq_len;
   p.kv = a.cache->kv;
   p.kv_scale = a.cache->kv_scale;
@@ -157,8 +158,8 @@ mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cuda
   const bool tc = use_tc_path(a.H);
   cudaError_t e = mla::launch_schedule(
       K ? nullptr : a.end_pos, a.max_end_pos, ws, a.B,
-      tc ? mla::decode_tc_units(a.cache->fmt, K > 0, sms) : mla::target_units_mma(a.H, sms),
-      tc ? mla::decode_tc_granule(a.cache->fmt, K > 0) : mla::decode_mma_granule(), tc, a.mtp_s,
+      tc ? mla::decode_tc_units(mla::decode_fmt(a.cache->fmt), K > 0, sms) : mla::target_units_mma(a.H, sms),
+      tc ? mla::decode_tc_granule(mla::decode_fmt(a.cache->fmt), K > 0) : mla::decode_mma_granule(), tc, a.mtp_s,
       s);
   if (e != cudaSuccess) return cuda_fail(e, "schedule");
   const bool traced = trace_start(s);

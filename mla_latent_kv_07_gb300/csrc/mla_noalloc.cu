@@ -75,10 +75,11 @@ mla_status mla_decode_noalloc(const mla_cache* c, const void* q_latent, const vo
                               const int32_t* end_pos, int32_t max_end_pos, int32_t B, int32_t H,
                               float softmax_scale, void* out, float* lse, void* stream) {
   if (!c || !c->kv || !c->pe) return MLA_ERR_INVALID_ARG;
-  if (c->fmt != MLA_KV_BF16 && c->fmt != MLA_KV_FP8_E4M3_B128) return MLA_ERR_UNSUPPORTED;
+  if (c->fmt != MLA_KV_BF16 && c->fmt != MLA_KV_FP8_E4M3_B128 && c->fmt != MLA_KV_FP8_E4M3_B128_POW2)
+    return MLA_ERR_UNSUPPORTED;
   if (c->max_batch <= 0 || c->max_seq_len <= 0) return MLA_ERR_INVALID_ARG;
   if (!aligned16(c->kv) || !aligned16(c->pe)) return MLA_ERR_INVALID_ARG;
-  if (c->fmt == MLA_KV_FP8_E4M3_B128 && (!c->kv_scale || !aligned16(c->kv_scale)))
+  if (c->fmt != MLA_KV_BF16 && (!c->kv_scale || !aligned16(c->kv_scale)))
     return MLA_ERR_INVALID_ARG;
   if (!(H == 16 || H == 32 || H == 64 || H == 128)) return MLA_ERR_UNSUPPORTED;
   if (B <= 0 || B > c->max_batch) return MLA_ERR_INVALID_ARG;
@@ -99,7 +100,7 @@ mla_status mla_decode_noalloc(const mla_cache* c, const void* q_latent, const vo
   cudaStream_t s = static_cast<cudaStream_t>(stream);
 
   mla::DecodeParams p{};
-  p.fmt = c->fmt;
+  p.fmt = mla::decode_fmt(c->fmt);
   p.max_seq_len = c->max_seq_len;
   p.kv = c->kv;
   p.kv_scale = c->kv_scale;
@@ -120,8 +121,8 @@ mla_status mla_decode_noalloc(const mla_cache* c, const void* q_latent, const vo
   // it is written
   cudaError_t e = mla::launch_schedule(
       end_pos, max_end_pos, ws, B,
-      tc ? mla::decode_tc_units(c->fmt, false, sms) : mla::target_units_mma(H, sms),
-      tc ? mla::decode_tc_granule(c->fmt, false) : mla::decode_mma_granule(), tc, 1, s);
+      tc ? mla::decode_tc_units(mla::decode_fmt(c->fmt), false, sms) : mla::target_units_mma(H, sms),
+      tc ? mla::decode_tc_granule(mla::decode_fmt(c->fmt), false) : mla::decode_mma_granule(), tc, 1, s);
   if (e == cudaSuccess) e = tc ? mla::launch_decode_tc(p, s) : mla::launch_decode_mma(p, s);
   if (e == cudaSuccess) e = mla::launch_combine(ws, B, H, out, lse, s);
   if (e != cudaSuccess) {

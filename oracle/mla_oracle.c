@@ -119,10 +119,11 @@ uint8_t orc_e4m3_encode(float y) {
 /* Cache-write step: FP8 block quantisation and its round trip [KVC]   */
 /* ------------------------------------------------------------------ */
 
-/* Smallest power of two >= s, for a finite s > 0 (fp32 subnormals included):
- * frexp writes s = m * 2^e with m in [0.5, 1); s is itself a power of two
- * exactly when m == 0.5. */
+/* Smallest power of two >= s, for s > 0 (fp32 subnormals included; +inf is
+ * returned as it is): frexp writes s = m * 2^e with m in [0.5, 1); s is
+ * itself a power of two exactly when m == 0.5. */
 static float pow2_at_least(float s) {
+  if (isinf(s)) return s;
   int e;
   double m = frexp((double)s, &e);
   return (float)(m == 0.5 ? (double)s : ldexp(1.0, e));

@@ -28,8 +28,8 @@ def oracle_cache(kv_bf16: torch.Tensor, pe_bf16: torch.Tensor, fmt: int) -> dict
     pe = bits(pe_bf16)
     if fmt == 0:
         return {"fmt": 0, "kv": kv, "pe": pe}
-    q, s = orc.quantize_rows(kv)
-    return {"fmt": 1, "kv": q, "kv_scale": s, "pe": pe}
+    q, s = orc.quantize_rows(kv, pow2=fmt == 2)
+    return {"fmt": fmt, "kv": q, "kv_scale": s, "pe": pe}
 
 
 def device_cache(oc: dict) -> mla.Cache:
@@ -39,7 +39,7 @@ def device_cache(oc: dict) -> mla.Cache:
         return mla.Cache(B, S, 0, kv=kv, pe=_pe(oc))
     kv = torch.from_numpy(oc["kv"]).cuda()
     sc = torch.from_numpy(oc["kv_scale"]).cuda()
-    return mla.Cache(B, S, 1, kv=kv, kv_scale=sc, pe=_pe(oc))
+    return mla.Cache(B, S, oc["fmt"], kv=kv, kv_scale=sc, pe=_pe(oc))
 
 
 def _pe(oc):

@@ -54,7 +54,7 @@ def test_status_strings(L):
 
 
 def _cache(fmt=0, B=2, S=64, scale=True):
-    return mla._CCache(fmt, B, S, FAKE, FAKE + 4096 if (fmt == 1 and scale) else None, FAKE + 8192)
+    return mla._CCache(fmt, B, S, FAKE, FAKE + 4096 if (fmt in (1, 2) and scale) else None, FAKE + 8192)
 
 
 def test_append_rejects_bad_arguments(L):
@@ -70,6 +70,8 @@ def test_append_rejects_bad_arguments(L):
     assert L.mla_cache_append(ctypes.byref(c), ctypes.c_void_p(FAKE + 8), ok_args[2], pos, 2, None) == 1
     c8 = _cache(fmt=1, scale=False)                        # FP8 without scales
     assert L.mla_cache_append(ctypes.byref(c8), ok_args[1], ok_args[2], pos, 2, None) == 1
+    c82 = _cache(fmt=2, scale=False)                       # power-of-two FP8 without scales
+    assert L.mla_cache_append(ctypes.byref(c82), ok_args[1], ok_args[2], pos, 2, None) == 1
     cx = _cache(fmt=7)
     assert L.mla_cache_append(ctypes.byref(cx), ok_args[1], ok_args[2], pos, 2, None) == 3
     wide = _cache(B=4096)                                  # more rows than one call may write

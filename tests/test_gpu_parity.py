@@ -32,7 +32,7 @@ def _rand_bf16(shape, seed):
 
 # ------------------------------------------------------------------ append
 
-@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("fmt", [0, 1, 2])
 def test_append_bit_exact(fmt):
     B, S = 64, 300
     g = torch.Generator().manual_seed(7)
@@ -40,6 +40,8 @@ def test_append_bit_exact(fmt):
     kv_new[0, :128] = 0.0                         # an all-zero block
     kv_new[1, 128:256] = 448.0                    # scale exactly 1
     kv_new[2, 256:384] = torch.tensor([2.0 ** -9, -2.0 ** -10] * 64)
+    kv_new[4, 384:512] = torch.tensor([2.0 ** -132, -(2.0 ** -133)] * 64)   # subnormal fp32 scale
+    kv_new[5, :128] = 450.0                       # power-of-two scale 2 (format 2)
     pe_new = _rand_bf16((B, 64), 8)
     start = np.random.default_rng(9).integers(0, S, B).astype(np.int32)
     start[3] = S - 1
@@ -76,6 +78,8 @@ SMALL = [  # (fmt, H, end_pos per sequence, S)
     (1, 64, [129, 77], 160),
     (0, 128, [300, 33, 1], 320),
     (1, 128, [1000, 513, 2, 64], 1024),
+    (2, 64, [129, 77], 160),                    # power-of-two scales: read like format 1
+    (2, 128, [1000, 513, 2, 64], 1024),
 ]
 
 
@@ -261,9 +265,10 @@ def test_sparse_small_lists_and_outputs():
     check_close(f64(lse).reshape(-1), ref_lse, "lse")
 
 
-def test_sparse_fused_append_sees_the_new_row():
+@pytest.mark.parametrize("fmt", [1, 2])
+def test_sparse_fused_append_sees_the_new_row(fmt):
     B, S, H, K = 3, 128, 128, 64
-    oc = oracle_cache(_rand_bf16((B, S, 512), 61), _rand_bf16((B, S, 64), 62), 1)
+    oc = oracle_cache(_rand_bf16((B, S, 512), 61), _rand_bf16((B, S, 64), 62), fmt)
     dc = device_cache(oc)
     ql, qp = _rand_bf16((B, H, 512), 63), _rand_bf16((B, H, 64), 64)
     ends = np.array([128, 50, 7], np.int32)
@@ -274,6 +279,7 @@ def test_sparse_fused_append_sees_the_new_row():
     orc.cache_append(oc, bits(kv_new), bits(pe_new), ends - 1)
     torch.cuda.synchronize()
     assert np.array_equal(dc.kv.cpu().numpy(), oc["kv"])
+    assert np.array_equal(dc.kv_scale.cpu().numpy().view(np.uint32), oc["kv_scale"].view(np.uint32))
     ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), ends, 0.2, topk=topk)
     check_close(f64(out).reshape(-1, 512), ref, "out")
     check_close(f64(lse).reshape(-1), ref_lse, "lse")
