@@ -42,25 +42,12 @@ __device__ __forceinline__ float pow2_at_least(float s) {
 }
 
 // ---------------------------------------------------------------- append
-// One CTA (4 warps) per row.  Warp j owns latent block j (128 values, 4 per
-// lane): amax by shuffle, scale = amax / 448 (IEEE fp32 division; format 2
-// rounds it up to a power of two), codes = e4m3 of x / scale with
-// round-to-nearest-even and saturation.
-template <bool kDevicePos>
-__global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
-  pdl_wait();   // earlier kernels may still read the cache rows written here
-  pdl_trigger();
-  const int b = blockIdx.x;
-  int row;
-  if (kDevicePos) {
-    row = p.end_pos[b] - 1;
-    if (row < 0 || row >= p.max_seq_len) {
-      if (threadIdx.x == 0) atomicOr(p.status, kDevAppendSkipped);
-      return;
-    }
-  } else {
-    row = p.pos[b];
-  }
+// Row b of the new rows into cache row `row` of slot b, by threads 0..127 of
+// the calling CTA.  Warp j owns latent block j (128 values, 4 per lane): amax
+// by shuffle, scale = amax / 448 (IEEE fp32 division; format 2 rounds it up to
+// a power of two), codes = e4m3 of x / scale with round-to-nearest-even and
+// saturation.
+__device__ void append_row(const AppendRows& p, int b, int row) {
   const size_t r = (size_t)b * p.max_seq_len + row;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int col = warp * kBlk + lane * 4;
@@ -92,6 +79,13 @@ __global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
         static_cast<const __nv_bfloat16*>(p.pe_new) + (size_t)b * kDr)[threadIdx.x];
     reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.pe) + r * kDr)[threadIdx.x] = v;
   }
+}
+
+// One CTA (4 warps) per row, positions from the host (checked there).
+__global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
+  pdl_wait();   // earlier kernels may still read the cache rows written here
+  pdl_trigger();
+  append_row(p.rows, blockIdx.x, p.pos[blockIdx.x]);
 }
 
 // ------------------------------------------------------------ block scan
@@ -136,15 +130,26 @@ constexpr int kPrepWindow = 1 << 18;   // positions per pass: a 32 KB bitmap
 __global__ void __launch_bounds__(1024) sparse_prep_kernel(const int* __restrict__ topk, int K,
                                                           const int* __restrict__ end_pos,
                                                           int max_end_pos, Workspace ws,
-                                                          int* gidx_out, int* gcount_out) {
+                                                          int* gidx_out, int* gcount_out,
+                                                          const AppendRows ap) {
   __shared__ uint32_t bm[kPrepWindow / 32];
   __shared__ int scan_smem[33];
-  pdl_wait();
+  pdl_wait();   // the previous call's kernels may still read the workspace and the cache
   pdl_trigger();
   const int b = blockIdx.x;
-  int T = end_pos[b];
+  const int end = end_pos[b];
+  uint32_t flags = 0;
+  // the fused append: the new row is position end_pos[b] - 1 (warps 0-3)
+  if (ap.kv_new) {
+    const int row = end - 1;
+    if (row < 0 || row >= ap.max_seq_len)
+      flags |= kDevAppendSkipped;
+    else if (threadIdx.x < 128)
+      append_row(ap, b, row);
+  }
+  int T = end;
   if (T < 0 || T > max_end_pos) {
-    if (threadIdx.x == 0) atomicOr(ws.status, kDevEndPosClamped);
+    flags |= kDevEndPosClamped;
     T = T < 0 ? 0 : max_end_pos;
   }
   const int* list = topk + (size_t)b * K;
@@ -184,7 +189,7 @@ __global__ void __launch_bounds__(1024) sparse_prep_kernel(const int* __restrict
     if (gidx_out) gidx_out[(size_t)b * K + k] = -1;
   }
   if (threadIdx.x == 0) {
-    ws.gcount[b] = written;
+    ws.seq_flags[b] = flags;
     ws.lengths[b] = written;
     if (gcount_out) gcount_out[b] = written;
   }
@@ -202,11 +207,12 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
   __shared__ int scan_smem[33];
   __shared__ unsigned long long total_len;
   __shared__ int count_smem, max_len_smem;
+  __shared__ uint32_t flags_smem;
   pdl_wait();   // the previous call's kernels may still read this workspace
   if (threadIdx.x == 0) {
     total_len = 0;
     max_len_smem = 0;
-    if (end_pos) *ws.status = 0u;   // dense: first kernel of the call
+    flags_smem = 0u;
   }
   __syncthreads();
   pdl_trigger();
@@ -214,12 +220,13 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
   const int b0 = threadIdx.x * per;
   unsigned long long mine = 0;
   int longest = 0;
+  uint32_t flags = 0;
   for (int b = b0; b < b0 + per && b < B; ++b) {
     int len;
     if (end_pos) {
       len = end_pos[b / mtp_s];
       if (len < 0 || len > max_end_pos) {
-        atomicOr(ws.status, kDevEndPosClamped);
+        flags |= kDevEndPosClamped;
         len = len < 0 ? 0 : max_end_pos;
       }
       len -= mtp_s - 1 - b % mtp_s;   // token j of the step: one position per later token fewer
@@ -227,6 +234,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
       ws.lengths[b] = len;
     } else {
       len = ws.lengths[b];
+      flags |= ws.seq_flags[b];
     }
     mine += (unsigned long long)len;
     longest = len > longest ? len : longest;
@@ -237,9 +245,11 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
     mine += __shfl_xor_sync(0xffffffffu, mine, o);
     longest = max(longest, __shfl_xor_sync(0xffffffffu, longest, o));
   }
+  flags = __reduce_or_sync(0xffffffffu, flags);
   if ((threadIdx.x & 31) == 0) {
     atomicAdd(&total_len, mine);
     atomicMax(&max_len_smem, longest);
+    if (flags) atomicOr(&flags_smem, flags);
   }
   __syncthreads();
   // a chunk of the longest length gives every non-empty sequence one unit; no
@@ -287,7 +297,10 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
   }
   for (int i = total_units + threadIdx.x; i < ws.max_units; i += blockDim.x)
     ws.units[i] = Unit{-1, 0, 0, 0};
-  if (threadIdx.x == 0) *ws.n_units = total_units;
+  if (threadIdx.x == 0) {
+    *ws.n_units = total_units;
+    *ws.status = flags_smem;   // the call's status word, written afresh
+  }
 }
 
 // ---------------------------------------------------------------- combine
@@ -623,18 +636,14 @@ cudaError_t launch_read_ceiling(const void* buf, size_t bytes, uint32_t* sink, i
 }
 
 cudaError_t launch_append_host_pos(const AppendParams& p, cudaStream_t s) {
-  return launch_pdl(append_kernel<false>, dim3(p.B), dim3(128), 0, s, p);
-}
-
-cudaError_t launch_append_device_pos(const AppendParams& p, cudaStream_t s) {
-  return launch_pdl(append_kernel<true>, dim3(p.B), dim3(128), 0, s, p);
+  return launch_pdl(append_kernel, dim3(p.B), dim3(128), 0, s, p);
 }
 
 cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int max_end_pos,
                                const Workspace& ws, int B, int* gidx_out, int* gcount_out,
-                               cudaStream_t s) {
+                               const AppendRows& ap, cudaStream_t s) {
   return launch_pdl(sparse_prep_kernel, dim3(B), dim3(1024), 0, s, topk, K, end_pos, max_end_pos, ws,
-                    gidx_out, gcount_out);
+                    gidx_out, gcount_out, ap);
 }
 
 cudaError_t launch_schedule(const int* end_pos, int max_end_pos, const Workspace& ws, int B,

@@ -41,7 +41,8 @@ struct Workspace {
   float* part_lse;    // [max_units, H]
   float* part_o;      // [max_units, H, 512]
   int* gidx;          // [B, K] sorted unique gather lists (sparse only)
-  int* gcount;        // [B]
+  uint32_t* seq_flags;  // [B] status bits the sparse prep found per sequence
+                        // (the schedule ORs them into the status word)
   size_t bytes;
   int max_units;
 };
@@ -80,7 +81,7 @@ inline Workspace carve_workspace(void* base, int B, int H, int K, int num_sms) {
   w.part_o = reinterpret_cast<float*>(take(sizeof(float) * (size_t)w.max_units * H * kDc));
   if (K > 0) {
     w.gidx = reinterpret_cast<int*>(take(sizeof(int) * (size_t)B * K));
-    w.gcount = reinterpret_cast<int*>(take(sizeof(int) * (size_t)B));
+    w.seq_flags = reinterpret_cast<uint32_t*>(take(sizeof(uint32_t) * (size_t)B));
   }
   w.bytes = off;
   return w;
@@ -91,7 +92,8 @@ inline Workspace carve_workspace(void* base, int B, int H, int K, int num_sms) {
 // cache write tells them apart.
 inline int decode_fmt(int fmt) { return fmt == 2 ? 1 : fmt; }
 
-struct AppendParams {
+// The cache and the new rows of an append (kv_new == nullptr: no append).
+struct AppendRows {
   int fmt;                // 0 bf16, 1 FP8, 2 FP8 with power-of-two scales
   int max_seq_len;
   void* kv;
@@ -99,10 +101,13 @@ struct AppendParams {
   void* pe;
   const void* kv_new;     // bf16 [B, 512]
   const void* pe_new;     // bf16 [B, 64]
-  const int* end_pos;     // device positions (fused path): row = end_pos[b] - 1
-  uint32_t* status;
+};
+
+// Plain append: row pos[b] of slot b, positions from the host.
+struct AppendParams {
+  AppendRows rows;
   int B;
-  int pos[kMaxAppendB];   // host positions (plain path)
+  int pos[kMaxAppendB];
 };
 
 // Parameters of the decode kernels.
@@ -172,13 +177,15 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // Launchers (defined in the kernel translation units).
 cudaError_t launch_append_host_pos(const AppendParams& p, cudaStream_t s);
-cudaError_t launch_append_device_pos(const AppendParams& p, cudaStream_t s);
+// The sparse call's first kernel: gather lists, gather counts and per-sequence
+// status bits, and (ap.kv_new != nullptr) the append of row end_pos[b] - 1.
 cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int max_end_pos,
                                const Workspace& ws, int B, int* gidx_out, int* gcount_out,
-                               cudaStream_t s);
-// end_pos != nullptr: dense (lengths = clamped end_pos, and the schedule is the
-// first kernel of the call, so it clears the status word); nullptr: the
-// lengths were already written (sparse prep) and the status word cleared.
+                               const AppendRows& ap, cudaStream_t s);
+// end_pos != nullptr: dense (lengths = clamped end_pos); nullptr: the lengths
+// and per-sequence status bits were written by the sparse prep.  Either way
+// the schedule writes the status word afresh (the call's earlier kernels
+// leave it alone), so no memset precedes a call.
 // direct: a sequence that gets a single unit is finished by the decode kernel.
 // mtp_s > 1 (dense): B counts s sequences per cache slot; sequence b is token
 // b % s of slot b / s and attends to end_pos[b / s] - (s - 1 - b % s) positions.

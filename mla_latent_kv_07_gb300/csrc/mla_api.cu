@@ -83,6 +83,18 @@ mla_status check_cache(const mla_cache* c) {
   return MLA_OK;
 }
 
+mla::AppendRows append_rows(const mla_cache* c, const void* kv_new, const void* pe_new) {
+  mla::AppendRows r{};
+  r.fmt = c->fmt;
+  r.max_seq_len = c->max_seq_len;
+  r.kv = c->kv;
+  r.kv_scale = c->kv_scale;
+  r.pe = c->pe;
+  r.kv_new = kv_new;
+  r.pe_new = pe_new;
+  return r;
+}
+
 struct DecodeArgs {
   const mla_cache* cache;
   const void* q_latent;
@@ -197,13 +209,7 @@ mla_status mla_cache_append(const mla_cache* cache, const void* kv_new, const vo
   for (int b = 0; b < B; ++b)
     if (start_pos[b] < 0 || start_pos[b] >= cache->max_seq_len) return MLA_ERR_OUT_OF_RANGE;
   mla::AppendParams p{};
-  p.fmt = cache->fmt;
-  p.max_seq_len = cache->max_seq_len;
-  p.kv = cache->kv;
-  p.kv_scale = cache->kv_scale;
-  p.pe = cache->pe;
-  p.kv_new = kv_new;
-  p.pe_new = pe_new;
+  p.rows = append_rows(cache, kv_new, pe_new);
   p.B = B;
   memcpy(p.pos, start_pos, sizeof(int32_t) * (size_t)B);
   cudaError_t e = mla::launch_append_host_pos(p, static_cast<cudaStream_t>(stream));
@@ -298,25 +304,10 @@ mla_status mla_decode_sparse(const mla_cache* cache, const void* q_latent, const
   mla_status st = check_decode(a, K, &ws);
   if (st != MLA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemsetAsync(ws.status, 0, 16, s);
-  if (e != cudaSuccess) return cuda_fail(e, "memset");
-  if (kv_new) {
-    mla::AppendParams p{};
-    p.fmt = cache->fmt;
-    p.max_seq_len = cache->max_seq_len;
-    p.kv = cache->kv;
-    p.kv_scale = cache->kv_scale;
-    p.pe = cache->pe;
-    p.kv_new = kv_new;
-    p.pe_new = pe_new;
-    p.end_pos = end_pos;
-    p.status = ws.status;
-    p.B = B;
-    e = mla::launch_append_device_pos(p, s);
-    if (e != cudaSuccess) return cuda_fail(e, "append");
-    trace_launches(1);
-  }
-  e = mla::launch_sparse_prep(topk_idx, K, end_pos, max_end_pos, ws, B, gidx_out, gcount_out, s);
+  // the prep kernel also appends the new rows (kv_new may be NULL); the
+  // schedule after it writes the status word, so no memset precedes them
+  cudaError_t e = mla::launch_sparse_prep(topk_idx, K, end_pos, max_end_pos, ws, B, gidx_out,
+                                          gcount_out, append_rows(cache, kv_new, pe_new), s);
   if (e != cudaSuccess) return cuda_fail(e, "sparse_prep");
   trace_launches(1);
   return run_decode(a, ws, K, s);
