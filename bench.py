@@ -234,16 +234,16 @@ class Setup:
                               out=self.out, lse=self.lse, workspace=self.ws)
         else:
             c = self.caches[i % self.rot]
-            for sp in self.start_pos:
-                mla.cache_append(c, self.kv_new, self.pe_new, sp)
             if w.absorb:
                 mla.absorb_q(self.q_nope, self.wkv_b, out=self.ql)
             if w.mtp > 1:
+                for sp in self.start_pos:
+                    mla.cache_append(c, self.kv_new, self.pe_new, sp)
                 mla.decode_mtp(c, self.ql, self.qp, self.ends, w.S, w.softmax_scale, out=self.out,
                                lse=self.lse, workspace=self.ws)
-            else:
-                mla.decode(c, self.ql, self.qp, self.ends, w.S, w.softmax_scale, out=self.out,
-                           lse=self.lse, workspace=self.ws)
+            else:   # the new row (position end_pos - 1) is written by the decode call itself
+                mla.decode_append(c, self.kv_new, self.pe_new, self.ql, self.qp, self.ends, w.S,
+                                  w.softmax_scale, out=self.out, lse=self.lse, workspace=self.ws)
             if w.absorb:
                 mla.project_out(self.out, self.wkv_b, out=self.o)
 
@@ -498,7 +498,7 @@ def run_gpu(args, rank, world, local_rank):
                             "append new row + query absorption + decode + value projection" if w.absorb else
                             f"prefill chunk of {w.mtp} tokens over the {w.T}-position prefix (rows already "
                             "in the cache; causal among the chunk)" if w.mtp > PREFILL_MTP else
-                            "append new row + decode" if w.mtp == 1 else
+                            "append new row + decode (one call: the decode writes the row)" if w.mtp == 1 else
                             f"append {w.mtp} new rows + multi-token decode (each cache position counted once)"),
                    "l2": f"inputs larger than L2: rotating {st.rotation}; L2 {st.l2_bytes / 1e6:.0f} MB",
                    "timing": "CUDA graph of exactly K steps, CUDA events on its stream",
@@ -570,16 +570,16 @@ def run_e2e(st: Setup, K: int, W: int):
                               workspace=st.ws)
             return
         c = st.caches[i % st.rot]
-        for sp in st.start_pos:
-            mla.cache_append(c, d["kv_new"], d["pe_new"], sp)
         ql = mla.absorb_q(d["qn"], st.wkv_b, out=st.ql) if w.absorb else d["ql"]
         x = st.out if w.absorb else o["res"]
         if w.mtp > 1:
+            for sp in st.start_pos:
+                mla.cache_append(c, d["kv_new"], d["pe_new"], sp)
             mla.decode_mtp(c, ql, d["qp"], d["ends"], w.S, w.softmax_scale, out=x, lse=o["lse"],
                            workspace=st.ws)
         else:
-            mla.decode(c, ql, d["qp"], d["ends"], w.S, w.softmax_scale, out=x, lse=o["lse"],
-                       workspace=st.ws)
+            mla.decode_append(c, d["kv_new"], d["pe_new"], ql, d["qp"], d["ends"], w.S, w.softmax_scale,
+                              out=x, lse=o["lse"], workspace=st.ws)
         if w.absorb:
             mla.project_out(x, st.wkv_b, out=o["res"])
 

@@ -154,6 +154,28 @@ MLA_API mla_status mla_decode(const mla_cache* cache, const void* q_latent, cons
                       size_t ws_bytes, void* stream);
 
 /*
+ * mla_decode_append -- the decoding step of "DeepSeek-V3.2-Exp . KV cache"
+ * as one call: the cache-write excerpt (the new latent, rounded through the
+ * cache's format, and rotary key stored at the step's position) followed by
+ * the MQA-decode excerpt (mla_decode), which reads the row just written.
+ * For every b with 1 <= end_pos[b] <= max_end_pos, row end_pos[b]-1 of slot
+ * b receives kv_new[b] / pe_new[b] exactly as mla_cache_append would store
+ * them; the decode then attends to positions 0..end_pos[b]-1.  Sequences
+ * with end_pos[b] outside that range are decoded as mla_decode does (clamped,
+ * flagged) and their row is not written (MLA_DEV_APPEND_SKIPPED).  With the
+ * tensor-memory kernel (H = 128) the row is written inside the decode by the
+ * CTA pair that reads it, so the call launches no append kernel.
+ *
+ *   kv_new, pe_new  device bf16 [B, 512] / [B, 64], 16-byte aligned
+ *   other arguments as mla_decode (one new token per slot: B <= max_batch)
+ */
+MLA_API mla_status mla_decode_append(const mla_cache* cache, const void* kv_new, const void* pe_new,
+                                     const void* q_latent, const void* q_pe, const int32_t* end_pos,
+                                     int32_t max_end_pos, int32_t B, int32_t H, float softmax_scale,
+                                     void* out, float* lse, void* workspace, size_t ws_bytes,
+                                     void* stream);
+
+/*
  * mla_topk_select -- top-k position selection per sequence: the index lists
  * that mla_decode_sparse consumes ("DeepSeek-V3.2-Exp . KV cache",
  * MQA-decode excerpt: topk_indices, one list per sequence, shared by its

@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
             L.mla_workspace_size.restype = SZ
             L.mla_decode.argtypes = [P, P, P, P, I32, I32, I32, F, P, P, P, SZ, P]
             L.mla_decode.restype = I32
+            L.mla_decode_append.argtypes = [P, P, P, P, P, P, I32, I32, I32, F, P, P, P, SZ, P]
+            L.mla_decode_append.restype = I32
             L.mla_topk_select.argtypes = [P, P, I32, I32, I32, P, P]
             L.mla_topk_select.restype = I32
             L.mla_selftest_decode_timeout.argtypes = [P, P, P, P, I32, I32, I32, F, P, P, P, SZ, P]
@@ -184,6 +186,28 @@ def decode(cache: Cache, q_latent, q_pe, end_pos, max_end_pos: int, softmax_scal
     _check(lib().mla_decode(cache.ref, _ptr(q_latent), _ptr(q_pe), _ptr(end_pos), int(max_end_pos),
                             B, H, float(softmax_scale), _ptr(out), _ptr(lse), _ptr(workspace),
                             workspace.numel(), _stream(stream)), "mla_decode")
+    return out, lse
+
+
+def decode_append(cache: Cache, kv_new, pe_new, q_latent, q_pe, end_pos, max_end_pos: int,
+                  softmax_scale: float, out=None, lse=None, workspace=None, want_lse: bool = True,
+                  stream=None):
+    """Append row end_pos[b]-1 of every sequence (kv_new bf16 [B,512], pe_new
+    bf16 [B,64]) and decode over it, in one call (see mla_decode_append);
+    returns (out, lse) as decode."""
+    B, H, _ = q_latent.shape
+    _need(kv_new, torch.bfloat16, (B, 512), "kv_new")
+    _need(pe_new, torch.bfloat16, (B, 64), "pe_new")
+    _need(q_latent, torch.bfloat16, (B, H, 512), "q_latent")
+    _need(q_pe, torch.bfloat16, (B, H, 64), "q_pe")
+    _need(end_pos, torch.int32, (B,), "end_pos")
+    out, lse = _outputs(B, H, q_latent.device, out, lse, want_lse)
+    if workspace is None:
+        workspace = alloc_workspace(B, H, max_end_pos, 0, q_latent.device)
+    _check(lib().mla_decode_append(cache.ref, _ptr(kv_new), _ptr(pe_new), _ptr(q_latent), _ptr(q_pe),
+                                   _ptr(end_pos), int(max_end_pos), B, H, float(softmax_scale), _ptr(out),
+                                   _ptr(lse), _ptr(workspace), workspace.numel(), _stream(stream)),
+           "mla_decode_append")
     return out, lse
 
 

@@ -14,6 +14,7 @@
 
 #include <cuda.h>
 
+#include "append_row.cuh"
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -29,63 +30,23 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
-// Smallest power of two >= s, for s > 0 or +inf (returned unchanged).  A
-// normal s with a zero fraction is already one; otherwise the next exponent.
-// A subnormal s is m * 2^-149 with m in [1, 2^23): the answer is 2^ceil(log2 m)
-// units of 2^-149, whose bit pattern is that single bit (2^23 units = the
-// smallest normal, bit 23, comes out the same way).
-__device__ __forceinline__ float pow2_at_least(float s) {
-  const uint32_t u = __float_as_uint(s);
-  const uint32_t e = u >> 23, m = u & 0x7fffffu;
-  if (e == 0) return __uint_as_float(1u << (32 - __clz(m - 1)));
-  return (m == 0 || e == 0xffu) ? s : __uint_as_float((e + 1) << 23);
-}
-
 // ---------------------------------------------------------------- append
-// Row b of the new rows into cache row `row` of slot b, by threads 0..127 of
-// the calling CTA.  Warp j owns latent block j (128 values, 4 per lane): amax
-// by shuffle, scale = amax / 448 (IEEE fp32 division; format 2 rounds it up to
-// a power of two), codes = e4m3 of x / scale with round-to-nearest-even and
-// saturation.
-__device__ void append_row(const AppendRows& p, int b, int row) {
-  const size_t r = (size_t)b * p.max_seq_len + row;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int col = warp * kBlk + lane * 4;
-  const uint2 raw = *reinterpret_cast<const uint2*>(
-      static_cast<const __nv_bfloat16*>(p.kv_new) + (size_t)b * kDc + col);
-  if (p.fmt == 0) {
-    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.kv) + r * kDc + col) = raw;
-  } else {
-    const __nv_bfloat162* h2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-    float2 x01 = __bfloat1622float2(h2[0]);
-    float2 x23 = __bfloat1622float2(h2[1]);
-    float amax = fmaxf(fmaxf(fabsf(x01.x), fabsf(x01.y)), fmaxf(fabsf(x23.x), fabsf(x23.y)));
-    amax = warp_max(amax);
-    float scale = __fdiv_rn(amax, 448.0f);
-    if (p.fmt == 2 && amax > 0.0f) scale = pow2_at_least(scale);
-    uint32_t packed = 0;
-    if (amax > 0.0f) {
-      float2 y01 = make_float2(__fdiv_rn(x01.x, scale), __fdiv_rn(x01.y, scale));
-      float2 y23 = make_float2(__fdiv_rn(x23.x, scale), __fdiv_rn(x23.y, scale));
-      uint32_t lo = __nv_cvt_float2_to_fp8x2(y01, __NV_SATFINITE, __NV_E4M3);
-      uint32_t hi = __nv_cvt_float2_to_fp8x2(y23, __NV_SATFINITE, __NV_E4M3);
-      packed = (lo & 0xffffu) | (hi << 16);
-    }
-    *reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(p.kv) + r * kDc + col) = packed;
-    if (lane == 0) p.kv_scale[r * kNblk + warp] = scale;
-  }
-  if (threadIdx.x < 8) {  // rotary key: 64 bf16 = 8 x 16 bytes
-    const uint4 v = reinterpret_cast<const uint4*>(
-        static_cast<const __nv_bfloat16*>(p.pe_new) + (size_t)b * kDr)[threadIdx.x];
-    reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.pe) + r * kDr)[threadIdx.x] = v;
-  }
-}
-
 // One CTA (4 warps) per row, positions from the host (checked there).
 __global__ void __launch_bounds__(128) append_kernel(const AppendParams p) {
   pdl_wait();   // earlier kernels may still read the cache rows written here
   pdl_trigger();
-  append_row(p.rows, blockIdx.x, p.pos[blockIdx.x]);
+  append_row(p.rows, blockIdx.x, p.pos[blockIdx.x], threadIdx.x);
+}
+
+// One CTA per sequence: row end_pos[b] - 1, where the dense decode reads it
+// (the warp-MMA decode path; the tensor-memory kernel writes the row itself).
+// Rows left out are flagged by the schedule kernel.
+__global__ void __launch_bounds__(128) append_end_kernel(const AppendRows ap, const int* __restrict__ end_pos,
+                                                         int max_end_pos) {
+  pdl_wait();
+  pdl_trigger();
+  const int end = end_pos[blockIdx.x];
+  if (append_row_valid(end, max_end_pos)) append_row(ap, blockIdx.x, end - 1, threadIdx.x);
 }
 
 // ------------------------------------------------------------ block scan
@@ -145,7 +106,7 @@ __global__ void __launch_bounds__(1024) sparse_prep_kernel(const int* __restrict
     if (row < 0 || row >= ap.max_seq_len)
       flags |= kDevAppendSkipped;
     else if (threadIdx.x < 128)
-      append_row(ap, b, row);
+      append_row(ap, b, row, threadIdx.x);
   }
   int T = end;
   if (T < 0 || T > max_end_pos) {
@@ -203,7 +164,7 @@ __global__ void __launch_bounds__(1024) sparse_prep_kernel(const int* __restrict
 __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ end_pos,
                                                        int max_end_pos, Workspace ws, int B,
                                                        int target, int granule, int direct,
-                                                       int mtp_s) {
+                                                       int mtp_s, int append) {
   __shared__ int scan_smem[33];
   __shared__ unsigned long long total_len;
   __shared__ int count_smem, max_len_smem;
@@ -225,6 +186,8 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
     int len;
     if (end_pos) {
       len = end_pos[b / mtp_s];
+      // a dense call with new rows appends row end_pos - 1 where its decode reads it
+      if (append && !append_row_valid(len, max_end_pos)) flags |= kDevAppendSkipped;
       if (len < 0 || len > max_end_pos) {
         flags |= kDevEndPosClamped;
         len = len < 0 ? 0 : max_end_pos;
@@ -647,10 +610,16 @@ cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int m
 }
 
 cudaError_t launch_schedule(const int* end_pos, int max_end_pos, const Workspace& ws, int B,
-                            int target, int granule, bool direct, int mtp_s, cudaStream_t s) {
+                            int target, int granule, bool direct, int mtp_s, bool append,
+                            cudaStream_t s) {
   const int threads = B >= 1024 ? 1024 : ((B + 31) / 32) * 32;
   return launch_pdl(schedule_kernel, dim3(1), dim3(threads), 0, s, end_pos, max_end_pos, ws, B,
-                    target, granule, direct ? 1 : 0, mtp_s < 1 ? 1 : mtp_s);
+                    target, granule, direct ? 1 : 0, mtp_s < 1 ? 1 : mtp_s, append ? 1 : 0);
+}
+
+cudaError_t launch_append_end(const AppendRows& ap, const int* end_pos, int max_end_pos, int B,
+                              cudaStream_t s) {
+  return launch_pdl(append_end_kernel, dim3(B), dim3(128), 0, s, ap, end_pos, max_end_pos);
 }
 
 cudaError_t launch_combine(const Workspace& ws, int B, int H, void* out, float* lse,

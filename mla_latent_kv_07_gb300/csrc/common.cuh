@@ -128,6 +128,10 @@ struct DecodeParams {
   int mtp_s;              // new tokens per cache slot: sequence b reads slot b / mtp_s (1: plain decode)
   long long spin_limit = 0;   // polls a bounded wait makes before it gives up (0: the default)
   int withhold_tile = -1;     // self-test of the bounded waits: this tile of the first unit is never loaded (-1: none)
+  // dense call with new rows (ap.kv_new != nullptr, one token per slot): the
+  // unit holding position end_pos[b] - 1 writes that row before loading it
+  AppendRows ap{};
+  const int* end_pos = nullptr;
 };
 
 // Raise a kernel's dynamic shared memory limit once per device.  The kernel
@@ -187,10 +191,18 @@ cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int m
 // the schedule writes the status word afresh (the call's earlier kernels
 // leave it alone), so no memset precedes a call.
 // direct: a sequence that gets a single unit is finished by the decode kernel.
+// append (dense): the call also writes new rows; sequences whose row it cannot
+// write (end_pos outside [1, max_end_pos]) raise MLA_DEV_APPEND_SKIPPED.
 // mtp_s > 1 (dense): B counts s sequences per cache slot; sequence b is token
 // b % s of slot b / s and attends to end_pos[b / s] - (s - 1 - b % s) positions.
 cudaError_t launch_schedule(const int* end_pos, int max_end_pos, const Workspace& ws, int B,
-                            int target_units, int granule, bool direct, int mtp_s, cudaStream_t s);
+                            int target, int granule, bool direct, int mtp_s, bool append,
+                            cudaStream_t s);
+// Dense call with new rows, warp-MMA decode path: row end_pos[b] - 1 of every
+// sequence with end_pos[b] in [1, max_end_pos] (schedule with append = true
+// flags the others).
+cudaError_t launch_append_end(const AppendRows& ap, const int* end_pos, int max_end_pos, int B,
+                              cudaStream_t s);
 cudaError_t launch_decode_mma(const DecodeParams& p, cudaStream_t s);
 int decode_mma_granule();
 // tensor-memory path (H = 128): one CTA pair per unit

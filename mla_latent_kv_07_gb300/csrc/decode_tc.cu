@@ -37,7 +37,10 @@
 //              head h <-> TMEM lane h, each half of the tile's positions;
 //              online softmax (lazy rescale), P, epilogue
 //   warps 8-11 exchange: partial S of each tile from TMEM -> peer (DSMEM),
-//              as soon as it is computed.  Distributed shared memory moves
+//              as soon as it is computed.  (A dense call with new rows: in
+//              the unit that reads the new row they first write it to the
+//              cache -- the cache-write step -- before the producer loads
+//              the unit's last tile.)  Distributed shared memory moves
 //              ~20-35 GB/s per SM with ~0.3 us latency on this part (its
 //              delivery is on the tile's critical path), so sending runs as
 //              its own pipeline stage, ahead of the softmax; the softmax adds
@@ -57,6 +60,7 @@
 #include <mutex>
 #include <string.h>
 
+#include "append_row.cuh"
 #include "common.cuh"
 #include "tc_ptx.cuh"
 
@@ -214,6 +218,7 @@ struct Bars {
   volatile int pv_issued;   // PV issuer: tiles whose PV is issued (paces QK)
   uint64_t qbar;    // query rows staged in shared memory
   uint64_t qready;  // query half in tensor memory
+  uint64_t appended;  // the new row is in the cache (dense call with new rows)
   uint32_t tmem;
   volatile int abort;
   float pair_max[2][256];   // softmax: tile maxima of the pair's halves, by tile parity
@@ -366,6 +371,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     bars->pv_issued = 0;
     bar_init(&bars->qbar, 1);
     bar_init(&bars->qready, 4);
+    bar_init(&bars->appended, 4);   // the exchange warps
     bars->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -387,6 +393,11 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   const Unit u = p.ws.units[unit_id];
   const bool live = u.b >= 0;   // both CTAs of the cluster read the same unit
   const int ntiles = live ? (u.t1 - u.t0 + kN - 1) / kN : 0;
+  // A dense call with new rows: the unit that ends at end_pos[b] (the
+  // sequence's last, and only if end_pos was not clamped) writes row
+  // end_pos[b] - 1 before its producer loads the last tile.  Both CTAs write
+  // the whole row (the same bytes), so each loads only what it wrote itself.
+  const bool app = !kSparse && live && p.ap.kv_new != nullptr && u.t1 == p.end_pos[u.b];
 
   // Q half -> tensor memory (A operand of QK): lane h, 2 bf16 per column.
   // Five TMA boxes stage the 128 rows (4 latent blocks of 64 columns, the 64
@@ -452,6 +463,10 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         // self-test: this tile's load is never issued, so the waits on it run
         // out (the drain below skips it)
         continue;
+      }
+      if (app && i == ntiles - 1) {   // the tile that holds the new row
+        if (!wt.wait(&bars->appended, 0)) break;
+        fence_async_global();
       }
       if (!kSparse) {
         if (lane == 0) {
@@ -644,6 +659,12 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     // writes 512 contiguous bytes per store), after releasing the S buffer.
     const int h = threadIdx.x - 256;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    if (app) {   // idle until the first scores: write the new row first
+      append_row(p.ap, u.b, u.t1 - 1, h);
+      fence_async_global();
+      __syncwarp();
+      if (lane == 0) bar_arrive(&bars->appended);
+    }
     for (int i = 0; i < ntiles; ++i) {
       const int b = ssel(i);
       if (!wt.wait(&bars->sfull[b], spar(i))) break;

@@ -163,21 +163,35 @@ bool use_tc_path(int H) {
 }
 
 // schedule -> decode -> combine, after the lengths are known on the device.
+// ap (dense, one token per slot): also write row end_pos[b] - 1 of every
+// sequence from ap.kv_new / ap.pe_new -- inside the tensor-memory decode
+// kernel, or by a kernel of its own ahead of the warp-MMA path.
 mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cudaStream_t s,
-                      long long spin_limit = 0, int withhold_tile = -1) {
+                      long long spin_limit = 0, int withhold_tile = -1,
+                      const mla::AppendRows* ap = nullptr) {
   int sms = 0;
   num_sms(&sms);
   const bool tc = use_tc_path(a.H);
-  cudaError_t e = mla::launch_schedule(
+  cudaError_t e;
+  if (ap && !tc) {
+    e = mla::launch_append_end(*ap, a.end_pos, a.max_end_pos, a.B, s);
+    if (e != cudaSuccess) return cuda_fail(e, "append");
+    trace_launches(1);
+  }
+  e = mla::launch_schedule(
       K ? nullptr : a.end_pos, a.max_end_pos, ws, a.B,
       tc ? mla::decode_tc_units(mla::decode_fmt(a.cache->fmt), K > 0, sms) : mla::target_units_mma(a.H, sms),
       tc ? mla::decode_tc_granule(mla::decode_fmt(a.cache->fmt), K > 0) : mla::decode_mma_granule(), tc, a.mtp_s,
-      s);
+      ap != nullptr, s);
   if (e != cudaSuccess) return cuda_fail(e, "schedule");
   const bool traced = trace_start(s);
   mla::DecodeParams p = make_params(a, ws, K);
   p.spin_limit = spin_limit;
   p.withhold_tile = withhold_tile;
+  if (ap && tc) {
+    p.ap = *ap;
+    p.end_pos = a.end_pos;
+  }
   e = tc ? mla::launch_decode_tc(p, s) : mla::launch_decode_mma(p, s);
   trace_stop(s, traced);
   if (e != cudaSuccess) return cuda_fail(e, "decode");
@@ -236,8 +250,23 @@ mla_status mla_decode(const mla_cache* cache, const void* q_latent, const void* 
   mla::Workspace ws;
   mla_status st = check_decode(a, 0, &ws);
   if (st != MLA_OK) return st;
-  // the schedule kernel, first of the dense call, clears the status word
+  // the schedule kernel, first of the dense call, writes the status word afresh
   return run_decode(a, ws, 0, static_cast<cudaStream_t>(stream));
+}
+
+mla_status mla_decode_append(const mla_cache* cache, const void* kv_new, const void* pe_new,
+                             const void* q_latent, const void* q_pe, const int32_t* end_pos,
+                             int32_t max_end_pos, int32_t B, int32_t H, float softmax_scale, void* out,
+                             float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  g_last_error[0] = 0;
+  if (!kv_new || !pe_new || !aligned16(kv_new) || !aligned16(pe_new)) return MLA_ERR_INVALID_ARG;
+  DecodeArgs a{cache, q_latent, q_pe, end_pos, max_end_pos, B, H, softmax_scale, out, lse,
+               workspace, ws_bytes, 1};
+  mla::Workspace ws;
+  mla_status st = check_decode(a, 0, &ws);
+  if (st != MLA_OK) return st;
+  const mla::AppendRows ap = append_rows(cache, kv_new, pe_new);
+  return run_decode(a, ws, 0, static_cast<cudaStream_t>(stream), 0, -1, &ap);
 }
 
 mla_status mla_topk_select(const float* scores, const int32_t* end_pos, int32_t B, int32_t max_end_pos,

@@ -122,7 +122,8 @@ mla_status mla_decode_noalloc(const mla_cache* c, const void* q_latent, const vo
   cudaError_t e = mla::launch_schedule(
       end_pos, max_end_pos, ws, B,
       tc ? mla::decode_tc_units(mla::decode_fmt(c->fmt), false, sms) : mla::target_units_mma(H, sms),
-      tc ? mla::decode_tc_granule(mla::decode_fmt(c->fmt), false) : mla::decode_mma_granule(), tc, 1, s);
+      tc ? mla::decode_tc_granule(mla::decode_fmt(c->fmt), false) : mla::decode_mma_granule(), tc, 1,
+      false, s);
   if (e == cudaSuccess) e = tc ? mla::launch_decode_tc(p, s) : mla::launch_decode_mma(p, s);
   if (e == cudaSuccess) e = mla::launch_combine(ws, B, H, out, lse, s);
   if (e != cudaSuccess) {

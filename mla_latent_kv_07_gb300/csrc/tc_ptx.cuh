@@ -76,6 +76,10 @@ __device__ __forceinline__ void cluster_sync() {
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// generic-proxy global writes of this thread -> later tensor copies (async proxy)
+__device__ __forceinline__ void fence_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
 __device__ __forceinline__ void tc_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }

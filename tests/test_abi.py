@@ -95,6 +95,22 @@ def test_decode_rejects_bad_arguments(L):
     assert dec(scale=float("nan")) == 1
 
 
+def test_decode_append_rejects_bad_arguments(L):
+    c = _cache(fmt=1)
+    f = ctypes.c_void_p(FAKE)
+
+    def da(kv=f, pe=f, B=2, H=128, max_end=64):
+        return L.mla_decode_append(ctypes.byref(c), kv, pe, f, f, f, max_end, B, H, 0.1, f, None, f,
+                                   1 << 30, None)
+
+    assert da(kv=None) == 1
+    assert da(pe=None) == 1
+    assert da(kv=ctypes.c_void_p(FAKE + 8)) == 1            # misaligned new rows
+    assert da(B=3) == 1                                     # B > max_batch
+    assert da(H=48) == 3
+    assert da(max_end=65) == 2
+
+
 def test_sparse_rejects_bad_arguments(L):
     c = _cache(fmt=1)
     f = ctypes.c_void_p(FAKE)

@@ -153,6 +153,80 @@ def test_empty_and_clamped_sequences():
     assert mla.workspace_status(ws) == 0
 
 
+# ------------------------------------------------- decode with the append
+
+def _oracle_append(oc, kv_new, pe_new, seqs, pos):
+    """The oracle's cache write of row pos[i] of sequence seqs[i] (numpy views
+    of the oracle cache, so the rows land in place)."""
+    for b, t in zip(seqs, pos):
+        view = {k: (v[b:b + 1] if isinstance(v, np.ndarray) else v) for k, v in oc.items()}
+        orc.cache_append(view, kv_new[b:b + 1], pe_new[b:b + 1], [int(t)])
+
+
+APPEND_CASES = [  # (fmt, H, end_pos per sequence, max_end_pos, S)
+    (0, 128, [1000, 33, 1, 700, 0], 1000, 1024),   # split, single-unit, one row, empty
+    (1, 128, [1000, 513, 2, 64], 1000, 1024),
+    (2, 128, [900, 47, 48, 49], 900, 960),          # tile edges around the new row
+    (0, 64, [300, 1, 129], 300, 320),               # warp-MMA path: an append kernel of its own
+    (1, 16, [100, 257, 5], 257, 300),
+]
+
+
+@pytest.mark.parametrize("fmt,H,ends,max_end,S", APPEND_CASES)
+def test_decode_append_equals_append_then_decode(fmt, H, ends, max_end, S):
+    # the call writes row end_pos - 1 exactly as mla_cache_append would and the
+    # decode reads it: the cache-write and MQA-decode excerpts in that order
+    B = len(ends)
+    seed = 7 * H + S + fmt
+    oc = oracle_cache(_rand_bf16((B, S, 512), seed), _rand_bf16((B, S, 64), seed + 1), fmt)
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((B, H, 512), seed + 2), _rand_bf16((B, H, 64), seed + 3)
+    kv_new, pe_new = _rand_bf16((B, 512), seed + 4), _rand_bf16((B, 64), seed + 5)
+    kv_new[0, :128] = 0.0                                  # an all-zero block
+    end_pos = np.array(ends, np.int32)
+    ws = mla.alloc_workspace(B, H, max_end)
+    out, lse = mla.decode_append(dc, kv_new.cuda(), pe_new.cuda(), ql.cuda(), qp.cuda(),
+                                 torch.from_numpy(end_pos).cuda(), max_end, 0.11, workspace=ws)
+    ok = (end_pos >= 1) & (end_pos <= max_end)
+    _oracle_append(oc, bits(kv_new), bits(pe_new), np.flatnonzero(ok), end_pos[ok] - 1)
+    torch.cuda.synchronize()
+    if fmt == 0:
+        assert np.array_equal(bits(dc.kv.cpu()), oc["kv"])
+    else:
+        assert np.array_equal(dc.kv.cpu().numpy(), oc["kv"])
+        assert np.array_equal(dc.kv_scale.cpu().numpy().view(np.uint32), oc["kv_scale"].view(np.uint32))
+    assert np.array_equal(bits(dc.pe.cpu()), oc["pe"])
+    want = (0 if ok.all() else mla.DEV_APPEND_SKIPPED) | \
+        (0 if ((end_pos >= 0) & (end_pos <= max_end)).all() else mla.DEV_END_POS_CLAMPED)
+    assert mla.workspace_status(ws) == want
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), np.clip(end_pos, 0, max_end), 0.11)
+    check_close(f64(out).reshape(-1, 512), ref, "out")
+    check_close(f64(lse).reshape(-1), ref_lse, "lse")
+
+
+def test_decode_append_skips_clamped_rows():
+    # end_pos past max_end_pos: decoded clamped, row not written, both flagged
+    B, S, H = 2, 256, 128
+    oc = oracle_cache(_rand_bf16((B, S, 512), 141), _rand_bf16((B, S, 64), 142), 1)
+    dc = device_cache(oc)
+    before = dc.kv.clone(), dc.kv_scale.clone(), dc.pe.clone()
+    ql, qp = _rand_bf16((B, H, 512), 143), _rand_bf16((B, H, 64), 144)
+    kv_new, pe_new = _rand_bf16((B, 512), 145), _rand_bf16((B, 64), 146)
+    ends = torch.tensor([200, 150], dtype=torch.int32).cuda()       # max_end_pos 160
+    ws = mla.alloc_workspace(B, H, 160)
+    out, lse = mla.decode_append(dc, kv_new.cuda(), pe_new.cuda(), ql.cuda(), qp.cuda(), ends, 160, 0.2,
+                                 workspace=ws)
+    assert mla.workspace_status(ws) == mla.DEV_APPEND_SKIPPED | mla.DEV_END_POS_CLAMPED
+    torch.cuda.synchronize()
+    assert torch.equal(dc.kv[0], before[0][0]) and torch.equal(dc.pe[0], before[2][0])
+    _oracle_append(oc, bits(kv_new), bits(pe_new), [1], [149])
+    assert np.array_equal(dc.kv[1].cpu().numpy(), oc["kv"][1])
+    assert np.array_equal(dc.kv_scale[1].cpu().numpy().view(np.uint32), oc["kv_scale"][1].view(np.uint32))
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), np.array([160, 150], np.int32), 0.2)
+    check_close(f64(out).reshape(-1, 512), ref, "out")
+    check_close(f64(lse).reshape(-1), ref_lse, "lse")
+
+
 @pytest.mark.parametrize("fmt", [0, 1])
 def test_bounded_wait_runs_out_and_reports(fmt):
     # the self-test withholds the first unit's first tile: its waits run out
