@@ -250,11 +250,14 @@ __global__ void __launch_bounds__(1024) schedule_kernel(const int* __restrict__ 
     const int len = ws.lengths[b];
     const int n = (int)((len + chunk - 1) / chunk);
     const int one = direct && n == 1;
+    // the new row end_pos - 1 lies in the sequence's last unit (t1 = end_pos:
+    // a valid end_pos is not clamped)
+    const int app = append && end_pos && mtp_s == 1 && append_row_valid(end_pos[b], max_end_pos) ? kUnitAppend : 0;
     ws.seq[b] = make_int2(u, one ? -1 : n);
     for (int i = 0; i < n; ++i) {
       int t0 = (int)(i * chunk);
       int t1 = (int)((i + 1) * chunk < len ? (i + 1) * chunk : len);
-      ws.units[u + i] = Unit{b, t0, t1, one};
+      ws.units[u + i] = Unit{b, t0, t1, (one ? kUnitDirect : 0) | (i == n - 1 ? app : 0)};
     }
     u += n;
   }

@@ -24,11 +24,14 @@ constexpr uint32_t kDevAppendSkipped = 0x2u;
 constexpr uint32_t kDevTimeout = 0x4u;
 
 // One unit of decode work: positions [t0, t1) of sequence b (dense), or
-// entries [t0, t1) of b's gather list (sparse).  b < 0: no work.  direct: the
-// unit is its sequence's only one and the decode writes the final output and
-// log-sum-exp itself (the combine skips the sequence).
+// entries [t0, t1) of b's gather list (sparse).  b < 0: no work.  Flags:
+// kUnitDirect, the unit is its sequence's only one and the decode writes the
+// final output and log-sum-exp itself (the combine skips the sequence);
+// kUnitAppend, a dense call with new rows whose row end_pos - 1 = t1 - 1 this
+// unit writes before reading it (tensor-memory kernel).
+constexpr int kUnitDirect = 1, kUnitAppend = 2;
 struct Unit {
-  int b, t0, t1, direct;
+  int b, t0, t1, flags;
 };
 
 // Workspace carve-up.  Every region starts on a 256-byte boundary.
@@ -129,9 +132,8 @@ struct DecodeParams {
   long long spin_limit = 0;   // polls a bounded wait makes before it gives up (0: the default)
   int withhold_tile = -1;     // self-test of the bounded waits: this tile of the first unit is never loaded (-1: none)
   // dense call with new rows (ap.kv_new != nullptr, one token per slot): the
-  // unit holding position end_pos[b] - 1 writes that row before loading it
+  // unit flagged kUnitAppend writes row t1 - 1 before loading it
   AppendRows ap{};
-  const int* end_pos = nullptr;
 };
 
 // Raise a kernel's dynamic shared memory limit once per device.  The kernel

@@ -393,11 +393,11 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   const Unit u = p.ws.units[unit_id];
   const bool live = u.b >= 0;   // both CTAs of the cluster read the same unit
   const int ntiles = live ? (u.t1 - u.t0 + kN - 1) / kN : 0;
-  // A dense call with new rows: the unit that ends at end_pos[b] (the
-  // sequence's last, and only if end_pos was not clamped) writes row
-  // end_pos[b] - 1 before its producer loads the last tile.  Both CTAs write
-  // the whole row (the same bytes), so each loads only what it wrote itself.
-  const bool app = !kSparse && live && p.ap.kv_new != nullptr && u.t1 == p.end_pos[u.b];
+  // A dense call with new rows: the unit the schedule flagged (the
+  // sequence's last; end_pos not clamped) writes row t1 - 1 = end_pos - 1
+  // before its producer loads the last tile.  Both CTAs write the whole row
+  // (the same bytes), so each loads only what it wrote itself.
+  const bool app = !kSparse && live && (u.flags & kUnitAppend) && p.ap.kv_new != nullptr;
 
   // Q half -> tensor memory (A operand of QK): lane h, 2 bf16 per column.
   // Five TMA boxes stage the 128 rows (4 latent blocks of 64 columns, the 64
@@ -464,10 +464,9 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         // out (the drain below skips it)
         continue;
       }
-      if (app && i == ntiles - 1) {   // the tile that holds the new row
-        if (!wt.wait(&bars->appended, 0)) break;
-        fence_async_global();
-      }
+      // the tile that holds the new row: its writers fenced their stores
+      // for the tensor copies before arriving
+      if (app && i == ntiles - 1 && !wt.wait(&bars->appended, 0)) break;
       if (!kSparse) {
         if (lane == 0) {
           if (kFmt == 0) {
@@ -863,14 +862,14 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       softmax_sync();
       const float lt = bars->l_half[h] + bars->l_half[128 + h];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      if (u.direct)
+      if (u.flags & kUnitDirect)
         stage_output_bf16(lane_base, sm, h, inv, 4 * sh, 4 * sh + 4);
       else
         stage_output(lane_base, sm, h, inv, 4 * sh, 4 * sh + 4);
       fence_async_smem();
       softmax_sync();
       if (sh == 0 && h == 0) {
-        if (u.direct) {
+        if (u.flags & kUnitDirect) {
           for (int c = 0; c < kHalf / 64; ++c)
             tma3_store(&tp.m_out, rank * kHalf + 64 * c, 0, u.b, sm + c * kSwBlk);
         } else {
@@ -881,7 +880,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       }
       if (rank == 0 && sh == 0) {
         const float lse = (ok && lt > 0.f) ? (m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
-        if (!u.direct)
+        if (!(u.flags & kUnitDirect))
           p.ws.part_lse[(size_t)unit_id * p.H + h] = lse;
         else if (p.lse)
           p.lse[(size_t)u.b * p.H + h] = lse;

@@ -188,10 +188,7 @@ mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cuda
   mla::DecodeParams p = make_params(a, ws, K);
   p.spin_limit = spin_limit;
   p.withhold_tile = withhold_tile;
-  if (ap && tc) {
-    p.ap = *ap;
-    p.end_pos = a.end_pos;
-  }
+  if (ap && tc) p.ap = *ap;
   e = tc ? mla::launch_decode_tc(p, s) : mla::launch_decode_mma(p, s);
   trace_stop(s, traced);
   if (e != cudaSuccess) return cuda_fail(e, "decode");
