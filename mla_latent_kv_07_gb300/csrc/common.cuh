@@ -113,6 +113,17 @@ struct AppendParams {
   int pos[kMaxAppendB];
 };
 
+// A dense call's split schedule, for kernels that compute it themselves
+// (schedule.cuh); end_pos == nullptr: the schedule kernel wrote the units.
+// One warp holds the lengths (four per lane), so B <= kWarpScheduleMaxB.
+constexpr int kWarpScheduleMaxB = 128;
+struct DenseSchedule {
+  const int* end_pos;   // device [B / mtp_s]
+  int max_end_pos, B, target, granule, mtp_s;
+  int direct;           // a sequence with a single unit is finished by the decode
+  int append;           // the call writes row end_pos - 1 (the last unit does)
+};
+
 // Parameters of the decode kernels.
 struct DecodeParams {
   int fmt;
@@ -134,6 +145,7 @@ struct DecodeParams {
   // dense call with new rows (ap.kv_new != nullptr, one token per slot): the
   // unit flagged kUnitAppend writes row t1 - 1 before loading it
   AppendRows ap{};
+  DenseSchedule sched{};   // tensor-memory dense calls: each CTA finds its unit
 };
 
 // Raise a kernel's dynamic shared memory limit once per device.  The kernel

@@ -62,6 +62,7 @@
 
 #include "append_row.cuh"
 #include "common.cuh"
+#include "schedule.cuh"
 #include "tc_ptx.cuh"
 
 namespace mla {
@@ -219,6 +220,7 @@ struct Bars {
   uint64_t qbar;    // query rows staged in shared memory
   uint64_t qready;  // query half in tensor memory
   uint64_t appended;  // the new row is in the cache (dense call with new rows)
+  Unit unit;          // this pair's unit, when the kernel computes the schedule
   uint32_t tmem;
   volatile int abort;
   float pair_max[2][256];   // softmax: tile maxima of the pair's halves, by tile parity
@@ -390,7 +392,33 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   // call's schedule (and everything before it in the stream) is complete.
   pdl_wait();
   pdl_trigger();
-  const Unit u = p.ws.units[unit_id];
+  const Unit u = [&]() -> Unit {
+    // only the dense bf16 variant computes its schedule (the FP8 variant runs
+    // at its register limit, where this code cost more than it saved)
+    if constexpr (kSparse || kFmt != 0) {
+      return p.ws.units[unit_id];
+    } else {
+      if (p.sched.end_pos == nullptr) return p.ws.units[unit_id];
+      // warp 2 works out the schedule and this pair's unit (the first pair's
+      // rank-0 CTA also writes the combine's per-sequence table, the unit
+      // count and the call's status word, afresh)
+      if (warp == 2) {
+        const bool writer = unit_id == 0 && rank == 0;
+        uint32_t flags = 0;
+        int units = 0;
+        const Unit mine = warp_schedule(p.sched, unit_id, &flags, &units, writer ? p.ws.seq : nullptr);
+        if (lane == 0) {
+          bars->unit = mine;
+          if (writer) {
+            *p.ws.status = flags;
+            *p.ws.n_units = units;
+          }
+        }
+      }
+      __syncthreads();
+      return bars->unit;
+    }
+  }();
   const bool live = u.b >= 0;   // both CTAs of the cluster read the same unit
   const int ntiles = live ? (u.t1 - u.t0 + kN - 1) / kN : 0;
   // A dense call with new rows: the unit the schedule flagged (the

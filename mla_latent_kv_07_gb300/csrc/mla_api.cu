@@ -178,23 +178,35 @@ mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cuda
     if (e != cudaSuccess) return cuda_fail(e, "append");
     trace_launches(1);
   }
-  e = mla::launch_schedule(
-      K ? nullptr : a.end_pos, a.max_end_pos, ws, a.B,
-      tc ? mla::decode_tc_units(mla::decode_fmt(a.cache->fmt), K > 0, sms) : mla::target_units_mma(a.H, sms),
-      tc ? mla::decode_tc_granule(mla::decode_fmt(a.cache->fmt), K > 0) : mla::decode_mma_granule(), tc, a.mtp_s,
-      ap != nullptr, s);
-  if (e != cudaSuccess) return cuda_fail(e, "schedule");
+  const int target =
+      tc ? mla::decode_tc_units(mla::decode_fmt(a.cache->fmt), K > 0, sms) : mla::target_units_mma(a.H, sms);
+  const int granule = tc ? mla::decode_tc_granule(mla::decode_fmt(a.cache->fmt), K > 0) : mla::decode_mma_granule();
+  // dense bf16 calls of up to kWarpScheduleMaxB sequences on the
+  // tensor-memory kernel: every CTA pair works out its own unit, so no
+  // schedule kernel sits between the call's start and its first loads.  (The
+  // FP8 variant runs at its register limit, where the added code cost more
+  // than it saved; long calls -- prefill chunks -- keep the schedule kernel.)
+  const bool fused_schedule =
+      tc && K == 0 && mla::decode_fmt(a.cache->fmt) == 0 && a.B <= mla::kWarpScheduleMaxB;
+  if (!fused_schedule) {
+    e = mla::launch_schedule(K ? nullptr : a.end_pos, a.max_end_pos, ws, a.B, target, granule, tc, a.mtp_s,
+                             ap != nullptr, s);
+    if (e != cudaSuccess) return cuda_fail(e, "schedule");
+    trace_launches(1);
+  }
   const bool traced = trace_start(s);
   mla::DecodeParams p = make_params(a, ws, K);
   p.spin_limit = spin_limit;
   p.withhold_tile = withhold_tile;
   if (ap && tc) p.ap = *ap;
+  if (fused_schedule)
+    p.sched = mla::DenseSchedule{a.end_pos, a.max_end_pos, a.B, target, granule, a.mtp_s, 1, ap != nullptr ? 1 : 0};
   e = tc ? mla::launch_decode_tc(p, s) : mla::launch_decode_mma(p, s);
   trace_stop(s, traced);
   if (e != cudaSuccess) return cuda_fail(e, "decode");
   e = mla::launch_combine(ws, a.B, a.H, a.out, a.lse, s);
   if (e != cudaSuccess) return cuda_fail(e, "combine");
-  trace_launches(3);
+  trace_launches(2);
   return MLA_OK;
 }
 

@@ -227,6 +227,43 @@ def test_decode_append_skips_clamped_rows():
     check_close(f64(lse).reshape(-1), ref_lse, "lse")
 
 
+SCHEDULE_CASES = [  # (end_pos per slot, max_end_pos, S, new tokens per slot)
+    ([4096] * 8, 4096, 4096, 1),
+    ([1, 0, 5000, 37, 4096, 48, 49, 2000, 3000], 4096, 4096, 1),    # empty, clamped, tile edges
+    (list(np.random.default_rng(151).integers(0, 1000, 33)), 900, 1000, 1),   # two lane blocks
+    (list(np.random.default_rng(152).integers(0, 300, 128)), 256, 300, 1),    # the warp's limit
+    ([100, 3, 2, 50, 0], 128, 128, 3),                              # multi-token
+]
+
+
+@pytest.mark.parametrize("ends,max_end,S,s", SCHEDULE_CASES)
+def test_kernel_schedule_matches_schedule_kernel(ends, max_end, S, s):
+    # dense bf16 calls (H = 128, up to 128 sequences) compute the split
+    # schedule inside the decode kernel; FP8 calls run the schedule kernel.
+    # Both follow one rule, so for the same end_pos the workspace's status
+    # word, unit count and per-sequence table must agree byte for byte.
+    B, H = len(ends), 128
+    end_pos = torch.tensor(ends, dtype=torch.int32).cuda()
+    tables = []
+    for fmt in (0, 1):
+        dc = mla.Cache(B, S, fmt)
+        ql = _rand_bf16((B * s, H, 512), 153).cuda() if s == 1 else _rand_bf16((B, s, H, 512), 153).cuda()
+        qp = _rand_bf16((B * s, H, 64), 154).cuda() if s == 1 else _rand_bf16((B, s, H, 64), 154).cuda()
+        ws = mla.alloc_workspace(B * s, H, max_end)
+        if s == 1:
+            kv_new, pe_new = _rand_bf16((B, 512), 155).cuda(), _rand_bf16((B, 64), 156).cuda()
+            mla.decode_append(dc, kv_new, pe_new, ql, qp, end_pos, max_end, 0.1, workspace=ws)
+        else:
+            mla.decode_mtp(dc, ql, qp, end_pos, max_end, 0.1, workspace=ws)
+        torch.cuda.synchronize()
+        tables.append(ws[:256 + 8 * B * s].cpu().numpy())
+    hdr = [tb[:8].view(np.int32) for tb in tables]
+    assert hdr[0][0] == hdr[1][0] and hdr[0][1] == hdr[1][1], hdr
+    assert np.array_equal(tables[0][256:], tables[1][256:])
+    seq = tables[0][256:].view(np.int32).reshape(-1, 2)
+    assert (seq[:, 1] >= -1).all() and hdr[0][1] >= int((seq[:, 1] != 0).sum())
+
+
 @pytest.mark.parametrize("fmt", [0, 1])
 def test_bounded_wait_runs_out_and_reports(fmt):
     # the self-test withholds the first unit's first tile: its waits run out
