@@ -32,7 +32,9 @@
 //   warp 0  producer: TMA tiles (dense) or four-row TMA gathers (gather)
 //   warp 1  MMA issuer (one thread; of QK only in the dense variants) and
 //           tensor-memory owner
-//   dense variants: PV issuer (one thread), warp 2 (bf16) or warp 20 (FP8)
+//   dense variants: PV issuer (one thread), warp 2 (bf16) or warp 20 (FP8);
+//           in a dense bf16 call warp 2 first works out the split schedule
+//           and the pair's unit (schedule.cuh)
 //   warps 4-7 and 12-15 (16-19 with a converter)  softmax: two threads per
 //              head h <-> TMEM lane h, each half of the tile's positions;
 //              online softmax (lazy rescale), P, epilogue
