@@ -883,31 +883,38 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       // O half (128 heads x 256 fp32) -> workspace, normalised by the head's
       // l (the sum of the pair's halves).  With the last PV complete, every
       // stage, P and exchange buffer is idle (the peer sent its last partial
-      // before this CTA's last softmax step), so the whole half is staged at
-      // once as 8 swizzled blocks of 32 columns (4 per thread of the pair)
-      // and leaves as 8 TMA stores.
+      // before this CTA's last softmax step), so the half is staged as 8
+      // swizzled blocks of 32 columns, in four rounds of one block per thread
+      // of the pair: the TMA stores of the blocks a round completes leave
+      // while the next round is staged.
       // A sequence's only unit writes the final bf16 output (4 blocks of 64
-      // columns) and log-sum-exp itself.
+      // columns: two 32-column chunks each, complete after rounds 1 and 3)
+      // and log-sum-exp itself.
       bars->l_half[sh * 128 + h] = l;
       softmax_sync();
       const float lt = bars->l_half[h] + bars->l_half[128 + h];
       const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      if (u.flags & kUnitDirect)
-        stage_output_bf16(lane_base, sm, h, inv, 4 * sh, 4 * sh + 4);
-      else
-        stage_output(lane_base, sm, h, inv, 4 * sh, 4 * sh + 4);
-      fence_async_smem();
-      softmax_sync();
-      if (sh == 0 && h == 0) {
-        if (u.flags & kUnitDirect) {
-          for (int c = 0; c < kHalf / 64; ++c)
+      const bool direct = (u.flags & kUnitDirect) != 0;
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        if (direct)
+          stage_output_bf16(lane_base, sm, h, inv, 4 * sh + q, 4 * sh + q + 1);
+        else
+          stage_output(lane_base, sm, h, inv, 4 * sh + q, 4 * sh + q + 1);
+        fence_async_smem();
+        softmax_sync();
+        if (sh == 0 && h == 0) {
+          if (!direct) {
+            tma3_store(&tp.m_po, rank * kHalf + 32 * q, 0, unit_id, sm + q * kSwBlk);
+            tma3_store(&tp.m_po, rank * kHalf + 32 * (4 + q), 0, unit_id, sm + (4 + q) * kSwBlk);
+          } else if (q & 1) {
+            const int c = q >> 1;
             tma3_store(&tp.m_out, rank * kHalf + 64 * c, 0, u.b, sm + c * kSwBlk);
-        } else {
-          for (int c = 0; c < kHalf / 32; ++c)
-            tma3_store(&tp.m_po, rank * kHalf + 32 * c, 0, unit_id, sm + c * kSwBlk);
+            tma3_store(&tp.m_out, rank * kHalf + 64 * (2 + c), 0, u.b, sm + (2 + c) * kSwBlk);
+          }
         }
-        bulk_commit();
       }
+      if (sh == 0 && h == 0) bulk_commit();
       if (rank == 0 && sh == 0) {
         const float lse = (ok && lt > 0.f) ? (m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
         if (!(u.flags & kUnitDirect))
