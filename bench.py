@@ -1,14 +1,15 @@
 """Benchmark of the MLA latent-cache decode step on GB300.
 
 One step = the cache-write of this step's new row (row end_pos-1 of every
-sequence) followed by the absorbed decode over positions 0..end_pos-1 -- or,
-for the sparse workload, the fused append + top-k gather decode.  Inputs are
+sequence) followed by the absorbed decode over positions 0..end_pos-1, in one
+call (mla_decode_append; the sparse workload: mla_decode_sparse with its new
+rows; multi-token workloads: their new rows appended, then mla_decode_mtp).  Inputs are
 seeded synthetic tensors of the workload's shapes, resident in HBM before the
 timed region.  The timed region is one CUDA-graph launch holding exactly K
 steps; successive steps rotate over cache copies (or top-k lists) so that each
 step's working set is not served from L2.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..6]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..8]
     python bench.py --impl reference ...     # the CPU oracle, same metric
 
 Prints one JSON line (rank 0).  Under torchrun every rank runs its own
