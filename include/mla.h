@@ -85,8 +85,9 @@ typedef struct {
   void* pe;
 } mla_cache;
 
-/* Bit flags of the device status word (OR-ed, sticky until the workspace is
- * cleared by the next mla_decode / mla_decode_sparse call). */
+/* Bit flags of the device status word (OR-ed; each decode call on the
+ * workspace -- mla_decode, mla_decode_append, mla_decode_mtp,
+ * mla_decode_sparse -- writes the word afresh, then adds its own flags). */
 #define MLA_DEV_END_POS_CLAMPED   0x1u  /* an end_pos was < 0 or > max_end_pos  */
 #define MLA_DEV_APPEND_SKIPPED    0x2u  /* fused append: end_pos-1 out of range */
 #define MLA_DEV_PIPELINE_TIMEOUT  0x4u  /* a bounded wait in a kernel gave up   */

@@ -117,8 +117,8 @@ mla_status mla_decode_noalloc(const mla_cache* c, const void* q_latent, const vo
   p.mtp_s = 1;
 
   const bool tc = mla::decode_tc_supported(H);
-  // the schedule kernel clears the status word, the only region read before
-  // it is written
+  // the schedule kernel writes the status word afresh; every other region
+  // is written before it is read
   cudaError_t e = mla::launch_schedule(
       end_pos, max_end_pos, ws, B,
       tc ? mla::decode_tc_units(mla::decode_fmt(c->fmt), false, sms) : mla::target_units_mma(H, sms),
