@@ -64,7 +64,7 @@ def decode_path(H: int) -> str:
 def kernel_source_hash(kernel: str) -> str:
     h = hashlib.sha256()
     src = "decode_tc.cu" if kernel == "decode_tc_kernel" else "decode_mma.cu"
-    for name in (src, "common.cuh", "tc_ptx.cuh"):
+    for name in (src, "common.cuh", "tc_ptx.cuh", "append_row.cuh", "schedule.cuh"):
         with open(os.path.join(ROOT, "mla_latent_kv_07_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
