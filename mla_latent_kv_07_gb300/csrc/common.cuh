@@ -39,8 +39,10 @@ struct Workspace {
   uint32_t* status;   // device status word (MLA_DEV_* bits)
   int* n_units;       // units actually scheduled
   int2* seq;          // [B] (first unit, unit count; -1: written by the decode)
-  int* lengths;       // [B] clamped end_pos (dense) or gather count (sparse)
-  Unit* units;        // [max_units]
+  int* lengths;       // [B] clamped end_pos (dense) or gather count (sparse);
+                      // not written when the decode computes its schedule
+  Unit* units;        // [max_units] written by the schedule kernel (a decode
+                      // that computes its schedule keeps its unit on chip)
   float* part_lse;    // [max_units, H]
   float* part_o;      // [max_units, H, 512]
   int* gidx;          // [B, K] sorted unique gather lists (sparse only)
