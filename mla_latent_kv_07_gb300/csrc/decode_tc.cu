@@ -139,6 +139,9 @@ struct Cfg {
   static constexpr int kRawPe = (kFmt == 1 && !kSparse) ? kPeHalf * 2 : 128;
   static constexpr int kRaw = kConv ? kN * kRawRow + kScBytes + kN * kRawPe : 0;
   static constexpr int kRawSlots = kConv ? (kFmt == 1 && !kSparse ? 3 : 2) : 0;
+  // the converter's ring length in index arithmetic (never zero, so the
+  // converter code of the variants without one compiles cleanly)
+  static constexpr int kRawRing = kRawSlots > 0 ? kRawSlots : 1;
   static constexpr int kRawOff = kStages * kStage;
   static constexpr int kPOff = kRawOff + kRawSlots * kRaw;
   static constexpr int kXOff = kPOff + kPBufs * kPBytes;
@@ -930,10 +933,10 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     // PV of the stage's previous tile is done; kConvWarps warps share a tile
     const int t = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 384 + 64;
     for (int i = 0; i < ntiles; ++i) {
-      const int r = i % C::kRawSlots, j = i % C::kStages;
+      const int r = i % C::kRawRing, j = i % C::kStages;
       // FP8: stages 1-3 hold the staged query until it is in tensor memory
       if (kFmt == 1 && i == 1 && !wt.wait(&bars->qready, 0)) break;
-      if (!wt.wait(&bars->full[r], (i / C::kRawSlots) & 1)) break;
+      if (!wt.wait(&bars->full[r], (i / C::kRawRing) & 1)) break;
       if (!wt.wait(&bars->empty[j], ((i / C::kStages) & 1) ^ 1)) break;
       const int valid = min(kN, u.t1 - (u.t0 + i * kN));
       uint8_t* dst = opl(j);
