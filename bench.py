@@ -44,14 +44,33 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 
 # ----------------------------------------------------------------- helpers
 
-def peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+def peaks(path: str | None = None):
+    """Roofline denominators: each one the measured figure from
+    MEASURED_PEAKS.json when the file gives it (a number, or an object with a
+    "value"), else the fallback.  Returns (peaks, "measured" | "fallback" |
+    "measured and fallback")."""
+    path = path or os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             p = json.load(f)
-        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
-    except Exception:
-        return dict(FALLBACK_PEAKS), "fallback"
+    except (OSError, ValueError):
+        p = {}
+    out, got = {}, set()
+    for k, fb in FALLBACK_PEAKS.items():
+        v = p.get(k) if isinstance(p, dict) else None
+        if isinstance(v, dict):
+            v = v.get("value")
+        try:
+            v = float(v)
+        except (TypeError, ValueError):
+            v = None
+        if v is not None and v > 0 and math.isfinite(v):
+            out[k] = v
+            got.add(k)
+        else:
+            out[k] = fb
+    src = "measured" if len(got) == len(FALLBACK_PEAKS) else ("fallback" if not got else "measured and fallback")
+    return out, src
 
 
 def decode_path(H: int) -> str:

@@ -67,3 +67,25 @@ def test_e2e_packing_round_trips_and_aligns():
         v.copy_(named[k])
     for k, v in bench._views(buf.clone(), offs, named).items():
         assert v.dtype == named[k].dtype and v.shape == named[k].shape and torch.equal(v, named[k])
+
+
+def test_roofline_peaks_from_the_measured_file(tmp_path):
+    # each denominator is the measured one when the file gives it, else the fallback
+    import json as _json
+    import bench
+    fb = bench.FALLBACK_PEAKS
+    missing = tmp_path / "none.json"
+    assert bench.peaks(str(missing)) == (fb, "fallback")
+    full = tmp_path / "full.json"
+    full.write_text(_json.dumps({"hbm_gbs": 7400.5, "bf16_tflops": {"value": 2100}, "bf16_tflops_sustained": 1800,
+                                 "clocks": {"sm": 2070}}))
+    assert bench.peaks(str(full)) == ({"hbm_gbs": 7400.5, "bf16_tflops": 2100.0, "bf16_tflops_sustained": 1800.0},
+                                      "measured")
+    part = tmp_path / "part.json"
+    part.write_text(_json.dumps({"hbm_gbs": 7000, "bf16_tflops": "n/a"}))
+    pk, src = bench.peaks(str(part))
+    assert src == "measured and fallback" and pk["hbm_gbs"] == 7000.0
+    assert pk["bf16_tflops"] == fb["bf16_tflops"] and pk["bf16_tflops_sustained"] == fb["bf16_tflops_sustained"]
+    bad = tmp_path / "bad.json"
+    bad.write_text("{not json")
+    assert bench.peaks(str(bad)) == (fb, "fallback")
