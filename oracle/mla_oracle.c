@@ -390,3 +390,13 @@ int orc_num_threads(void) {
   return 1;
 #endif
 }
+
+/* Threads of the OpenMP loops that follow (timing only; results do not
+ * depend on it). */
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+  if (n > 0) omp_set_num_threads(n);
+#else
+  (void)n;
+#endif
+}

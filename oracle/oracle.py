@@ -65,6 +65,7 @@ def _load():
             lib.orc_decode_naive.argtypes = [I32, I64, P, P, P, P, P, P, I32, I32, P, D, P, P]
             lib.orc_decode_naive.restype = I32
             lib.orc_num_threads.restype = I32
+            lib.orc_set_num_threads.argtypes = [I32]
             _lib = lib
     return _lib
 
@@ -81,6 +82,11 @@ def _c(a, dtype):
 
 def num_threads() -> int:
     return int(_load().orc_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads of the oracle's OpenMP loops from here on (timing only)."""
+    _load().orc_set_num_threads(int(n))
 
 
 def e4m3_encode(y) -> np.ndarray:
