@@ -259,7 +259,8 @@ mla_status mla_decode(const mla_cache* cache, const void* q_latent, const void* 
   mla::Workspace ws;
   mla_status st = check_decode(a, 0, &ws);
   if (st != MLA_OK) return st;
-  // the schedule kernel, first of the dense call, writes the status word afresh
+  // the call's first kernel (the schedule kernel, or a decode kernel that
+  // computes its own schedule) writes the status word afresh
   return run_decode(a, ws, 0, static_cast<cudaStream_t>(stream));
 }
 
