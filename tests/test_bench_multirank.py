@@ -89,3 +89,22 @@ def test_roofline_peaks_from_the_measured_file(tmp_path):
     bad = tmp_path / "bad.json"
     bad.write_text("{not json")
     assert bench.peaks(str(bad)) == (fb, "fallback")
+
+
+def test_reference_arm_prints_one_json_line():
+    # the oracle timed on the host cores, on the tiny workload: one JSON line
+    # with the contract's keys (the arm runs without a GPU)
+    import json as _json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload", "1",
+                          "--steps", "1", "--warmup", "1"], capture_output=True, text=True, timeout=600, cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.strip()]
+    assert len(lines) == 1
+    d = _json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "TB/s" and d["value"] > 0
+    assert d["higher_is_better"] is True and d["config"]["workload"] == "tiny_b1_h16_t256_bf16"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
