@@ -37,7 +37,11 @@ sys.path.insert(0, ROOT)
 import mla_latent_kv_07_gb300 as mla  # noqa: E402
 from mla_latent_kv_07_gb300 import inputs, layout  # noqa: E402
 
-DEFAULT_WORKLOAD = 2
+# the long-context FP8 decode: the largest configuration and the one whose
+# target is a fraction of the HBM bandwidth
+DEFAULT_WORKLOAD = 4
+SOAK_SECONDS = 3.0     # graph replays under load before the timed steps (clock samples)
+CEILING_BYTES = 2 << 30  # one buffer far larger than L2 for the streaming-read ceiling
 METRIC = "MLA decode: cache HBM TB/s (algorithmic cache bytes / step time)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -150,7 +154,7 @@ class ClockSampler:
             except (ValueError, IndexError):
                 continue
         window = [r for r in rows if self.t0 - 0.05 <= r[0] <= self.t1 + 0.05]
-        where = "timed region"
+        where = "load soak + timed region"
         if not window:
             window, where = rows, "around the timed region (region shorter than the sampling period)"
         if not window:
@@ -273,33 +277,45 @@ class Setup:
 PREFILL_MTP = 16     # more new tokens than this: a prefill chunk (no per-step appends)
 PREFILL_SAMPLE = 8   # the oracle times this many of a chunk's tokens and scales to the chunk
 
-def read_ceiling_gbs(st, stream, reps: int = 24):
-    """HBM read rate of the library's streaming read kernel over the same
-    rotated cache tensors the steps read (every pass cold in L2), in GB/s.
-    The passes are captured in a CUDA graph, as the steps are, so the
-    launches run back to back on the device."""
-    sink = torch.zeros(1, dtype=torch.int32, device=st.device)
-    tensors = [[t for t in (c.kv, c.pe, c.kv_scale) if t is not None] for c in st.caches]
-    with torch.cuda.stream(stream):
-        for ts in tensors[:2]:
-            for t in ts:
-                mla.read_ceiling(t, sink, stream=stream)
-    torch.cuda.synchronize()
+def _time_graph(build, stream):
+    """Capture `build()` in a CUDA graph, replay it once to warm up, then time
+    one replay with CUDA events on `stream` (seconds)."""
     graph = torch.cuda.CUDAGraph()
-    nbytes = 0
     with torch.cuda.graph(graph, stream=stream):
-        for i in range(reps):
-            for t in tensors[i % len(tensors)]:
-                mla.read_ceiling(t, sink, stream=stream)
-                nbytes += t.numel() * t.element_size()
+        build()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
+        graph.replay()
         e0.record(stream)
         graph.replay()
         e1.record(stream)
     torch.cuda.synchronize()
-    return nbytes / (e0.elapsed_time(e1) / 1e3) / 1e9, nbytes / reps
+    return e0.elapsed_time(e1) / 1e3
+
+
+def read_ceiling_gbs(st, stream, passes: int = 8):
+    """HBM read rate of the library's streaming read kernel over one buffer of
+    CEILING_BYTES (far larger than L2, so every pass reads from HBM), one launch
+    per pass, `passes` launches in a CUDA graph: the device's achievable
+    streaming read rate, in GB/s.  Also returned: the same kernel over the
+    step's own rotated cache tensors (one launch per tensor), a size-limited
+    rate that includes the launch and ramp of short reads."""
+    sink = torch.zeros(1, dtype=torch.int32, device=st.device)
+    big = torch.empty(CEILING_BYTES, dtype=torch.uint8, device=st.device)
+    big.fill_(1)
+    with torch.cuda.stream(stream):
+        mla.read_ceiling(big, sink, stream=stream)
+    torch.cuda.synchronize()
+    t = _time_graph(lambda: [mla.read_ceiling(big, sink, stream=stream) for _ in range(passes)], stream)
+    ceiling = CEILING_BYTES * passes / t / 1e9
+    del big
+    tensors = [[x for x in (c.kv, c.pe, c.kv_scale) if x is not None] for c in st.caches]
+    reps = 24
+    nbytes = sum(x.numel() * x.element_size() for i in range(reps) for x in tensors[i % len(tensors)])
+    t = _time_graph(lambda: [mla.read_ceiling(x, sink, stream=stream)
+                             for i in range(reps) for x in tensors[i % len(tensors)]], stream)
+    return ceiling, nbytes / t / 1e9, nbytes / reps
 
 
 def run_warm(st, stream, steps: int = 200):
@@ -450,11 +466,30 @@ def run_gpu(args, rank, world, local_rank):
     if sampler:
         sampler.start()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
+    # Load soak: the same K-step graph replayed back to back for about
+    # SOAK_SECONDS right before the timed steps, so the clocks are sampled
+    # under sustained load and the timed steps run in that state.  Its mean
+    # per step is reported as "sustained"; `value` is the timed K steps.
     torch.cuda.synchronize()
     if sampler:
         sampler.mark(True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    one = max(e0.elapsed_time(e1) / 1e3, 1e-6)
+    soak_reps = max(1, min(100000, math.ceil(args.soak / one))) if args.soak > 0 else 1
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(soak_reps):
+            graph.replay()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    soak_s = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
     t_wall = time.perf_counter()
     with torch.cuda.stream(stream):
         e0.record(stream)
@@ -471,7 +506,7 @@ def run_gpu(args, rank, world, local_rank):
         kgraph.replay()
     kern_ms, timed, _ = mla.trace_end()
     clocks = sampler.stop() if sampler else None
-    ceil_gbs, ceil_bytes = read_ceiling_gbs(st, stream)
+    ceil_gbs, same_gbs, same_bytes = read_ceiling_gbs(st, stream)
     ms = slowest(ms, device)
     step_s = ms / 1e3 / K
     cache_bytes = st.tokens * layout.cache_bytes_per_token(w.fmt)
@@ -521,7 +556,8 @@ def run_gpu(args, rank, world, local_rank):
                             "append new row + decode (one call: the decode writes the row)" if w.mtp == 1 else
                             f"append {w.mtp} new rows + multi-token decode (each cache position counted once)"),
                    "l2": f"inputs larger than L2: rotating {st.rotation}; L2 {st.l2_bytes / 1e6:.0f} MB",
-                   "timing": "CUDA graph of exactly K steps, CUDA events on its stream",
+                   "timing": "CUDA graph of exactly K steps, CUDA events on its stream, right after a "
+                          f"{args.soak:g} s load soak of the same graph",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "tokens_per_s": round(tokens_per_s, 1),
         "wall_ms_per_step": round(t_wall * 1e3 / K, 6),
@@ -530,8 +566,17 @@ def run_gpu(args, rank, world, local_rank):
         "gemms": gemms,
         "select": select,
         "read_ceiling": {"gbs": round(ceil_gbs, 1), "kernel": "read_ceiling_kernel",
-                         "bytes_per_pass": int(ceil_bytes),
-                         "sample": "the step's rotated cache tensors, streamed with 16-byte loads"},
+                         "bytes_per_pass": CEILING_BYTES, "frac_of_measured_hbm": round(ceil_gbs / pk["hbm_gbs"], 4),
+                         "sample": f"one {CEILING_BYTES >> 30} GiB buffer (cold in L2) per launch, 8 launches "
+                                   "in a CUDA graph, 16-byte loads",
+                         "same_size_gbs": round(same_gbs, 1), "same_size_bytes_per_pass": int(same_bytes),
+                         "same_size_sample": "the step's own rotated cache tensors, one launch per tensor "
+                                             "(size-limited: includes launch and ramp)"},
+        "sustained": {"seconds": round(soak_s, 3), "steps": soak_reps * K,
+                      "ms_per_step": round(soak_s * 1e3 / (soak_reps * K), 6),
+                      "value": round(whole_job_rate(cache_bytes, world, soak_s / (soak_reps * K)) / 1e12, 4),
+                      "note": "the K-step graph replayed back to back right before the timed steps (clock "
+                              "samples under load); value is the timed K steps"},
         "cpu_baseline": cpu,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -804,6 +849,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--soak", type=float, default=SOAK_SECONDS,
+                    help="seconds of back-to-back graph replays before the timed steps (0: one replay)")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")

@@ -221,10 +221,13 @@ MLA_API mla_status mla_selftest_decode_timeout(const mla_cache* cache, const voi
  * mla_decode_mtp -- absorbed decode of s new tokens per sequence at once
  * (multi-token decode: speculative or multi-token-prediction steps).  The s
  * new rows of cache slot b are its positions end_pos[b]-s .. end_pos[b]-1
- * (already appended); token j attends to positions 0 .. end_pos[b]-s+j, the
- * causal mask among the step's tokens of "DeepSeek-V3.2-Exp . KV cache" (the
- * upper-triangular -inf mask of a step with several tokens).  A token with no
- * position gets out = 0, lse = -inf.
+ * (already appended); token j attends to positions 0 .. end_pos[b]-s+j:
+ * causal among the step's tokens.  That is this library's reading, not a mask
+ * printed on the pages -- the MQA-decode excerpt of "DeepSeek-V3.2-Exp . KV
+ * cache" scores a step's tokens against all of kv_cache[:bsz, :end_pos] with
+ * only the top-k index mask added; causality follows from token-by-token
+ * decoding and from the `mask` argument that excerpt passes to its indexer.
+ * A token with no position gets out = 0, lse = -inf.
  *
  *   q_latent    device bf16 [B, s, H, 512];  q_pe  device bf16 [B, s, H, 64]
  *   end_pos     device int32 [B]

@@ -16,10 +16,10 @@
 //   * QK: each CTA contracts its 288-wide half (Q half as the A operand held in
 //     tensor memory, K half from shared memory) into a partial S; the two
 //     partials are exchanged through distributed shared memory as 24-bit
-//     codes (each fp32 partial rounded to its top 24 bits, by both CTAs
-//     alike; asynchronous remote stores, counted on the receiver's barrier)
-//     and summed.  fp32 addition commutes, so both CTAs hold
-//     bit-identical S and take the same softmax decisions.
+//     codes (each fp32 partial rounded to its top 24 bits; asynchronous
+//     remote stores, counted on the receiver's barrier) and added to the
+//     receiver's own fp32 partial.  Each CTA runs the softmax on its sum and
+//     keeps its own reference maximum and row sums for its output half.
 //   * PV: each CTA multiplies P (shared memory) by its latent half V (the same
 //     shared-memory tile, read as an MN-major operand) into its own O half.
 // Every cache byte is fetched by exactly one CTA and there is no redundant
@@ -181,21 +181,21 @@ __device__ __forceinline__ void pair_sync(int q) {
 }
 // Partial scores cross between the pair as the top 24 bits of the fp32 value,
 // rounded (add half the dropped unit, truncate): relative error at most 2^-16
-// for normal values; both CTAs round their own partial the same way before
-// adding, so the pair still computes bit-identical scores.
-__device__ __forceinline__ float round24(float x) {
-  return __uint_as_float((__float_as_uint(x) + 0x80u) & 0xFFFFFF00u);
-}
-// four fp32 bit patterns -> three words of 24-bit codes
+// for normal values.  Each CTA adds the peer's rounded partial to its own
+// unrounded one, so the two CTAs' scores may differ in the last bits; each CTA
+// keeps its own softmax state (reference maximum, row sums) for its own half
+// of the output, so nothing needs them to agree.
+// four fp32 bit patterns -> three words of 24-bit codes: each value rounded
+// (half the dropped unit added), then its top three bytes taken in order
 __device__ __forceinline__ void pack24(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t& w0,
                                        uint32_t& w1, uint32_t& w2) {
-  a = (a + 0x80u) >> 8;
-  b = (b + 0x80u) >> 8;
-  c = (c + 0x80u) >> 8;
-  d = (d + 0x80u) >> 8;
-  w0 = a | (b << 24);
-  w1 = (b >> 8) | (c << 16);
-  w2 = (c >> 16) | (d << 8);
+  a += 0x80u;
+  b += 0x80u;
+  c += 0x80u;
+  d += 0x80u;
+  w0 = __byte_perm(a, b, 0x5321);   // a1 a2 a3 b1
+  w1 = __byte_perm(b, c, 0x6532);   // b2 b3 c1 c2
+  w2 = __byte_perm(c, d, 0x7653);   // c3 d1 d2 d3
 }
 __device__ __forceinline__ float4 unpack24(uint32_t w0, uint32_t w1, uint32_t w2) {
   return make_float4(__uint_as_float(w0 << 8), __uint_as_float(__funnelshift_r(w0, w1, 24) << 8),
@@ -691,6 +691,22 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     // writes 512 contiguous bytes per store), after releasing the S buffer.
     const int h = threadIdx.x - 256;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    if (kSparse && live) {
+      // idle until the first scores: ask L2 for every row this unit gathers
+      // (this CTA's latent half, the row's scales and its rotary row), so the
+      // producer's gathers of later tiles meet L2 latency instead of DRAM's
+      // (the list is sorted, so rows are read in increasing order)
+      const int* gl = p.ws.gidx + (size_t)u.b * p.K;
+      const size_t base = (size_t)u.b * p.max_seq_len;
+      const uint8_t* kvb = static_cast<const uint8_t*>(p.kv);
+      const uint8_t* peb = static_cast<const uint8_t*>(p.pe);
+      for (int e = u.t0 + C::kN * 2 + h; e < u.t1; e += 128) {
+        const size_t row = base + (size_t)gl[e];
+        prefetch_l2(kvb + row * (kFmt == 1 ? kDc : 2 * kDc) + rank * C::kRawRow, C::kRawRow);
+        if (kFmt == 1) prefetch_l2(p.kv_scale + row * kNblk, 16);
+        if (rank == 0) prefetch_l2(peb + row * (2 * kDr), 2 * kDr);
+      }
+    }
     if (app) {   // idle until the first scores: write the new row first
       append_row(p.ap, u.b, u.t1 - 1, h);
       fence_async_global();
@@ -757,8 +773,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         __syncwarp();
         if (lane == 0) bar_arrive(&bars->sfree[sb_i]);   // QK of tile i + kSBufs may overwrite
       }
-      // + the peer's partial, both rounded to 24 bits (fp32 addition commutes:
-      // both CTAs get the same S).  This half's positions p0..p0+15 are code
+      // + the peer's partial (rounded to 24 bits).  This half's positions p0..p0+15 are code
       // words 12 sh .. 12 sh + 11 (rows 3 sh .. 3 sh + 2), p1..p1+7 words
       // 24 + 6 sh .. 24 + 6 sh + 5 (within rows 6 + sh, 7 + sh).
       const int xb = xsel(i);
@@ -780,9 +795,8 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
             const int t = 3 * (k - 4);
             v = unpack24(sh ? w[14 + t] : w[12 + t], sh ? w[15 + t] : w[13 + t], sh ? w[16 + t] : w[14 + t]);
           }
-          const float2 a = __fadd2_rn(make_float2(round24(sc[4 * k]), round24(sc[4 * k + 1])), make_float2(v.x, v.y));
-          const float2 c2 =
-              __fadd2_rn(make_float2(round24(sc[4 * k + 2]), round24(sc[4 * k + 3])), make_float2(v.z, v.w));
+          const float2 a = __fadd2_rn(make_float2(sc[4 * k], sc[4 * k + 1]), make_float2(v.x, v.y));
+          const float2 c2 = __fadd2_rn(make_float2(sc[4 * k + 2], sc[4 * k + 3]), make_float2(v.z, v.w));
           sc[4 * k] = a.x; sc[4 * k + 1] = a.y; sc[4 * k + 2] = c2.x; sc[4 * k + 3] = c2.y;
         }
         __syncwarp();
@@ -845,7 +859,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         m_ref = m_new;
       }
       // this half of head h's P row (bf16), in the 16-byte chunks p0/8,
-      // p0/8 + 1 and p1/8; l sums the rounded values
+      // p0/8 + 1 and p1/8; l sums the fp32 values before their rounding
       ok = ok && wt.wait(&bars->pfree[b], par ^ 1);
       uint8_t* prow = pbuf(b);
       float2 ls = make_float2(0.f, 0.f);
@@ -856,8 +870,9 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const float2 t = __ffma2_rn(make_float2(sc[8 * c + 2 * k], sc[8 * c + 2 * k + 1]), ps2, nm2);
-          const __nv_bfloat162 two = __floats2bfloat162_rn(ex2_approx(t.x), ex2_approx(t.y));
-          ls = __fadd2_rn(ls, __bfloat1622float2(two));
+          const float2 e = make_float2(ex2_approx(t.x), ex2_approx(t.y));
+          const __nv_bfloat162 two = __float22bfloat162_rn(e);
+          ls = __fadd2_rn(ls, e);
           pk[k] = *reinterpret_cast<const uint32_t*>(&two);
         }
         const int chunk = c < 2 ? p0 / 8 + c : p1 / 8;

@@ -279,6 +279,31 @@ mla_status mla_decode_append(const mla_cache* cache, const void* kv_new, const v
   return run_decode(a, ws, 0, static_cast<cudaStream_t>(stream), 0, -1, &ap);
 }
 
+}  // extern "C"
+
+namespace mla {
+
+// The dense decode of mla_decode with a scratch region supplied by the library
+// itself (mla_noalloc.cu) instead of a caller workspace: the same argument
+// checks (a scratch smaller than this B and H need -> MLA_ERR_WORKSPACE), the
+// same kernels and launch sequence, the same error reporting.
+mla_status decode_in_scratch(const mla_cache* cache, const void* q_latent, const void* q_pe,
+                             const int32_t* end_pos, int32_t max_end_pos, int32_t B, int32_t H,
+                             float softmax_scale, void* out, float* lse, void* scratch,
+                             size_t scratch_bytes, void* stream) {
+  g_last_error[0] = 0;
+  DecodeArgs a{cache, q_latent, q_pe, end_pos, max_end_pos, B, H, softmax_scale, out, lse,
+               scratch, scratch_bytes, 1};
+  mla::Workspace ws;
+  mla_status st = check_decode(a, 0, &ws);
+  if (st != MLA_OK) return st;
+  return run_decode(a, ws, 0, static_cast<cudaStream_t>(stream));
+}
+
+}  // namespace mla
+
+extern "C" {
+
 mla_status mla_topk_select(const float* scores, const int32_t* end_pos, int32_t B, int32_t max_end_pos,
                            int32_t K, int32_t* topk_idx, void* stream) {
   g_last_error[0] = 0;

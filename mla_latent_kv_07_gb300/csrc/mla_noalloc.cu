@@ -31,13 +31,12 @@ constexpr size_t kScratchBytes = size_t(32) << 20;   // 32 MiB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
-
 // Device address of the scratch array on the current device (looked up once
-// per device; host code cannot use the array's name as a device address).
-mla_status scratch_address(void** out, int* sms) {
+// per device, with that device current; host code cannot use the array's name
+// as a device address).
+mla_status scratch_address(void** out) {
   static std::mutex mu;
   static void* addr[64] = {nullptr};
-  static int nsm[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
     cudaGetLastError();
@@ -51,86 +50,34 @@ mla_status scratch_address(void** out, int* sms) {
       cudaGetLastError();
       return MLA_ERR_CUDA;
     }
-    int n = 0;
-    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess || n <= 0) {
-      cudaGetLastError();
-      return MLA_ERR_CUDA;
-    }
     addr[dev] = p;
-    nsm[dev] = n;
   }
   *out = addr[dev];
-  *sms = nsm[dev];
   return MLA_OK;
 }
 
-bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
+
+namespace mla {
+// mla_api.cu: mla_decode's checks and launch sequence over a given scratch
+mla_status decode_in_scratch(const mla_cache* cache, const void* q_latent, const void* q_pe,
+                             const int32_t* end_pos, int32_t max_end_pos, int32_t B, int32_t H,
+                             float softmax_scale, void* out, float* lse, void* scratch,
+                             size_t scratch_bytes, void* stream);
+}  // namespace mla
 
 extern "C" {
 
 mla_status mla_decode_noalloc(const mla_cache* c, const void* q_latent, const void* q_pe,
                               const int32_t* end_pos, int32_t max_end_pos, int32_t B, int32_t H,
                               float softmax_scale, void* out, float* lse, void* stream) {
-  if (!c || !c->kv || !c->pe) return MLA_ERR_INVALID_ARG;
-  if (c->fmt != MLA_KV_BF16 && c->fmt != MLA_KV_FP8_E4M3_B128 && c->fmt != MLA_KV_FP8_E4M3_B128_POW2)
-    return MLA_ERR_UNSUPPORTED;
-  if (c->max_batch <= 0 || c->max_seq_len <= 0) return MLA_ERR_INVALID_ARG;
-  if (!aligned16(c->kv) || !aligned16(c->pe)) return MLA_ERR_INVALID_ARG;
-  if (c->fmt != MLA_KV_BF16 && (!c->kv_scale || !aligned16(c->kv_scale)))
-    return MLA_ERR_INVALID_ARG;
-  if (!(H == 16 || H == 32 || H == 64 || H == 128)) return MLA_ERR_UNSUPPORTED;
-  if (B <= 0 || B > c->max_batch) return MLA_ERR_INVALID_ARG;
-  if (max_end_pos <= 0 || max_end_pos > c->max_seq_len) return MLA_ERR_OUT_OF_RANGE;
-  if (!q_latent || !q_pe || !end_pos || !out) return MLA_ERR_INVALID_ARG;
-  if (!aligned16(q_latent) || !aligned16(q_pe) || !aligned16(out) ||
-      (reinterpret_cast<uintptr_t>(end_pos) & 3u) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
-    return MLA_ERR_INVALID_ARG;
-  if (!(softmax_scale == softmax_scale)) return MLA_ERR_INVALID_ARG;
-
   void* scratch = nullptr;
-  int sms = 0;
-  mla_status st = scratch_address(&scratch, &sms);
+  mla_status st = scratch_address(&scratch);
   if (st != MLA_OK) return st;
-  const mla::Workspace need = mla::carve_workspace(nullptr, B, H, 0, sms);
-  if (need.bytes > kScratchBytes) return MLA_ERR_WORKSPACE;   // the static scratch is too small
-  const mla::Workspace ws = mla::carve_workspace(scratch, B, H, 0, sms);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-
-  mla::DecodeParams p{};
-  p.fmt = mla::decode_fmt(c->fmt);
-  p.max_seq_len = c->max_seq_len;
-  p.kv = c->kv;
-  p.kv_scale = c->kv_scale;
-  p.pe = c->pe;
-  p.q_latent = q_latent;
-  p.q_pe = q_pe;
-  p.B = B;
-  p.H = H;
-  p.scale_log2 = softmax_scale * 1.4426950408889634f;
-  p.out = out;
-  p.lse = lse;
-  p.ws = ws;
-  p.K = 0;
-  p.mtp_s = 1;
-
-  const bool tc = mla::decode_tc_supported(H);
-  // the schedule kernel writes the status word afresh; every other region
-  // is written before it is read
-  cudaError_t e = mla::launch_schedule(
-      end_pos, max_end_pos, ws, B,
-      tc ? mla::decode_tc_units(mla::decode_fmt(c->fmt), false, sms) : mla::target_units_mma(H, sms),
-      tc ? mla::decode_tc_granule(mla::decode_fmt(c->fmt), false) : mla::decode_mma_granule(), tc, 1,
-      false, s);
-  if (e == cudaSuccess) e = tc ? mla::launch_decode_tc(p, s) : mla::launch_decode_mma(p, s);
-  if (e == cudaSuccess) e = mla::launch_combine(ws, B, H, out, lse, s);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return MLA_ERR_CUDA;
-  }
-  return MLA_OK;
+  // the array is 256-byte aligned, as a caller workspace must be; a call whose
+  // B and H need more than kScratchBytes is refused with MLA_ERR_WORKSPACE
+  return mla::decode_in_scratch(c, q_latent, q_pe, end_pos, max_end_pos, B, H, softmax_scale, out, lse,
+                                scratch, kScratchBytes, stream);
 }
 
 }  // extern "C"

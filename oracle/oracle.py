@@ -259,10 +259,13 @@ def decode_absorbed_mtp(cache: dict, q_latent, q_pe, end_pos, softmax_scale: flo
     """fp64 absorbed decode of s new tokens per sequence (multi-token decode).
 
     q_latent [B, s, H, 512], q_pe [B, s, H, 64].  The s new tokens of sequence
-    b sit at positions end_pos[b]-s .. end_pos[b]-1; token j attends, as the
-    causal mask of "DeepSeek-V3.2-Exp . KV cache" (the upper-triangular -inf
-    mask over the current step's tokens) prescribes, to the cache positions up
-    to and including its own: 0 .. end_pos[b]-s+j.  That is the single-token
+    b sit at positions end_pos[b]-s .. end_pos[b]-1; token j attends to the
+    cache positions up to and including its own: 0 .. end_pos[b]-s+j.  This
+    causal reading is not printed on the pages: the MQA-decode excerpt of
+    "DeepSeek-V3.2-Exp . KV cache" scores every token of the step against all
+    of kv_cache[:bsz, :end_pos] and adds only the top-k index mask; the reading
+    follows from decoding token by token (a token never sees later ones) and
+    from the `mask` argument that excerpt hands to its indexer.  That is the single-token
     decode with end_pos[b] - (s-1-j) (a token with no position attends to
     nothing: out 0, lse -inf).  Returns (out [B, s, H, 512], lse [B, s, H]);
     with ``token`` = j, only token j, for the (b, h) ``pairs`` (default all):

@@ -74,9 +74,14 @@ def check_close(got: np.ndarray, ref: np.ndarray, what: str):
 
 
 def sample_pairs(B: int, H: int, per_seq: int, seed: int) -> np.ndarray:
+    """(b, h) output pairs to check at full size: for every sequence the first
+    and last heads (0 and H - 1) plus `per_seq` further heads drawn uniformly
+    without replacement from 1 .. H - 2 (all of them when fewer remain)."""
     rng = np.random.default_rng(seed)
     pairs = []
+    inner = np.arange(1, H - 1)
     for b in range(B):
-        hs = {0, H - 1} | set(rng.choice(H, size=min(H, per_seq), replace=False).tolist())
-        pairs += [(b, h) for h in sorted(hs)[:max(per_seq, 2)]]
+        pick = rng.choice(inner, size=min(per_seq, inner.size), replace=False) if inner.size else []
+        hs = sorted({0, H - 1} | {int(h) for h in pick})
+        pairs += [(b, h) for h in hs]
     return np.array(pairs, np.int32)

@@ -472,7 +472,7 @@ def test_workload2_v3_decode():
 
 
 def test_workload3_serving_variable_lengths():
-    _run_dense_workload(inputs.WORKLOADS[3], 2)
+    _run_dense_workload(inputs.WORKLOADS[3], 8)
 
 
 def test_workload4_long_context():

@@ -38,7 +38,11 @@ def _built():
     mla.lib()
 
 
-@pytest.mark.parametrize("fmt,H,ends,S", [(1, 128, [700, 33, 1], 768), (0, 16, [256, 100], 256)])
+SCRATCH_BYTES = 32 << 20   # the library's static scratch (include/mla.h)
+
+
+@pytest.mark.parametrize("fmt,H,ends,S", [(1, 128, [700, 33, 1], 768), (0, 16, [256, 100], 256),
+                                          (0, 128, [520, 1, 97, 300], 640)])
 def test_noalloc_matches_workspace_decode_twice(fmt, H, ends, S):
     B = len(ends)
     kv = inputs.randn_bf16((B, S, 512), 7001 + H).cuda()
@@ -73,4 +77,26 @@ def test_noalloc_refuses_batches_beyond_its_scratch():
     end_pos = torch.ones((B,), dtype=torch.int32, device="cuda")
     with pytest.raises(mla.MLAError) as e:
         mla.decode_noalloc(cache, ql, qp, end_pos, S, 0.1)
+    assert e.value.code == 4
+
+
+def test_noalloc_limit_at_128_heads():
+    # the largest batch whose scratch need fits the array runs and matches the
+    # workspace decode; one more sequence is refused with MLA_ERR_WORKSPACE
+    H, S = 128, 64
+    fits = max(b for b in range(1, 512) if mla.workspace_size(b, H, S) <= SCRATCH_BYTES)
+    assert mla.workspace_size(fits + 1, H, S) > SCRATCH_BYTES
+    kv = inputs.randn_bf16((fits + 1, S, 512), 7101).cuda()
+    pe = inputs.randn_bf16((fits + 1, S, 64), 7102).cuda()
+    cache = mla.Cache(fits + 1, S, 0, kv=kv, pe=pe)
+    ql = inputs.randn_bf16((fits + 1, H, 512), 7103).cuda()
+    qp = inputs.randn_bf16((fits + 1, H, 64), 7104).cuda()
+    end_pos = torch.arange(1, fits + 2, dtype=torch.int32).remainder(S).add(1).cuda()
+    ref_out, ref_lse = mla.decode(cache, ql[:fits], qp[:fits], end_pos[:fits], S, 0.1352)
+    out, lse = mla.decode_noalloc(cache, ql[:fits], qp[:fits], end_pos[:fits], S, 0.1352)
+    torch.cuda.synchronize()
+    _close(out, ref_out, "out at the limit")
+    _close(lse, ref_lse, "lse at the limit")
+    with pytest.raises(mla.MLAError) as e:
+        mla.decode_noalloc(cache, ql, qp, end_pos, S, 0.1352)
     assert e.value.code == 4
