@@ -691,22 +691,6 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     // writes 512 contiguous bytes per store), after releasing the S buffer.
     const int h = threadIdx.x - 256;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    if (kSparse && live) {
-      // idle until the first scores: ask L2 for every row this unit gathers
-      // (this CTA's latent half, the row's scales and its rotary row), so the
-      // producer's gathers of later tiles meet L2 latency instead of DRAM's
-      // (the list is sorted, so rows are read in increasing order)
-      const int* gl = p.ws.gidx + (size_t)u.b * p.K;
-      const size_t base = (size_t)u.b * p.max_seq_len;
-      const uint8_t* kvb = static_cast<const uint8_t*>(p.kv);
-      const uint8_t* peb = static_cast<const uint8_t*>(p.pe);
-      for (int e = u.t0 + C::kN * 2 + h; e < u.t1; e += 128) {
-        const size_t row = base + (size_t)gl[e];
-        prefetch_l2(kvb + row * (kFmt == 1 ? kDc : 2 * kDc) + rank * C::kRawRow, C::kRawRow);
-        if (kFmt == 1) prefetch_l2(p.kv_scale + row * kNblk, 16);
-        if (rank == 0) prefetch_l2(peb + row * (2 * kDr), 2 * kDr);
-      }
-    }
     if (app) {   // idle until the first scores: write the new row first
       append_row(p.ap, u.b, u.t1 - 1, h);
       fence_async_global();
