@@ -12,44 +12,47 @@
 // Why a pair: an fp32 accumulator for 128 heads x 512 latent columns fills all
 // of one SM's tensor memory (512 columns x 128 lanes x 4 B), leaving no room
 // for the scores.  So CTA r of the pair owns latent columns [256r, 256r+256)
-// and rotary columns [32r, 32r+32):
+// and rotary columns [32r, 32r+32) of the cache and of O, and heads
+// [64r, 64r+64) of the softmax:
 //   * QK: each CTA contracts its 288-wide half (Q half as the A operand held in
-//     tensor memory, K half from shared memory) into a partial S; the two
-//     partials are exchanged through distributed shared memory as 24-bit
-//     codes (each fp32 partial rounded to its top 24 bits; asynchronous
-//     remote stores, counted on the receiver's barrier) and added to the
-//     receiver's own fp32 partial.  Each CTA runs the softmax on its sum and
-//     keeps its own reference maximum and row sums for its output half.
-//   * PV: each CTA multiplies P (shared memory) by its latent half V (the same
-//     shared-memory tile, read as an MN-major operand) into its own O half.
+//     tensor memory, K half from shared memory) into a partial S for all 128
+//     heads.  The partial rows of the peer's 64 heads go to the peer through
+//     distributed shared memory as 24-bit codes (each fp32 partial rounded to
+//     its top 24 bits; asynchronous remote stores, counted on the receiver's
+//     barrier), where they are added to the peer's own fp32 partial.
+//   * softmax: each CTA runs the online softmax of its own 64 heads only and
+//     writes their bf16 P rows into its own P buffer and, by asynchronous
+//     remote stores, into the peer's, with each head's rescale factor.
+//   * PV: each CTA multiplies P of all 128 heads (shared memory) by its latent
+//     half V (the same shared-memory tile, read as an MN-major operand) into
+//     its own O half.  When the owner of a head raised the head's reference
+//     maximum, the other CTA scales its row of that head first.
 // Every cache byte is fetched by exactly one CTA and there is no redundant
-// tensor-core work.
+// tensor-core or softmax work.
 //
 // Tensor memory (512 columns): O half [0,256) fp32; Q half [256,400) bf16 (2
 // per column); S double buffer [400,448) and [448,496) fp32.
 //
-// Warp roles (512 threads; 672 with a converter, 640 for gathers):
+// Warp roles (512 threads; 608 with a converter):
 //   warp 0  producer: TMA tiles (dense) or four-row TMA gathers (gather)
-//   warp 1  MMA issuer (one thread; of QK only in the dense variants) and
-//           tensor-memory owner
-//   dense variants: PV issuer (one thread), warp 2 (bf16) or warp 20 (FP8);
-//           in a dense bf16 call warp 2 first works out the split schedule
-//           and the pair's unit (schedule.cuh)
-//   warps 4-7 and 12-15 (16-19 with a converter)  softmax: two threads per
-//              head h <-> TMEM lane h, each half of the tile's positions;
-//              online softmax (lazy rescale), P, epilogue
-//   warps 8-11 exchange: partial S of each tile from TMEM -> peer (DSMEM),
-//              as soon as it is computed.  (A dense call with new rows: in
-//              the unit that reads the new row they first write it to the
-//              cache -- the cache-write step -- before the producer loads
-//              the unit's last tile.)  Distributed shared memory moves
-//              ~20-35 GB/s per SM with ~0.3 us latency on this part (its
-//              delivery is on the tile's critical path), so sending runs as
-//              its own pipeline stage, ahead of the softmax; the softmax adds
-//              the peer's partial when it reads its own.
-//   warps 2-3 and 12-15 converter (FP8 caches and gathers): raw rows -> bf16
-//              operand tile bf16(fp32(e4m3 * scale)) in the 128-byte
-//              swizzled layout
+//   warp 1  QK issuer (one thread) and tensor-memory owner
+//   warp 2  PV issuer (one thread); in a dense bf16 call it first works out
+//           the split schedule and the pair's unit (schedule.cuh)
+//   warps 4-15  the head pool, three warps per TMEM lane quadrant (a warp may
+//           access lanes 32 (warp & 3) .. + 31 only).  In the CTA's own
+//           quadrants: softmax, three threads per head, 16 positions of each
+//           tile each (with new rows in a dense call, slots 1-2 first write
+//           the row: the cache-write step).  In the peer's quadrants: slot 0
+//           sends the peer's heads' partial scores (in a gather call it first
+//           asks L2 for the unit's rows), slot 1 rescales the peer's heads'
+//           rows of O on request, slot 2 converts (if any).  Slots 0-1 of all
+//           four quadrants stage the output half in the epilogue.
+//   warps 3, 16-18 and the pool's slot-2 warps of the peer's quadrants
+//           converter (FP8 caches and gathers): raw rows -> bf16 operand tile
+//           bf16(fp32(e4m3 * scale)) in the 128-byte swizzled layout
+// Distributed shared memory moves ~20-35 GB/s per SM with ~0.3 us latency on
+// this part, so each tile sends 9 KB of partial scores and 6.3 KB of P rows
+// per direction.
 //
 // Every wait is bounded; on expiry the kernel raises a status bit, stops
 // issuing work, and still runs its teardown (cluster barrier, TMEM release).
@@ -74,10 +77,13 @@ using namespace ptx;
 
 constexpr int kHalf = kDc / 2;             // 256 latent columns per CTA
 constexpr int kPeHalf = kDr / 2;           // 32 rotary columns per CTA
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: p <= 2^8 between rescales
+// log2 units: p <= 2^16 between rescales (bf16 P and the fp32 sums hold that
+// with a wide margin); a larger threshold means fewer rescales, each of
+// which also holds up the peer's PV for its rows of the head
+constexpr float kRescaleThreshold = 16.0f;
 constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemS = 400;
 constexpr long kSpinLimit = 1L << 26;   // polls (~seconds) before giving up
-constexpr int kConvWarps = 6;             // converter: warps 2-3 and 12-15
+constexpr int kConvWarps = 6;             // converter: warps 3, 16-18 and two pool warps
 
 // Shared-memory plan per variant.  Tiles are 48 positions (MMA N for QK, K
 // for PV), with two S, P and exchange buffers.  An operand stage holds the
@@ -97,36 +103,37 @@ struct Cfg {
   // softmax writes P of tile i once PV of tile i-3 is done -- PV of tile i-2
   // runs behind the QK of tile i in the in-order tensor pipe
   static constexpr int kPBufs = kFmt == 0 ? 3 : 2;
-  // exchange buffers: two, except with FP8 caches, whose fourth operand stage
-  // takes the room of the second (the softmax reads a tile's exchange buffer
-  // well before the peer's partial of the next tile is due)
-  static constexpr int kXBufs = kFmt == 1 ? 1 : 2;
-  // warps: 0 producer, 1 MMA, 4-7 softmax (first half), 8-11 exchange,
-  // 12-15 converter (if any), then 4 warps of the softmax's second half
-  static constexpr int kHiWarp = kConv ? 16 : 12;
+  static constexpr int kXBufs = 2;   // exchange buffers
+  // Warps: 0 producer, 1 QK issuer, 2 PV issuer (a dense bf16 call's split
+  // schedule first), 3 converter; 4-15 the head pool, three warps per TMEM
+  // lane quadrant (quadrant = warp & 3, slot = (warp - 4) >> 2); 16-18
+  // converter.  Variants without a converter stop at warp 15.
+  static constexpr int kSmWarps = 6;   // softmax warps: the pool's warps in the CTA's own quadrants
+  static constexpr int kThreads = 32 * (kConv ? 19 : 16);
   // QK may be issued at most this many tiles past the last issued PV: enough
   // run-ahead to keep the tensor pipe busy through the exchange and softmax
   // of a tile, no more -- the pipe runs its queue in order, so each queued QK
-  // delays the PV behind it (measured: 2 starves the pipe, 3 is best).
+  // delays the PV behind it.
   static constexpr int kQkAhead = 3;
-  // Dense variants issue PV from a thread of its own (warp 2, idle without a
-  // converter; with one, a warp of its own after the softmax's second half),
-  // so a PV whose P is ready never waits behind the issue of a QK (which
-  // blocks on the tensor pipe's queue for about as long as it runs).  The
-  // gather variants keep one issuer: the extra warp costs them registers.
-  static constexpr bool kSplitIssue = !kSparse;
-  static constexpr int kPvWarp = kConv ? kHiWarp + 4 : 2;
-  static constexpr int kThreads = 32 * (kHiWarp + 4 + (kConv && kSplitIssue ? 1 : 0));
   static constexpr int kBlkBytes = kN * 128;       // one 64-column swizzled block of a tile
   static constexpr int kOplBytes = 4 * kBlkBytes;  // latent half operand
   static constexpr int kOpeBytes = kBlkBytes;      // rotary operand (full 64 columns)
-  static constexpr int kPBytes = ((kN + 63) / 64) * kSwBlk;  // P: 128 heads x kN bf16, swizzled
-  // exchange buffer: a head's kN partial scores as 24-bit codes (the fp32
-  // value rounded to its top 24 bits), four positions in three words, so
-  // 3 kN / 4 words = kXRows 16-byte rows per head; row q of head h at index
-  // q * 128 + h, so a warp's remote store is one contiguous 512-byte run
+  // P: 128 heads x kN bf16, swizzled (rows of 64 positions: chunks 6 and 7 of
+  // a row are padding, which carries the peer's rescale factors and flags)
+  static constexpr int kPBytes = ((kN + 63) / 64) * kSwBlk;
+  static_assert(kN == 48, "P rows keep chunks 6 and 7 free");
+  // exchange buffer: the kN partial scores of each of the peer's 64 heads as
+  // 24-bit codes (the fp32 value rounded to its top 24 bits), four positions
+  // in three words, so 3 kN / 4 words = kXRows 16-byte rows per head; row q
+  // of head h at index q * 64 + (h & 63), so a warp's remote store is one
+  // contiguous 512-byte run.  Buffers are kXStride apart (bf16 variants keep
+  // twice the room: the query is staged across the P and exchange buffers).
   static constexpr int kXRows = 3 * kN / 16;
-  static constexpr int kXBytes = kXRows * 128 * 16;
+  static constexpr int kXBytes = kXRows * 64 * 16;
+  static constexpr int kXStride = kFmt == 1 ? kXBytes : 2 * kXBytes;
+  // bytes of one tile's message of P rows to the peer: 64 rows x kN bf16,
+  // one rescale factor per row, one flag word per quadrant
+  static constexpr uint32_t kPMsgBytes = 64 * kN * 2 + 64 * 4 + 2 * 4;
   static constexpr int kStage = kOplBytes + kOpeBytes;
   static constexpr int kStages = kConv ? (kFmt == 1 ? 4 : 2) : 4;
   static constexpr int kRawRow = kFmt == 1 ? kHalf : kHalf * 2;  // bytes of a raw latent half row
@@ -145,7 +152,7 @@ struct Cfg {
   static constexpr int kRawOff = kStages * kStage;
   static constexpr int kPOff = kRawOff + kRawSlots * kRaw;
   static constexpr int kXOff = kPOff + kPBufs * kPBytes;
-  static constexpr int kBarOff = kXOff + kXBufs * kXBytes;
+  static constexpr int kBarOff = kXOff + kXBufs * kXStride;
   // query staging (5 swizzled blocks): the P and exchange buffers, or with
   // FP8 caches operand stages 1-3, which the converter fills only once the
   // query has moved to tensor memory
@@ -156,7 +163,7 @@ struct Cfg {
   static_assert(kN % 16 == 0 && kTmemS + kSBufs * kN <= 512, "tile width");
   // the output half is staged from offset 0 (8 blocks of 32 fp32 columns)
   static_assert(kFmt == 1 ? (kStages - 1) * kStage >= 5 * kSwBlk
-                          : kPBufs * kPBytes + kXBufs * kXBytes >= 5 * kSwBlk,
+                          : kPBufs * kPBytes + kXBufs * kXStride >= 5 * kSwBlk,
                 "query staging fits");
   static_assert(kQOff % 1024 == 0 && kPOff % 1024 == 0, "1 KB alignment of the query staging");
   static_assert(kBarOff >= 8 * kSwBlk, "output staging fits the idle buffers");
@@ -173,12 +180,15 @@ struct TcParams {
   CUtensorMap m_out;  // final output [B][128][512] bf16 (box 64 x 128, 128-byte swizzle)
 };
 
-// named barrier 1 among the 256 softmax threads; barriers 2..5 between the
-// two softmax warps that serve the same 32 heads
-__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-__device__ __forceinline__ void pair_sync(int q) {
-  asm volatile("bar.sync %0, 64;" ::"r"(2 + q) : "memory");
+// Named barriers: 1 among the 8 epilogue warps (pool slots 0 and 1); 2 + q
+// among the 3 softmax warps of quadrant q; 6 among warps 4-7 after the query
+// staging; 7 among the 12 pool warps before the epilogue.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void quad_sync(int q) {
+  asm volatile("bar.sync %0, 96;" ::"r"(2 + q) : "memory");
 }
+__device__ __forceinline__ void qstage_sync() { asm volatile("bar.sync 6, 128;" ::: "memory"); }
+__device__ __forceinline__ void pool_sync() { asm volatile("bar.sync 7, 384;" ::: "memory"); }
 // Partial scores cross between the pair as the top 24 bits of the fp32 value,
 // rounded (add half the dropped unit, truncate): relative error at most 2^-16
 // for normal values.  Each CTA adds the peer's rounded partial to its own
@@ -218,18 +228,30 @@ struct Bars {
   uint64_t deq[4];     // operand stage converted
   uint64_t empty[4];   // PV done: operand stage free
   uint64_t rfree[3];   // raw slot read by the converter
-  uint64_t sfull[2], sfree[2], pfull[3], pfree[3], xfull[2], xempty[2];
-  uint64_t drain;   // final commit of the MMA issuer (of QK, when PV has its own)
-  uint64_t drain_pv;  // final commit of the PV issuer
+  uint64_t sfull[2], sfree[2];
+  uint64_t pfull[3];   // P rows of this CTA's heads written (its softmax warps)
+  uint64_t pfree[3];   // PV of the buffer's tile done in both CTAs (one multicast commit from each)
+  uint64_t rpfull[3];  // the peer's P rows (with rescale factors and flags) landed
+  uint64_t xfull[2], xempty[2];
+  uint64_t lpeer;      // the peer's row sums of its heads landed (epilogue)
+  uint64_t drain;      // final commit of the QK issuer
+  uint64_t drain_pv;   // final commit of the PV issuer
   volatile int pv_issued;   // PV issuer: tiles whose PV is issued (paces QK)
+  // rescale of the peer's heads' rows of O: the PV issuer posts tile + 1 in
+  // resc_req and waits until both rescaler warps have counted it in resc_done
+  volatile int resc_req;
+  int resc_done;
+  volatile int resc_stop;   // the PV issuer has issued its last PV (or gave up)
   uint64_t qbar;    // query rows staged in shared memory
   uint64_t qready;  // query half in tensor memory
   uint64_t appended;  // the new row is in the cache (dense call with new rows)
   Unit unit;          // this pair's unit, when the kernel computes the schedule
   uint32_t tmem;
   volatile int abort;
-  float pair_max[2][256];   // softmax: tile maxima of the pair's halves, by tile parity
-  float l_half[256];        // epilogue: the pair's halves of l
+  float pm[2][3][64];    // softmax: tile maxima of each own head's three threads, by tile parity
+  float l_part[3][64];   // epilogue: the three threads' row sums of each own head
+  float l_peer[64];      // epilogue: row sums of the peer's heads (sent by the peer)
+  float m_fin[64];       // epilogue: final reference maximum of each own head
 };
 static_assert(sizeof(Bars) <= 4096, "barrier block");
 
@@ -339,13 +361,23 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Waiter wt{bars, p.ws.status, p.spin_limit > 0 ? (long)p.spin_limit : kSpinLimit};
 
+  // the head pool: warp & 3 is the TMEM lane quadrant the warp may access;
+  // this CTA owns heads [64 rank, 64 rank + 64), quadrants 2 rank and 2 rank + 1
+  const int quad = warp & 3;
+  const bool pool = warp >= 4 && warp < 16;
+  const int slot = (warp - 4) >> 2;
+  const bool own_q = (quad >> 1) == (int)rank;
+  const int hq = 32 * quad + lane;   // this lane's head (TMEM lane) in the pool and epilogue
+  // converter warps: 3, 16-18 and the pool's third warp in each of the peer's quadrants
+  const int conv_id = warp == 3 ? 0 : warp >= 16 ? warp - 15 : (pool && !own_q && slot == 2) ? 4 + (quad & 1) : -1;
+
   auto opl = [&](int j) { return sm + j * C::kStage; };               // operand stage j
   auto ope = [&](int j) { return sm + j * C::kStage + kOplBytes; };
   auto raw = [&](int r) { return sm + C::kRawOff + r * C::kRaw; };    // raw slot r
   auto rsc = [&](int r) { return raw(r) + kN * C::kRawRow; };
   auto rpe = [&](int r) { return raw(r) + kN * C::kRawRow + C::kScBytes; };
   auto pbuf = [&](int b) { return sm + C::kPOff + b * C::kPBytes; };
-  auto xbuf = [&](int b) { return reinterpret_cast<float*>(sm + C::kXOff + b * C::kXBytes); };
+  auto xbuf = [&](int b) { return sm + C::kXOff + b * C::kXStride; };
   // tile i uses S buffer ssel(i) and P buffer psel(i); spar(i) / ppar(i) is
   // the parity of the phase that tile completes on that buffer's barriers
   auto ssel = [](int i) { return i % C::kSBufs; };
@@ -364,21 +396,26 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     }
     for (int r = 0; r < C::kRawSlots; ++r) bar_init(&bars->rfree[r], kConvWarps);
     for (int b = 0; b < C::kPBufs; ++b) {
-      bar_init(&bars->pfull[b], 8);
-      bar_init(&bars->pfree[b], 1);
+      bar_init(&bars->pfull[b], C::kSmWarps);
+      bar_init(&bars->pfree[b], 2);    // both CTAs' PV commits
+      bar_init(&bars->rpfull[b], 1);   // one arrival (with the message's bytes) from the peer
     }
     for (int b = 0; b < 2; ++b) {
       bar_init(&bars->sfull[b], 1);
-      bar_init(&bars->sfree[b], 12);   // softmax (8) and exchange (4) warps read S
+      bar_init(&bars->sfree[b], C::kSmWarps + 2);   // softmax warps and the two sender warps read S
       bar_init(&bars->xfull[b], 1);    // one arrival (with the tile's bytes) from the peer
-      bar_init(&bars->xempty[b], 8);   // the peer's softmax warps
+      bar_init(&bars->xempty[b], C::kSmWarps);   // the peer's softmax warps
     }
+    bar_init(&bars->lpeer, 1);
     bar_init(&bars->drain, 1);
     bar_init(&bars->drain_pv, 1);
     bars->pv_issued = 0;
+    bars->resc_req = 0;
+    bars->resc_done = 0;
+    bars->resc_stop = 0;
     bar_init(&bars->qbar, 1);
     bar_init(&bars->qready, 4);
-    bar_init(&bars->appended, 4);   // the exchange warps
+    bar_init(&bars->appended, 4);
     bars->abort = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -398,8 +435,8 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   pdl_wait();
   pdl_trigger();
   const Unit u = [&]() -> Unit {
-    // only the dense bf16 variant computes its schedule (the FP8 variant runs
-    // at its register limit, where this code cost more than it saved)
+    // only the dense bf16 variant computes its schedule (the FP8 variant
+    // keeps the schedule kernel; see the host launcher)
     if constexpr (kSparse || kFmt != 0) {
       return p.ws.units[unit_id];
     } else {
@@ -434,10 +471,10 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
 
   // Q half -> tensor memory (A operand of QK): lane h, 2 bf16 per column.
   // Five TMA boxes stage the 128 rows (4 latent blocks of 64 columns, the 64
-  // rotary columns, 128-byte swizzled) in the P and exchange buffers, which
-  // are idle until the first tile, so the producer starts on the cache at
-  // once.  Each thread then moves its row to its TMEM lane and signals the MMA
-  // issuer, and the peer that its exchange buffers may be written.
+  // rotary columns, 128-byte swizzled) in idle buffers, so the producer starts
+  // on the cache at once.  Each thread of warps 4-7 then moves its row to its
+  // TMEM lane and signals the QK issuer, and the peer that its exchange
+  // buffers may be written (the bf16 variants stage the query in them).
   if (live && warp >= 4 && warp < 8) {
     const int h = threadIdx.x - 128;
     uint8_t* qs = sm + C::kQOff;
@@ -448,6 +485,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       tma3(qs + 4 * kSwBlk, &tp.m_qp, 0, 0, u.b, &bars->qbar);
     }
     wt.drain(&bars->qbar, 0);
+    __syncwarp();   // the tensor-memory stores below are warp-collective
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
 #pragma unroll
     for (int c = 0; c < 9; ++c) {  // 144 columns = 9 x 16 = 36 chunks of 16 bytes
@@ -465,18 +503,13 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     tc_wait_st();
     tc_before();
     __syncwarp();
-    if (lane == 0) {
-      bar_arrive(&bars->qready);
-      // phase 0 of the peer's xempty[0/1]: this CTA's exchange buffers are free
-      bar_arrive_remote(mapa(&bars->xempty[0], peer));
-      bar_arrive_remote(mapa(&bars->xempty[1], peer));
+    if (lane == 0) bar_arrive(&bars->qready);
+    qstage_sync();
+    // phase 0 of the peer's xempty[0/1]: this CTA's exchange buffers are free
+    if (h == 0) {
+      bar_arrive_remote_n(mapa(&bars->xempty[0], peer), C::kSmWarps);
+      bar_arrive_remote_n(mapa(&bars->xempty[1], peer), C::kSmWarps);
     }
-  }
-  // the second-half softmax warps count towards that phase too (it completes
-  // only with the first half's arrivals, after the staged rows were read)
-  if (live && warp >= C::kHiWarp && warp < C::kHiWarp + 4 && lane == 0) {
-    bar_arrive_remote(mapa(&bars->xempty[0], peer));
-    bar_arrive_remote(mapa(&bars->xempty[1], peer));
   }
 
   if (warp == 0) {
@@ -546,16 +579,53 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       for (int i = issued > kSlots ? issued - kSlots : 0; i < issued; ++i)
         if (!(unit_id == 0 && i == p.withhold_tile)) wt.drain(&bars->full[i % kSlots], (i / kSlots) & 1);
     }
-  } else if (C::kSplitIssue && warp == C::kPvWarp) {
+  } else if (warp == 2) {
     // ------------------------------------------------------------ PV issuer
+    // P of tile i: this CTA's heads from its own softmax, the peer's heads
+    // from the peer.  When the peer rescaled some of its heads in this tile,
+    // the rescaler warps first scale those heads' rows of this CTA's O half.
+    // The commit reaches pfree in both CTAs (each P buffer is written by
+    // both), empty only here.
     if (lane == 0) {
       constexpr uint32_t id_pv = idesc(128, kHalf, true);
       const uint64_t d_v0 = sdesc(sa(opl(0)), kBlkBytes, 1024);
       const uint64_t d_p0 = sdesc(sa(pbuf(0)), 16, 1024);
       const uint32_t t_o = tmem + kTmemO;
+      const int pq0 = 2 * (int)peer;   // the peer's first quadrant
+      int nreq = 0;
       for (int i = 0; i < ntiles; ++i) {
         const int j = i % C::kStages, b = psel(i);
         if (!wt.wait(&bars->pfull[b], ppar(i))) break;
+        if (!wt.wait(&bars->rpfull[b], ppar(i))) break;
+        // the peer's rows were written by another CTA's asynchronous stores:
+        // order them before the tensor core reads the buffer
+        fence_async_smem();
+        const uint8_t* pb = pbuf(b);
+        const uint32_t f0 = *reinterpret_cast<const volatile uint32_t*>(pb + swz_chunk(32 * pq0, 7));
+        const uint32_t f1 = *reinterpret_cast<const volatile uint32_t*>(pb + swz_chunk(32 * pq0 + 32, 7));
+        if (f0 | f1) {
+          // the rescalers scale rows of O that PV of tile i - 1 writes
+          if (i > 0 && !wt.wait(&bars->pfree[psel(i - 1)], ppar(i - 1))) break;
+          ++nreq;
+          asm volatile("st.release.cta.shared.b32 [%0], %1;" ::"r"(sa((const void*)&bars->resc_req)), "r"(i + 1)
+                       : "memory");
+          bool done = false;
+          for (long it = 0; it < wt.lim && !bars->abort; ++it) {
+            int d;
+            asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(d) : "r"(sa(&bars->resc_done)) : "memory");
+            if (d >= 2 * nreq) {
+              done = true;
+              break;
+            }
+          }
+          if (!done) {
+            if (!bars->abort) {
+              bars->abort = 1;
+              atomicOr(p.ws.status, kDevTimeout);
+            }
+            break;
+          }
+        }
         tc_after();
         const uint64_t pd = sdesc_at(d_p0, b * C::kPBytes), vd = sdesc_at(d_v0, j * C::kStage);
         if (i == 0)
@@ -565,14 +635,15 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
 #pragma unroll
         for (int kk = 1; kk < kN / 16; ++kk)
           mma_ss_c<true>(t_o, sdesc_at(pd, (kk >> 2) * kSwBlk + (kk & 3) * 32), sdesc_at(vd, 2048 * kk), id_pv);
-        mma_commit(&bars->pfree[b]);
+        mma_commit_mc(&bars->pfree[b], 3);
         mma_commit(&bars->empty[j]);
         bars->pv_issued = i + 1;
       }
+      bars->resc_stop = 1;
       mma_commit(&bars->drain_pv);
       wt.drain(&bars->drain_pv, 0);
     }
-  } else if (C::kSplitIssue && warp == 1) {
+  } else if (warp == 1) {
     // ------------------------------------------------------------ QK issuer
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc(128, kN, false);
@@ -612,90 +683,27 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       mma_commit(&bars->drain);
       wt.drain(&bars->drain, 0);
     }
-  } else if (warp == 1) {
-    // -------------------------------------------------------- MMA issuer
-    // Event-driven: QK of the next tile is issued as soon as its stage, its
-    // converted operand and its S buffer are ready (at most kSBufs tiles ahead
-    // of the softmax); PV of the next tile as soon as its P is written.
-    // Neither waits behind the other's inputs.
-    if (lane == 0) {
-      constexpr uint32_t id_qk = idesc(128, kN, false);
-      constexpr uint32_t id_pv = idesc(128, kHalf, true);
-      // descriptors of stage 0 and P buffer 0; a tile's are these plus
-      // constant offsets (one add per MMA on this thread)
-      const uint64_t d_k0 = sdesc(sa(opl(0)), 16, 1024);          // K-major operand tiles
-      const uint64_t d_v0 = sdesc(sa(opl(0)), kBlkBytes, 1024);   // the latent tile read MN-major (V)
-      const uint64_t d_p0 = sdesc(sa(pbuf(0)), 16, 1024);
-      const uint32_t t_q = tmem + kTmemQ, t_o = tmem + kTmemO;
-      int nq = 0, np = 0;
-      long idle = 0;
-      if (live && wt.wait(&bars->qready, 0)) tc_after();
-      while (np < ntiles && !bars->abort) {
-        bool did = false;
-        // PV first: it is on the critical path (the softmax waits for it), and
-        // issuing the 18 QK instructions takes about as long as running them
-        if (np < nq) {
-          const int i = np, j = i % C::kStages, b = psel(i);
-          if (bar_try(&bars->pfull[b], ppar(i))) {
-            tc_after();
-            const uint64_t pd = sdesc_at(d_p0, b * C::kPBytes), vd = sdesc_at(d_v0, j * C::kStage);
-            if (i == 0)
-              mma_ss_c<false>(t_o, pd, vd, id_pv);
-            else
-              mma_ss_c<true>(t_o, pd, vd, id_pv);
-#pragma unroll
-            for (int kk = 1; kk < kN / 16; ++kk)
-              mma_ss_c<true>(t_o, sdesc_at(pd, (kk >> 2) * kSwBlk + (kk & 3) * 32), sdesc_at(vd, 2048 * kk),
-                             id_pv);
-            mma_commit(&bars->pfree[b]);
-            mma_commit(&bars->empty[j]);
-            ++np;
-            did = true;
-          }
-        }
-        if (nq < ntiles && nq < np + C::kQkAhead) {
-          const int k = nq, j = k % C::kStages, b = ssel(k);
-          const uint32_t use = k / C::kStages;
-          if (bar_try(C::kConv ? &bars->deq[j] : &bars->full[j], use & 1) &&
-              bar_try(&bars->sfree[b], spar(k) ^ 1)) {
-            tc_after();
-            const uint32_t sd = tmem + kTmemS + b * kN;
-            const uint64_t kd = sdesc_at(d_k0, j * C::kStage);
-            const uint64_t ped = sdesc_at(kd, kOplBytes + rank * (kPeHalf * 2));
-            mma_ts_c<false>(sd, t_q, kd, id_qk);
-#pragma unroll
-            for (int kk = 1; kk < kHalf / 16; ++kk)
-              mma_ts_c<true>(sd, t_q + 8 * kk, sdesc_at(kd, (kk >> 2) * kBlkBytes + (kk & 3) * 32), id_qk);
-#pragma unroll
-            for (int kk = 0; kk < kPeHalf / 16; ++kk)
-              mma_ts_c<true>(sd, t_q + kHalf / 2 + 8 * kk, sdesc_at(ped, 32 * kk), id_qk);
-            mma_commit(&bars->sfull[b]);
-            ++nq;
-            did = true;
-          }
-        }
-        if (did) {
-          idle = 0;
-        } else if (++idle > wt.lim) {
-          bars->abort = 1;
-          atomicOr(p.ws.status, kDevTimeout);
-        }
+  } else if (pool && !own_q && slot == 0) {
+    // ------------------------------------------------------------ sender
+    // Partial S of the peer's heads (this warp's quadrant) -> the peer's
+    // exchange buffer, as soon as each tile's scores are computed.
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    const int hl = hq & 63;   // the head's row among the peer's 64
+    if (kSparse && live) {
+      // idle until the first scores: ask L2 for every row this unit gathers
+      // after its first two tiles (this CTA's latent half, the row's scales
+      // and its rotary row), so the producer's gathers of later tiles meet L2
+      // latency instead of DRAM's
+      const int* gl = p.ws.gidx + (size_t)u.b * p.K;
+      const size_t base = (size_t)u.b * p.max_seq_len;
+      const uint8_t* kvb = static_cast<const uint8_t*>(p.kv);
+      const uint8_t* peb = static_cast<const uint8_t*>(p.pe);
+      for (int e = u.t0 + 2 * kN + hl; e < u.t1; e += 64) {
+        const size_t row = base + (size_t)gl[e];
+        prefetch_l2(kvb + row * (kFmt == 1 ? kDc : 2 * kDc) + rank * C::kRawRow, C::kRawRow);
+        if (kFmt == 1) prefetch_l2(p.kv_scale + row * kNblk, 16);
+        if (rank == 0) prefetch_l2(peb + row * (2 * kDr), 2 * kDr);
       }
-      // every MMA issued by this thread completes before tensor memory is freed
-      mma_commit(&bars->drain);
-      wt.drain(&bars->drain, 0);
-    }
-  } else if (warp >= 8 && warp < 12) {
-    // ------------------------------------------------------------ exchange
-    // Send only: partial S of tile i -> the peer's exchange buffer (a warp
-    // writes 512 contiguous bytes per store), after releasing the S buffer.
-    const int h = threadIdx.x - 256;
-    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    if (app) {   // idle until the first scores: write the new row first
-      append_row(p.ap, u.b, u.t1 - 1, h);
-      fence_async_global();
-      __syncwarp();
-      if (lane == 0) bar_arrive(&bars->appended);
     }
     for (int i = 0; i < ntiles; ++i) {
       const int b = ssel(i);
@@ -711,84 +719,125 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       if (lane == 0) bar_arrive(&bars->sfree[b]);
       const int xb = xsel(i);
       if (!wt.wait(&bars->xempty[xb], xpar(i))) break;   // phase 0: the peer's query staging is done
-      const uint32_t xd = mapa(xbuf(xb) + 4 * h, peer), xf = mapa(&bars->xfull[xb], peer);
+      const uint32_t xd = mapa(xbuf(xb) + 16 * hl, peer), xf = mapa(&bars->xfull[xb], peer);
       uint32_t w[C::kXRows * 4];
 #pragma unroll
       for (int g = 0; g < kN / 4; ++g)
         pack24(r[4 * g], r[4 * g + 1], r[4 * g + 2], r[4 * g + 3], w[3 * g], w[3 * g + 1], w[3 * g + 2]);
       // the peer's phase completes on one arrival carrying the tile's bytes
       // and on those bytes landing, in either order
-      if (h == 0) bar_arrive_expect_tx_remote(xf, C::kXBytes);
+      if (hl == 0) bar_arrive_expect_tx_remote(xf, C::kXBytes);
 #pragma unroll
       for (int q = 0; q < C::kXRows; ++q)
-        st_async_v4(xd + 16 * 128 * q, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3], xf);
+        st_async_v4(xd + 16 * 64 * q, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3], xf);
     }
-  } else if ((warp >= 4 && warp < 8) || (warp >= C::kHiWarp && warp < C::kHiWarp + 4)) {
+  } else if (pool && !own_q && slot == 1) {
+    // ------------------------------------------------------------ rescaler
+    // When the peer raises the reference maximum of one of its heads, this
+    // CTA's row of that head in O (its latent half) is scaled by the factor
+    // the peer sent with the tile's P rows, before PV of that tile.  The PV
+    // issuer posts the request once PV of the previous tile is complete.
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    int handled = 0;
+    for (long it = 0; it < wt.lim; ++it) {
+      if (bars->abort) break;
+      int req;
+      asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(req) : "r"(sa((const void*)&bars->resc_req)) : "memory");
+      if (req > handled) {
+        const int i = req - 1;
+        tc_after();
+        const float alpha = *reinterpret_cast<const float*>(pbuf(psel(i)) + swz_chunk(hq, 6));
+        // tensor-memory loads and stores are warp-collective: the whole warp
+        // takes the branch when any of its rows needs scaling (factor 1 for
+        // the others)
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            uint32_t r[16], q[16];
+            TC_LD16(lane_base + kTmemO + 32 * c, r);
+            TC_LD16(lane_base + kTmemO + 32 * c + 16, q);
+            tc_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
+              q[k] = __float_as_uint(__uint_as_float(q[k]) * alpha);
+            }
+            TC_ST16(lane_base + kTmemO + 32 * c, r);
+            TC_ST16(lane_base + kTmemO + 32 * c + 16, q);
+          }
+          tc_wait_st();
+        }
+        tc_before();
+        __syncwarp();
+        if (lane == 0)
+          asm volatile("red.release.cta.shared.add.s32 [%0], 1;" ::"r"(sa(&bars->resc_done)) : "memory");
+        handled = req;
+        it = 0;
+      } else if (bars->resc_stop) {
+        break;
+      }
+    }
+  } else if (pool && own_q) {
     // ------------------------------------------------------------ softmax
-    // Two threads per head h (TMEM lane h): half sh = 0 takes the tile's
-    // positions [0,16) and [32,40), half 1 [16,32) and [40,48) (16- and
-    // 8-column TMEM loads).  The pair agrees on each tile's maximum through
-    // shared memory and a 64-thread barrier, so both take the same rescale
-    // decisions; each rescales and, at the end, normalises half of the O row.
-    const int sh = warp >= 8 ? 1 : 0;
-    const int h = 32 * (warp & 3) + lane;
-    const int p0 = 16 * sh, p1 = 32 + 8 * sh;   // first position of each run
-    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    // Three threads per head h (TMEM lane h, one of this CTA's 64 heads),
+    // thread `slot` taking the tile's positions [16 slot, 16 slot + 16).  The
+    // three agree on each tile's maximum through shared memory and a 96-thread
+    // barrier, so they take the same rescale decisions.  P is written into
+    // this CTA's buffer and, by asynchronous remote stores, into the peer's.
+    const int h = hq, hl = h & 63, s16 = 16 * slot;
+    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const float sl2 = p.scale_log2;
     const bool pos_scale = sl2 > 0.f;
     const float ps = pos_scale ? sl2 : 1.f;   // the factor still to apply to sc in P
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
+    if (app && slot > 0) {   // idle until the first scores: write the new row first
+      append_row(p.ap, u.b, u.t1 - 1, 64 * (slot - 1) + 32 * (quad & 1) + lane);
+      fence_async_global();
+      __syncwarp();
+      if (lane == 0) bar_arrive(&bars->appended);
+    }
     for (int i = 0; i < ntiles; ++i) {
       const int j = i % C::kStages, sb_i = ssel(i), b = psel(i);
       const uint32_t par = ppar(i);
-      float sc[24];
+      float sc[16];
       ok = ok && wt.wait(&bars->sfull[sb_i], spar(i));
       {
         tc_after();
-        const uint32_t sb = lane_base + kTmemS + sb_i * kN;
-        uint32_t r[24];
-        TC_LD16(sb + p0, r);
-        TC_LD8(sb + p1, (r + 16));
+        uint32_t r[16];
+        TC_LD16(lane_base + kTmemS + sb_i * kN + s16, r);
         tc_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 24; ++k) sc[k] = __uint_as_float(r[k]);
+        for (int k = 0; k < 16; ++k) sc[k] = __uint_as_float(r[k]);
         tc_before();
         __syncwarp();
         if (lane == 0) bar_arrive(&bars->sfree[sb_i]);   // QK of tile i + kSBufs may overwrite
       }
-      // + the peer's partial (rounded to 24 bits).  This half's positions p0..p0+15 are code
-      // words 12 sh .. 12 sh + 11 (rows 3 sh .. 3 sh + 2), p1..p1+7 words
-      // 24 + 6 sh .. 24 + 6 sh + 5 (within rows 6 + sh, 7 + sh).
+      // + the peer's partial (rounded to 24 bits): positions s16 .. s16 + 15
+      // are code words 12 slot .. 12 slot + 11, rows 3 slot .. 3 slot + 2
       const int xb = xsel(i);
       ok = ok && wt.wait(&bars->xfull[xb], xpar(i));
       {
-        const uint4* xr = reinterpret_cast<const uint4*>(xbuf(xb)) + h;
-        uint32_t w[20];
+        const uint4* xr = reinterpret_cast<const uint4*>(xbuf(xb)) + hl;
+        uint32_t w[12];
 #pragma unroll
-        for (int q = 0; q < 5; ++q) {
-          const uint4 v = xr[128 * (q < 3 ? 3 * sh + q : 6 + sh + q - 3)];
+        for (int q = 0; q < 3; ++q) {
+          const uint4 v = xr[64 * (3 * slot + q)];
           w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
         }
 #pragma unroll
-        for (int k = 0; k < 6; ++k) {
-          float4 v;
-          if (k < 4) {
-            v = unpack24(w[3 * k], w[3 * k + 1], w[3 * k + 2]);
-          } else {
-            const int t = 3 * (k - 4);
-            v = unpack24(sh ? w[14 + t] : w[12 + t], sh ? w[15 + t] : w[13 + t], sh ? w[16 + t] : w[14 + t]);
-          }
+        for (int k = 0; k < 4; ++k) {
+          const float4 v = unpack24(w[3 * k], w[3 * k + 1], w[3 * k + 2]);
           const float2 a = __fadd2_rn(make_float2(sc[4 * k], sc[4 * k + 1]), make_float2(v.x, v.y));
           const float2 c2 = __fadd2_rn(make_float2(sc[4 * k + 2], sc[4 * k + 3]), make_float2(v.z, v.w));
           sc[4 * k] = a.x; sc[4 * k + 1] = a.y; sc[4 * k + 2] = c2.x; sc[4 * k + 3] = c2.y;
         }
         __syncwarp();
-        // my buffer b may be refilled: the values read above are already in
+        // the buffer may be refilled: the values read above are already in
         // registers, so no release ordering is needed
         if (lane == 0) bar_arrive_remote_relaxed(mapa(&bars->xempty[xb], peer));
       }
-      // masked scores and the tile maximum of the pair.  With a positive
+      // masked scores and the tile maximum of the head.  With a positive
       // scale the scores stay unscaled here: round-to-nearest is monotone, so
       // the maximum of the scaled scores is the scaled maximum, and P below
       // takes scale and reference in one fused multiply-add.  (A scale <= 0
@@ -796,35 +845,35 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       const int valid = min(kN, u.t1 - (u.t0 + i * kN));
       if (!pos_scale) {
 #pragma unroll
-        for (int k = 0; k < 24; ++k) sc[k] *= sl2;
+        for (int k = 0; k < 16; ++k) sc[k] *= sl2;
       }
       if (valid < kN) {   // the unit's last tile
 #pragma unroll
-        for (int k = 0; k < 24; ++k)
-          if ((k < 16 ? p0 + k : p1 + k - 16) >= valid) sc[k] = -INFINITY;
+        for (int k = 0; k < 16; ++k)
+          if (s16 + k >= valid) sc[k] = -INFINITY;
       }
       float mx[4] = {sc[0], sc[1], sc[2], sc[3]};
 #pragma unroll
-      for (int k = 4; k < 24; ++k) mx[k & 3] = fmaxf(mx[k & 3], sc[k]);
-      float* pm = bars->pair_max[i & 1];
+      for (int k = 4; k < 16; ++k) mx[k & 3] = fmaxf(mx[k & 3], sc[k]);
       const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      pm[sh * 128 + h] = pos_scale ? mloc * sl2 : mloc;
-      pair_sync(warp & 3);
-      const float mt = fmaxf(pm[h], pm[128 + h]);
+      bars->pm[i & 1][slot][hl] = pos_scale ? mloc * sl2 : mloc;
+      quad_sync(quad);
+      const float mt = fmaxf(fmaxf(bars->pm[i & 1][0][hl], bars->pm[i & 1][1][hl]), bars->pm[i & 1][2][hl]);
       // lazy rescale of the running reference max
       const bool need = ok && mt > m_ref + kRescaleThreshold;
+      float alpha = 1.f;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? mt : m_ref;
-        const float alpha = exp2f(m_ref - m_new);   // 0 when m_ref = -inf
+        alpha = exp2f(m_ref - m_new);   // 0 when m_ref = -inf
         if (i > 0) {
           // O holds tiles < i: wait for PV of tile i-1 (its P buffer's release;
           // the previous use of that buffer is known complete, so the parity
           // wait cannot be fooled by a phase two steps back), then scale this
-          // thread's half of the lane's row
+          // thread's blocks of the lane's row (3, 3 and 2 of the 8)
           ok = ok && wt.wait(&bars->pfree[psel(i - 1)], ppar(i - 1));
           tc_after();
 #pragma unroll 1
-          for (int c = 4 * sh; c < 4 * sh + 4; ++c) {
+          for (int c = 3 * slot; c < 3 * slot + 3 && c < 8; ++c) {
             uint32_t r[16], q[16];
             TC_LD16(lane_base + kTmemO + 32 * c, r);
             TC_LD16(lane_base + kTmemO + 32 * c + 16, q);
@@ -842,14 +891,19 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         l *= alpha;
         m_ref = m_new;
       }
-      // this half of head h's P row (bf16), in the 16-byte chunks p0/8,
-      // p0/8 + 1 and p1/8; l sums the fp32 values before their rounding
+      // this thread's 16 positions of head h's P row (bf16): chunks 2 slot
+      // and 2 slot + 1, here and in the peer's buffer; l sums the fp32 values
+      // before their rounding.  Thread slot 0 also sends the head's rescale
+      // factor (chunk 6) and lane 0 the quadrant's "some head rescaled" flag
+      // (chunk 7 of the quadrant's first row).
       ok = ok && wt.wait(&bars->pfree[b], par ^ 1);
       uint8_t* prow = pbuf(b);
+      const uint32_t rp = mapa(prow, peer), rbar = mapa(&bars->rpfull[b], peer);
+      if (slot == 0 && hl == 0) bar_arrive_expect_tx_remote(rbar, C::kPMsgBytes);
       float2 ls = make_float2(0.f, 0.f);
       const float2 ps2 = make_float2(ps, ps), nm2 = make_float2(-m_ref, -m_ref);
 #pragma unroll
-      for (int c = 0; c < 3; ++c) {
+      for (int c = 0; c < 2; ++c) {
         uint32_t pk[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -859,16 +913,22 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           ls = __fadd2_rn(ls, e);
           pk[k] = *reinterpret_cast<const uint32_t*>(&two);
         }
-        const int chunk = c < 2 ? p0 / 8 + c : p1 / 8;
-        *reinterpret_cast<uint4*>(prow + (chunk >> 3) * kSwBlk + swz_chunk(h, chunk & 7)) =
-            make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        const uint32_t off = swz_chunk(h, 2 * slot + c);
+        *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+        st_async_v4(rp + off, pk[0], pk[1], pk[2], pk[3], rbar);
+      }
+      if (slot == 0) {
+        // (tile 0 sets the first reference: O holds nothing yet)
+        const bool any = __any_sync(0xffffffffu, i > 0 && alpha != 1.f);
+        st_async_b32(rp + swz_chunk(h, 6), __float_as_uint(alpha), rbar);
+        if (lane == 0) st_async_b32(rp + swz_chunk(h, 7), any ? 1u : 0u, rbar);
       }
       l += ls.x + ls.y;
       if (!C::kConv && valid < kN) {
         // dense bf16 tail: rows past the unit hold whatever the cache holds
         // there; zero them so P = 0 never meets a non-finite value
         uint8_t* v = opl(j);
-        for (int idx = sh * 128 + h; idx < (kN - valid) * 32; idx += 256) {
+        for (int idx = slot * 64 + hl; idx < (kN - valid) * 32; idx += 64 * 3) {
           const int row = valid + idx / 32, blk = (idx / 8) & 3, ch = idx & 7;
           *reinterpret_cast<uint4*>(v + blk * kBlkBytes + swz_chunk(row, ch)) = make_uint4(0, 0, 0, 0);
         }
@@ -878,59 +938,16 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       __syncwarp();
       if (lane == 0) bar_arrive(&bars->pfull[b]);
     }
-    // ------------------------------------------------------------ epilogue
-    if (live) {
-      if (ntiles > 0) ok = ok && wt.wait(&bars->pfree[psel(ntiles - 1)], ppar(ntiles - 1));
-      tc_after();
-      // O half (128 heads x 256 fp32) -> workspace, normalised by the head's
-      // l (the sum of the pair's halves).  With the last PV complete, every
-      // stage, P and exchange buffer is idle (the peer sent its last partial
-      // before this CTA's last softmax step), so the half is staged as 8
-      // swizzled blocks of 32 columns, in four rounds of one block per thread
-      // of the pair: the TMA stores of the blocks a round completes leave
-      // while the next round is staged.
-      // A sequence's only unit writes the final bf16 output (4 blocks of 64
-      // columns: two 32-column chunks each, complete after rounds 1 and 3)
-      // and log-sum-exp itself.
-      bars->l_half[sh * 128 + h] = l;
-      softmax_sync();
-      const float lt = bars->l_half[h] + bars->l_half[128 + h];
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      const bool direct = (u.flags & kUnitDirect) != 0;
-#pragma unroll 1
-      for (int q = 0; q < 4; ++q) {
-        if (direct)
-          stage_output_bf16(lane_base, sm, h, inv, 4 * sh + q, 4 * sh + q + 1);
-        else
-          stage_output(lane_base, sm, h, inv, 4 * sh + q, 4 * sh + q + 1);
-        fence_async_smem();
-        softmax_sync();
-        if (sh == 0 && h == 0) {
-          if (!direct) {
-            tma3_store(&tp.m_po, rank * kHalf + 32 * q, 0, unit_id, sm + q * kSwBlk);
-            tma3_store(&tp.m_po, rank * kHalf + 32 * (4 + q), 0, unit_id, sm + (4 + q) * kSwBlk);
-          } else if (q & 1) {
-            const int c = q >> 1;
-            tma3_store(&tp.m_out, rank * kHalf + 64 * c, 0, u.b, sm + c * kSwBlk);
-            tma3_store(&tp.m_out, rank * kHalf + 64 * (2 + c), 0, u.b, sm + (2 + c) * kSwBlk);
-          }
-        }
-      }
-      if (sh == 0 && h == 0) bulk_commit();
-      if (rank == 0 && sh == 0) {
-        const float lse = (ok && lt > 0.f) ? (m_ref + log2f(lt)) * 0.69314718055994531f : -INFINITY;
-        if (!(u.flags & kUnitDirect))
-          p.ws.part_lse[(size_t)unit_id * p.H + h] = lse;
-        else if (p.lse)
-          p.lse[(size_t)u.b * p.H + h] = lse;
-      }
-      if (sh == 0 && h == 0) bulk_wait_read();
-    }
-  } else if (C::kConv && (warp == 2 || warp == 3 || (warp >= 12 && warp < 16))) {
+    // the row sum and log-sum-exp of the head are formed after the pool
+    // barrier below
+    bars->l_part[slot][hl] = l;
+    if (slot == 0) bars->m_fin[hl] = m_ref;
+    (void)ok;
+  } else if (C::kConv && conv_id >= 0) {
     // ------------------------------------------------------------ converter
     // raw slot r of tile i -> operand stage j, once the rows have landed and
     // PV of the stage's previous tile is done; kConvWarps warps share a tile
-    const int t = warp < 4 ? threadIdx.x - 64 : threadIdx.x - 384 + 64;
+    const int t = 32 * conv_id + lane;
     for (int i = 0; i < ntiles; ++i) {
       const int r = i % C::kRawRing, j = i % C::kStages;
       // FP8: stages 1-3 hold the staged query until it is in tensor memory
@@ -983,16 +1000,88 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     }
   }
 
+  // -------------------------------------------------------------- epilogue
+  // Every pool warp meets here once its role is done.  The softmax threads
+  // have stored their row sums; the owner of each head (slot 0) forms its l
+  // and log-sum-exp and sends l to the peer.  Pool slots 0 and 1 of every
+  // quadrant (8 warps) then stage the O half (128 heads x 256 fp32), each
+  // row normalised by its head's l -- this CTA's heads from its own sums,
+  // the peer's heads from the peer's -- in four rounds of one 32-column block
+  // per thread: the TMA stores of the blocks a round completes leave while
+  // the next round is staged.  With the last PV complete in both CTAs, every
+  // stage, P and exchange buffer is idle, so the half is staged from offset 0.
+  // A sequence's only unit writes the final bf16 output (4 blocks of 64
+  // columns: two 32-column chunks each, complete after rounds 1 and 3) and
+  // log-sum-exp itself.
+  if (live && pool) {
+    pool_sync();
+    const int hl = hq & 63;
+    if (own_q && slot == 0) {
+      const float lt = bars->l_part[0][hl] + bars->l_part[1][hl] + bars->l_part[2][hl];
+      const float m = bars->m_fin[hl];
+      const uint32_t lbar = mapa(&bars->lpeer, peer);
+      if (hl == 0) bar_arrive_expect_tx_remote(lbar, 64 * 4);
+      st_async_b32(mapa(&bars->l_peer[hl], peer), __float_as_uint(lt), lbar);
+      const bool finite = !bars->abort && lt > 0.f;
+      const float lse = finite ? (m + log2f(lt)) * 0.69314718055994531f : -INFINITY;
+      if (!(u.flags & kUnitDirect))
+        p.ws.part_lse[(size_t)unit_id * p.H + hq] = lse;
+      else if (p.lse)
+        p.lse[(size_t)u.b * p.H + hq] = lse;
+    }
+    if (slot < 2) {
+      bool ok = true;
+      if (ntiles > 0) ok = wt.wait(&bars->pfree[psel(ntiles - 1)], ppar(ntiles - 1));
+      float lt;
+      if (own_q) {
+        lt = bars->l_part[0][hl] + bars->l_part[1][hl] + bars->l_part[2][hl];
+      } else {
+        ok = wt.wait(&bars->lpeer, 0) && ok;
+        lt = bars->l_peer[hl];
+      }
+      __syncwarp();   // the tensor-memory loads below are warp-collective
+      tc_after();
+      const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+      const float inv = (ok && lt > 0.f) ? 1.f / lt : 0.f;
+      const bool direct = (u.flags & kUnitDirect) != 0;
+      const int sh = slot;
+#pragma unroll 1
+      for (int q = 0; q < 4; ++q) {
+        if (direct)
+          stage_output_bf16(lane_base, sm, hq, inv, 4 * sh + q, 4 * sh + q + 1);
+        else
+          stage_output(lane_base, sm, hq, inv, 4 * sh + q, 4 * sh + q + 1);
+        fence_async_smem();
+        epi_sync();
+        if (warp == 4 && lane == 0) {
+          if (!direct) {
+            tma3_store(&tp.m_po, rank * kHalf + 32 * q, 0, unit_id, sm + q * kSwBlk);
+            tma3_store(&tp.m_po, rank * kHalf + 32 * (4 + q), 0, unit_id, sm + (4 + q) * kSwBlk);
+          } else if (q & 1) {
+            const int c = q >> 1;
+            tma3_store(&tp.m_out, rank * kHalf + 64 * c, 0, u.b, sm + c * kSwBlk);
+            tma3_store(&tp.m_out, rank * kHalf + 64 * (2 + c), 0, u.b, sm + (2 + c) * kSwBlk);
+          }
+        }
+      }
+      if (warp == 4 && lane == 0) {
+        bulk_commit();
+        bulk_wait_read();
+      }
+    }
+  }
+
   // ---------------------------------------------------------------- teardown
   tc_before();
   __syncthreads();
   cluster_sync();  // neither CTA issues remote stores any more
   if (bars->abort) {
-    // The partial scores arrive by asynchronous remote stores, which the
-    // cluster barrier does not wait for.  On the normal path every one has
-    // landed (this CTA waited for each tile's); after an abort some the peer
-    // issued may still be in flight into this CTA's shared memory, so it
-    // stays alive for a bound far above their delivery time (microseconds).
+    // The partial scores, P rows and row sums arrive by asynchronous remote
+    // stores, which the cluster barrier does not wait for.  On the normal
+    // path every one has landed (this CTA waited for each); after an abort
+    // some the peer issued may still be in flight into this CTA's shared
+    // memory, so it stays alive for a bound far above their delivery time
+    // (microseconds).
     if (threadIdx.x == 0) {
       uint64_t t0, t;
       asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));

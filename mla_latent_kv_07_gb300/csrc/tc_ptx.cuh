@@ -46,6 +46,19 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, ui
                "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
                : "memory");
 }
+// 4 bytes into a peer CTA's shared memory, counted on the peer's barrier when
+// they land
+__device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr),
+               "r"(v), "r"(remote_bar)
+               : "memory");
+}
+// `count` arrivals at once on a peer CTA's barrier (release: this thread's
+// earlier memory accesses are ordered before them)
+__device__ __forceinline__ void bar_arrive_remote_n(uint32_t remote_addr, uint32_t count) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0], %1;" ::"r"(remote_addr), "r"(count)
+               : "memory");
+}
 __device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa(b)), "r"(bytes)
                : "memory");
@@ -138,6 +151,15 @@ __device__ __forceinline__ void mma_commit(uint64_t* b) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                    sa(b))
                : "memory");
+}
+// the MMAs issued so far arrive, once complete, on the barrier at the same
+// shared-memory offset in every CTA of the cluster named by `mask`
+__device__ __forceinline__ void mma_commit_mc(uint64_t* b, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          sa(b)),
+      "h"(mask)
+      : "memory");
 }
 #define TC_LD16(taddr, r)                                                                       \
   asm volatile(                                                                                 \

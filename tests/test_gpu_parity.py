@@ -116,6 +116,32 @@ def test_rows_past_end_pos_are_never_used():
 
 
 @pytest.mark.parametrize("fmt", [0, 1])
+def test_rising_scores_rescale_mid_unit(fmt):
+    # the latent rows drift along a fixed direction u, 100 units per 48
+    # positions: a head whose query has q.u ~ 1 sees its maximum score rise by
+    # ~19 (log2 units) every tile -- past the lazy-rescale threshold, so its
+    # running reference and its rows of O are rescaled inside a unit (units
+    # here span about four tiles), while heads with q.u < 0 keep their first
+    # reference.  Each CTA of a pair owns half the heads and scales the other
+    # half's rows of its own output half on the owner's request.
+    B, S, H = 2, 8192, 128
+    rng = np.random.default_rng(77 + fmt)
+    u = rng.standard_normal(512)
+    u /= np.linalg.norm(u)
+    t = np.arange(S, dtype=np.float64)[None, :, None]
+    kv = torch.from_numpy(rng.standard_normal((B, S, 512)) + 100.0 * (t / 48.0) * u[None, None, :]).float()
+    kv_bf16 = kv.to(torch.bfloat16)
+    oc = oracle_cache(kv_bf16, _rand_bf16((B, S, 64), 79), fmt)
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((B, H, 512), 80), _rand_bf16((B, H, 64), 81)
+    ends = np.array([8192, 6000], np.int32)
+    out, lse = mla.decode(dc, ql.cuda(), qp.cuda(), torch.from_numpy(ends).cuda(), S, 0.1352)
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), ends, 0.1352)
+    check_close(f64(out).reshape(-1, 512), ref, "out")
+    check_close(f64(lse).reshape(-1), ref_lse, "lse")
+
+
+@pytest.mark.parametrize("fmt", [0, 1])
 def test_single_unit_sequences_write_directly(fmt):
     # sequences of one or two tiles get a single unit, which writes the final
     # output (and lse, when asked) itself; the long one is split and combined
