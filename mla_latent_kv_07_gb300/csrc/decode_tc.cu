@@ -43,9 +43,8 @@
 //           quadrants: softmax, three threads per head, 16 positions of each
 //           tile each (with new rows in a dense call, slots 1-2 first write
 //           the row: the cache-write step).  In the peer's quadrants: slot 0
-//           sends the peer's heads' partial scores (in a gather call it first
-//           asks L2 for the unit's rows), slot 1 rescales the peer's heads'
-//           rows of O on request, slot 2 converts (if any).  Slots 0-1 of all
+//           sends the peer's heads' partial scores, slot 1 rescales the
+//           peer's heads' rows of O on request, slot 2 converts (if any).  Slots 0-1 of all
 //           four quadrants stage the output half in the epilogue.
 //   warps 3, 16-18 and the pool's slot-2 warps of the peer's quadrants
 //           converter (FP8 caches and gathers): raw rows -> bf16 operand tile
@@ -113,8 +112,9 @@ struct Cfg {
   // QK may be issued at most this many tiles past the last issued PV: enough
   // run-ahead to keep the tensor pipe busy through the exchange and softmax
   // of a tile, no more -- the pipe runs its queue in order, so each queued QK
-  // delays the PV behind it.
-  static constexpr int kQkAhead = 3;
+  // delays the PV behind it.  (Measured with the head-split softmax: 4 beats 3
+  // by 3% on the FP8 workloads; the two S buffers bound it anyway.)
+  static constexpr int kQkAhead = 4;
   static constexpr int kBlkBytes = kN * 128;       // one 64-column swizzled block of a tile
   static constexpr int kOplBytes = 4 * kBlkBytes;  // latent half operand
   static constexpr int kOpeBytes = kBlkBytes;      // rotary operand (full 64 columns)
@@ -689,22 +689,10 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     // exchange buffer, as soon as each tile's scores are computed.
     const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
     const int hl = hq & 63;   // the head's row among the peer's 64
-    if (kSparse && live) {
-      // idle until the first scores: ask L2 for every row this unit gathers
-      // after its first two tiles (this CTA's latent half, the row's scales
-      // and its rotary row), so the producer's gathers of later tiles meet L2
-      // latency instead of DRAM's
-      const int* gl = p.ws.gidx + (size_t)u.b * p.K;
-      const size_t base = (size_t)u.b * p.max_seq_len;
-      const uint8_t* kvb = static_cast<const uint8_t*>(p.kv);
-      const uint8_t* peb = static_cast<const uint8_t*>(p.pe);
-      for (int e = u.t0 + 2 * kN + hl; e < u.t1; e += 64) {
-        const size_t row = base + (size_t)gl[e];
-        prefetch_l2(kvb + row * (kFmt == 1 ? kDc : 2 * kDc) + rank * C::kRawRow, C::kRawRow);
-        if (kFmt == 1) prefetch_l2(p.kv_scale + row * kNblk, 16);
-        if (rank == 0) prefetch_l2(peb + row * (2 * kDr), 2 * kDr);
-      }
-    }
+    // the peer's exchange buffer 0 (this head's first row) and its xfull[0];
+    // buffer b is a fixed stride further (distributed shared addresses of one
+    // CTA are linear)
+    const uint32_t xd0 = mapa(xbuf(0) + 16 * hl, peer), xf0 = mapa(&bars->xfull[0], peer);
     for (int i = 0; i < ntiles; ++i) {
       const int b = ssel(i);
       if (!wt.wait(&bars->sfull[b], spar(i))) break;
@@ -719,7 +707,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       if (lane == 0) bar_arrive(&bars->sfree[b]);
       const int xb = xsel(i);
       if (!wt.wait(&bars->xempty[xb], xpar(i))) break;   // phase 0: the peer's query staging is done
-      const uint32_t xd = mapa(xbuf(xb) + 16 * hl, peer), xf = mapa(&bars->xfull[xb], peer);
+      const uint32_t xd = xd0 + xb * C::kXStride, xf = xf0 + xb * 8u;
       uint32_t w[C::kXRows * 4];
 #pragma unroll
       for (int g = 0; g < kN / 4; ++g)
@@ -791,6 +779,13 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     const float ps = pos_scale ? sl2 : 1.f;   // the factor still to apply to sc in P
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
+    // loop-invariant addresses: this thread's two P chunks, the rescale
+    // factor and flag slots, the peer's P buffer 0 and rpfull[0], and the
+    // peer's xempty[0] (buffer b of each is a fixed stride further)
+    const uint32_t off_p0 = swz_chunk(h, 2 * slot), off_p1 = swz_chunk(h, 2 * slot + 1);
+    const uint32_t off_a = swz_chunk(h, 6), off_f = swz_chunk(h, 7);
+    const uint32_t rp0 = mapa(pbuf(0), peer), rbar0 = mapa(&bars->rpfull[0], peer);
+    const uint32_t rxe0 = mapa(&bars->xempty[0], peer);
     if (app && slot > 0) {   // idle until the first scores: write the new row first
       append_row(p.ap, u.b, u.t1 - 1, 64 * (slot - 1) + 32 * (quad & 1) + lane);
       fence_async_global();
@@ -835,7 +830,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         __syncwarp();
         // the buffer may be refilled: the values read above are already in
         // registers, so no release ordering is needed
-        if (lane == 0) bar_arrive_remote_relaxed(mapa(&bars->xempty[xb], peer));
+        if (lane == 0) bar_arrive_remote_relaxed(rxe0 + xb * 8u);
       }
       // masked scores and the tile maximum of the head.  With a positive
       // scale the scores stay unscaled here: round-to-nearest is monotone, so
@@ -898,7 +893,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       // (chunk 7 of the quadrant's first row).
       ok = ok && wt.wait(&bars->pfree[b], par ^ 1);
       uint8_t* prow = pbuf(b);
-      const uint32_t rp = mapa(prow, peer), rbar = mapa(&bars->rpfull[b], peer);
+      const uint32_t rp = rp0 + b * C::kPBytes, rbar = rbar0 + b * 8u;
       if (slot == 0 && hl == 0) bar_arrive_expect_tx_remote(rbar, C::kPMsgBytes);
       float2 ls = make_float2(0.f, 0.f);
       const float2 ps2 = make_float2(ps, ps), nm2 = make_float2(-m_ref, -m_ref);
@@ -913,15 +908,15 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           ls = __fadd2_rn(ls, e);
           pk[k] = *reinterpret_cast<const uint32_t*>(&two);
         }
-        const uint32_t off = swz_chunk(h, 2 * slot + c);
+        const uint32_t off = c == 0 ? off_p0 : off_p1;
         *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
         st_async_v4(rp + off, pk[0], pk[1], pk[2], pk[3], rbar);
       }
       if (slot == 0) {
         // (tile 0 sets the first reference: O holds nothing yet)
         const bool any = __any_sync(0xffffffffu, i > 0 && alpha != 1.f);
-        st_async_b32(rp + swz_chunk(h, 6), __float_as_uint(alpha), rbar);
-        if (lane == 0) st_async_b32(rp + swz_chunk(h, 7), any ? 1u : 0u, rbar);
+        st_async_b32(rp + off_a, __float_as_uint(alpha), rbar);
+        if (lane == 0) st_async_b32(rp + off_f, any ? 1u : 0u, rbar);
       }
       l += ls.x + ls.y;
       if (!C::kConv && valid < kN) {

@@ -216,11 +216,6 @@ __device__ __forceinline__ void bulk_store(void* gdst, const void* src, uint32_t
                "r"(sa(src)), "r"(bytes)
                : "memory");
 }
-// Asynchronous prefetch of `bytes` (a multiple of 16, 16-byte aligned) of
-// global memory into L2; nothing waits for it.
-__device__ __forceinline__ void prefetch_l2(const void* g, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(g), "r"(bytes) : "memory");
-}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the bulk stores of this thread have read their shared-memory sources (their
 // global writes complete with the grid)
