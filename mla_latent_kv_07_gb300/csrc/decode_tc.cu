@@ -12,8 +12,9 @@
 // Why a pair: an fp32 accumulator for 128 heads x 512 latent columns fills all
 // of one SM's tensor memory (512 columns x 128 lanes x 4 B), leaving no room
 // for the scores.  So CTA r of the pair owns latent columns [256r, 256r+256)
-// and rotary columns [32r, 32r+32) of the cache and of O, and heads
-// [64r, 64r+64) of the softmax:
+// and rotary columns [32r, 32r+32) of the cache and of O, and half of the
+// heads for the softmax: TMEM lanes 32 q + 16 r .. 32 q + 16 r + 15 of every
+// lane quadrant q (head h lives in lane h).
 //   * QK: each CTA contracts its 288-wide half (Q half as the A operand held in
 //     tensor memory, K half from shared memory) into a partial S for all 128
 //     heads.  The partial rows of the peer's 64 heads go to the peer through
@@ -28,27 +29,31 @@
 //     its own O half.  When the owner of a head raised the head's reference
 //     maximum, the other CTA scales its row of that head first.
 // Every cache byte is fetched by exactly one CTA and there is no redundant
-// tensor-core or softmax work.
+// tensor-core or softmax work.  Interleaving the heads by quadrant puts one
+// softmax warp on each of the SM's four schedulers.
 //
 // Tensor memory (512 columns): O half [0,256) fp32; Q half [256,400) bf16 (2
 // per column); S double buffer [400,448) and [448,496) fp32.
 //
-// Warp roles (512 threads; 608 with a converter):
+// Warp roles (512 threads; 544 with a converter):
 //   warp 0  producer: TMA tiles (dense) or four-row TMA gathers (gather)
 //   warp 1  QK issuer (one thread) and tensor-memory owner
 //   warp 2  PV issuer (one thread); in a dense bf16 call it first works out
 //           the split schedule and the pair's unit (schedule.cuh)
 //   warps 4-15  the head pool, three warps per TMEM lane quadrant (a warp may
-//           access lanes 32 (warp & 3) .. + 31 only).  In the CTA's own
-//           quadrants: softmax, three threads per head, 16 positions of each
-//           tile each (with new rows in a dense call, slots 1-2 first write
-//           the row: the cache-write step).  In the peer's quadrants: slot 0
-//           sends the peer's heads' partial scores, slot 1 rescales the
-//           peer's heads' rows of O on request, slot 2 converts (if any).  Slots 0-1 of all
-//           four quadrants stage the output half in the epilogue.
-//   warps 3, 16-18 and the pool's slot-2 warps of the peer's quadrants
-//           converter (FP8 caches and gathers): raw rows -> bf16 operand tile
-//           bf16(fp32(e4m3 * scale)) in the 128-byte swizzled layout
+//           access lanes 32 (warp & 3) .. + 31 only), by slot:
+//           4-7   softmax of the quadrant's 16 own heads (16-lane TMEM
+//                 access: thread t holds two heads x 12 positions a tile);
+//                 warps 4-7 first stage the query half into tensor memory
+//           8-11  senders of the quadrant's 16 peer heads' partial scores,
+//                 and rescalers of those heads' rows of O (served while they
+//                 wait); with new rows in a dense call they first write the
+//                 row (the cache-write step)
+//           12-15 converter (if any)
+//           Slots 4-11 stage the output half in the epilogue.
+//   warps 3, 16 and 12-15  converter (FP8 caches and gathers): raw rows ->
+//           bf16 operand tile bf16(fp32(e4m3 * scale)) in the 128-byte
+//           swizzled layout
 // Distributed shared memory moves ~20-35 GB/s per SM with ~0.3 us latency on
 // this part, so each tile sends 9 KB of partial scores and 6.3 KB of P rows
 // per direction.
@@ -82,7 +87,7 @@ constexpr int kPeHalf = kDr / 2;           // 32 rotary columns per CTA
 constexpr float kRescaleThreshold = 16.0f;
 constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemS = 400;
 constexpr long kSpinLimit = 1L << 26;   // polls (~seconds) before giving up
-constexpr int kConvWarps = 6;             // converter: warps 3, 16-18 and two pool warps
+constexpr int kConvWarps = 6;             // converter: warps 3, 16 and the pool's four slot-2 warps
 
 // Shared-memory plan per variant.  Tiles are 48 positions (MMA N for QK, K
 // for PV), with two S, P and exchange buffers.  An operand stage holds the
@@ -105,10 +110,11 @@ struct Cfg {
   static constexpr int kXBufs = 2;   // exchange buffers
   // Warps: 0 producer, 1 QK issuer, 2 PV issuer (a dense bf16 call's split
   // schedule first), 3 converter; 4-15 the head pool, three warps per TMEM
-  // lane quadrant (quadrant = warp & 3, slot = (warp - 4) >> 2); 16-18
-  // converter.  Variants without a converter stop at warp 15.
-  static constexpr int kSmWarps = 6;   // softmax warps: the pool's warps in the CTA's own quadrants
-  static constexpr int kThreads = 32 * (kConv ? 19 : 16);
+  // lane quadrant (quadrant = warp & 3, slot = (warp - 4) >> 2: softmax,
+  // sender/rescaler, converter); 16 converter.  Variants without a converter
+  // stop at warp 15 (warp 3 and the pool's third slot idle).
+  static constexpr int kSmWarps = 4;   // softmax warps: one per TMEM lane quadrant
+  static constexpr int kThreads = 32 * (kConv ? 17 : 16);
   // QK may be issued at most this many tiles past the last issued PV: enough
   // run-ahead to keep the tensor pipe busy through the exchange and softmax
   // of a tile, no more -- the pipe runs its queue in order, so each queued QK
@@ -123,17 +129,20 @@ struct Cfg {
   static constexpr int kPBytes = ((kN + 63) / 64) * kSwBlk;
   static_assert(kN == 48, "P rows keep chunks 6 and 7 free");
   // exchange buffer: the kN partial scores of each of the peer's 64 heads as
-  // 24-bit codes (the fp32 value rounded to its top 24 bits), four positions
-  // in three words, so 3 kN / 4 words = kXRows 16-byte rows per head; row q
-  // of head h at index q * 64 + (h & 63), so a warp's remote store is one
-  // contiguous 512-byte run.  Buffers are kXStride apart (bf16 variants keep
-  // twice the room: the query is staged across the P and exchange buffers).
-  static constexpr int kXRows = 3 * kN / 16;
-  static constexpr int kXBytes = kXRows * 64 * 16;
+  // 24-bit codes (the fp32 value rounded to its top 24 bits), four values in
+  // three words.  A quadrant's 16 peer heads x kN positions travel from the
+  // sender thread t to the softmax thread t of the same quadrant in the peer
+  // (both hold the same fragment: two heads x kN / 4 positions), 18 words a
+  // thread: four 16-byte rows at q * 512 + 16 t and 8 bytes at 2048 + 8 t of
+  // the quadrant's kXQuad bytes, so a warp's remote store is contiguous.
+  // Buffers are kXStride apart (bf16 variants keep twice the room: the query
+  // is staged across the P and exchange buffers).
+  static constexpr int kXQuad = 32 * 72;
+  static constexpr int kXBytes = 4 * kXQuad;
   static constexpr int kXStride = kFmt == 1 ? kXBytes : 2 * kXBytes;
   // bytes of one tile's message of P rows to the peer: 64 rows x kN bf16,
   // one rescale factor per row, one flag word per quadrant
-  static constexpr uint32_t kPMsgBytes = 64 * kN * 2 + 64 * 4 + 2 * 4;
+  static constexpr uint32_t kPMsgBytes = 64 * kN * 2 + 64 * 4 + 4 * 4;
   static constexpr int kStage = kOplBytes + kOpeBytes;
   static constexpr int kStages = kConv ? (kFmt == 1 ? 4 : 2) : 4;
   static constexpr int kRawRow = kFmt == 1 ? kHalf : kHalf * 2;  // bytes of a raw latent half row
@@ -180,13 +189,10 @@ struct TcParams {
   CUtensorMap m_out;  // final output [B][128][512] bf16 (box 64 x 128, 128-byte swizzle)
 };
 
-// Named barriers: 1 among the 8 epilogue warps (pool slots 0 and 1); 2 + q
-// among the 3 softmax warps of quadrant q; 6 among warps 4-7 after the query
-// staging; 7 among the 12 pool warps before the epilogue.
+// Named barriers: 1 among the 8 epilogue warps (pool slots 0 and 1); 6 among
+// warps 4-7 after the query staging; 7 among the 12 pool warps before the
+// epilogue.
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-__device__ __forceinline__ void quad_sync(int q) {
-  asm volatile("bar.sync %0, 96;" ::"r"(2 + q) : "memory");
-}
 __device__ __forceinline__ void qstage_sync() { asm volatile("bar.sync 6, 128;" ::: "memory"); }
 __device__ __forceinline__ void pool_sync() { asm volatile("bar.sync 7, 384;" ::: "memory"); }
 // Partial scores cross between the pair as the top 24 bits of the fp32 value,
@@ -248,10 +254,8 @@ struct Bars {
   Unit unit;          // this pair's unit, when the kernel computes the schedule
   uint32_t tmem;
   volatile int abort;
-  float pm[2][3][64];    // softmax: tile maxima of each own head's three threads, by tile parity
-  float l_part[3][64];   // epilogue: the three threads' row sums of each own head
-  float l_peer[64];      // epilogue: row sums of the peer's heads (sent by the peer)
-  float m_fin[64];       // epilogue: final reference maximum of each own head
+  float l_own[128];      // epilogue: row sums of this CTA's heads (indexed by head)
+  float l_peer[128];     // epilogue: row sums of the peer's heads (sent by the peer)
 };
 static_assert(sizeof(Bars) <= 4096, "barrier block");
 
@@ -292,6 +296,23 @@ __device__ __forceinline__ void dequant16(uint4 v, float sc, uint4& lo, uint4& h
   }
   lo = make_uint4(o[0], o[1], o[2], o[3]);
   hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+// Scale the O half's rows of the 16 TMEM lanes from `lanes` (a tensor-memory
+// address with the lane field set): lane fl = t/4 by a, lane fl + 8 by b (the
+// 16-lane access touches only those rows, so warps that own the other 16
+// lanes of the quadrant may scale them at the same time).  Warp-collective.
+__device__ __forceinline__ void scale_rows16(uint32_t lanes, float a, float b) {
+#pragma unroll 1
+  for (int c = 0; c < 8; ++c) {
+    uint32_t r[16];
+    TC_LD16L_X4(lanes + kTmemO + 32 * c, r);
+    tc_wait_ld();
+#pragma unroll
+    for (int k = 0; k < 16; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * ((k & 2) ? b : a));
+    TC_ST16L_X4(lanes + kTmemO + 32 * c, r);
+  }
+  tc_wait_st();
 }
 
 // Epilogue: O columns [32 c0, 32 c1) of TMEM lane h, times inv, into the
@@ -361,15 +382,21 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   Waiter wt{bars, p.ws.status, p.spin_limit > 0 ? (long)p.spin_limit : kSpinLimit};
 
-  // the head pool: warp & 3 is the TMEM lane quadrant the warp may access;
-  // this CTA owns heads [64 rank, 64 rank + 64), quadrants 2 rank and 2 rank + 1
+  // the head pool: warp & 3 is the TMEM lane quadrant the warp may access.
+  // This CTA owns heads (TMEM lanes) 32 q + 16 rank .. + 15 of every quadrant
+  // q, the peer the other 16: each CTA's softmax, senders and rescalers have
+  // one warp per quadrant, so they spread over all four schedulers.
   const int quad = warp & 3;
   const bool pool = warp >= 4 && warp < 16;
-  const int slot = (warp - 4) >> 2;
-  const bool own_q = (quad >> 1) == (int)rank;
-  const int hq = 32 * quad + lane;   // this lane's head (TMEM lane) in the pool and epilogue
-  // converter warps: 3, 16-18 and the pool's third warp in each of the peer's quadrants
-  const int conv_id = warp == 3 ? 0 : warp >= 16 ? warp - 15 : (pool && !own_q && slot == 2) ? 4 + (quad & 1) : -1;
+  const int slot = (warp - 4) >> 2;   // 0 softmax, 1 sender/rescaler, 2 converter
+  const int hq = 32 * quad + lane;    // this lane's head under the 32-lane access (epilogue, rescales)
+  const bool own_lane = (lane >> 4) == (int)rank;
+  const int own_base = 32 * quad + 16 * (int)rank, peer_base = 32 * quad + 16 * (int)peer;
+  // 16-lane fragments (TC_LD16L_*): this thread holds heads base + fl and
+  // base + fl + 8 at the column pairs 8k + 2 fc, 8k + 2 fc + 1
+  const int fl = lane >> 2, fc = lane & 3;
+  // converter warps: 3, 16 and the pool's third slot (one per quadrant)
+  const int conv_id = warp == 3 ? 0 : warp == 16 ? 1 : (pool && slot == 2) ? 2 + quad : -1;
 
   auto opl = [&](int j) { return sm + j * C::kStage; };               // operand stage j
   auto ope = [&](int j) { return sm + j * C::kStage + kOplBytes; };
@@ -402,7 +429,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       bar_init(&bars->sfull[b], 1);
-      bar_init(&bars->sfree[b], C::kSmWarps + 2);   // softmax warps and the two sender warps read S
+      bar_init(&bars->sfree[b], C::kSmWarps + 4);   // softmax and sender warps read S
       bar_init(&bars->xfull[b], 1);    // one arrival (with the tile's bytes) from the peer
       bar_init(&bars->xempty[b], C::kSmWarps);   // the peer's softmax warps
     }
@@ -591,7 +618,6 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       const uint64_t d_v0 = sdesc(sa(opl(0)), kBlkBytes, 1024);
       const uint64_t d_p0 = sdesc(sa(pbuf(0)), 16, 1024);
       const uint32_t t_o = tmem + kTmemO;
-      const int pq0 = 2 * (int)peer;   // the peer's first quadrant
       int nreq = 0;
       for (int i = 0; i < ntiles; ++i) {
         const int j = i % C::kStages, b = psel(i);
@@ -601,9 +627,11 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         // order them before the tensor core reads the buffer
         fence_async_smem();
         const uint8_t* pb = pbuf(b);
-        const uint32_t f0 = *reinterpret_cast<const volatile uint32_t*>(pb + swz_chunk(32 * pq0, 7));
-        const uint32_t f1 = *reinterpret_cast<const volatile uint32_t*>(pb + swz_chunk(32 * pq0 + 32, 7));
-        if (f0 | f1) {
+        uint32_t flags = 0;   // one word per quadrant, in the padding of its first peer row
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          flags |= *reinterpret_cast<const volatile uint32_t*>(pb + swz_chunk(32 * q + 16 * (int)peer, 7));
+        if (flags) {
           // the rescalers scale rows of O that PV of tile i - 1 writes
           if (i > 0 && !wt.wait(&bars->pfree[psel(i - 1)], ppar(i - 1))) break;
           ++nreq;
@@ -613,7 +641,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           for (long it = 0; it < wt.lim && !bars->abort; ++it) {
             int d;
             asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(d) : "r"(sa(&bars->resc_done)) : "memory");
-            if (d >= 2 * nreq) {
+            if (d >= 4 * nreq) {
               done = true;
               break;
             }
@@ -683,145 +711,163 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       mma_commit(&bars->drain);
       wt.drain(&bars->drain, 0);
     }
-  } else if (pool && !own_q && slot == 0) {
-    // ------------------------------------------------------------ sender
-    // Partial S of the peer's heads (this warp's quadrant) -> the peer's
-    // exchange buffer, as soon as each tile's scores are computed.
-    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-    const int hl = hq & 63;   // the head's row among the peer's 64
-    // the peer's exchange buffer 0 (this head's first row) and its xfull[0];
+  } else if (pool && slot == 1) {
+    // ------------------------------------------------------------ sender / rescaler
+    // Partial S of the peer's 16 heads of this quadrant -> the peer's
+    // exchange buffer, as soon as each tile's scores are computed.  (With new
+    // rows in a dense call, the four warps first write the row: the
+    // cache-write step, while they wait for the first scores.)
+    // Rescaler duty, served inside this warp's waits: when the peer raises
+    // the reference maximum of one of its heads, this CTA's row of that head
+    // in O (its latent half) is scaled by the factor the peer sent with the
+    // tile's P rows, before PV of that tile.  The PV issuer posts the request
+    // once PV of the previous tile is complete and waits for all four warps.
+    if (app) {
+      append_row(p.ap, u.b, u.t1 - 1, 32 * quad + lane);
+      fence_async_global();
+      __syncwarp();
+      if (lane == 0) bar_arrive(&bars->appended);
+    }
+    const uint32_t tl = tmem + ((uint32_t)peer_base << 16);
+    const uint32_t off_aA = swz_chunk(peer_base + fl, 6), off_aB = swz_chunk(peer_base + fl + 8, 6);
+    int handled = 0;
+    // one look at the request word; true if a request was served.  Tensor-
+    // memory loads and stores are warp-collective, so the whole warp takes
+    // the branch when any of its 16 rows needs scaling (factor 1 for the
+    // others).
+    auto serve = [&]() -> bool {
+      __syncwarp();
+      int req;
+      asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(req) : "r"(sa((const void*)&bars->resc_req)) : "memory");
+      if (req <= handled) return false;
+      const int i = req - 1;
+      tc_after();
+      const uint8_t* pb = pbuf(psel(i));
+      const float a = *reinterpret_cast<const float*>(pb + off_aA);
+      const float bb = *reinterpret_cast<const float*>(pb + off_aB);
+      if (__any_sync(0xffffffffu, a != 1.f || bb != 1.f)) scale_rows16(tl, a, bb);
+      tc_before();
+      __syncwarp();
+      if (lane == 0)
+        asm volatile("red.release.cta.shared.add.s32 [%0], 1;" ::"r"(sa(&bars->resc_done)) : "memory");
+      handled = req;
+      return true;
+    };
+    // a bounded wait that serves rescale requests while it polls
+    auto swait = [&](uint64_t* bar, uint32_t parity) -> bool {
+      for (long it = 0; it < wt.lim; ++it) {
+        if (bar_try(bar, parity)) return true;
+        if (bars->abort) return false;
+        if (serve()) it = 0;
+      }
+      if (!bars->abort) {
+        bars->abort = 1;
+        atomicOr(p.ws.status, kDevTimeout);
+      }
+      return false;
+    };
+    // the peer's exchange buffer 0 (this thread's rows) and its xfull[0];
     // buffer b is a fixed stride further (distributed shared addresses of one
     // CTA are linear)
-    const uint32_t xd0 = mapa(xbuf(0) + 16 * hl, peer), xf0 = mapa(&bars->xfull[0], peer);
+    const uint32_t xd0 = mapa(xbuf(0) + quad * C::kXQuad + 16 * lane, peer);
+    const uint32_t xe0 = mapa(xbuf(0) + quad * C::kXQuad + 2048 + 8 * lane, peer);
+    const uint32_t xf0 = mapa(&bars->xfull[0], peer);
     for (int i = 0; i < ntiles; ++i) {
       const int b = ssel(i);
-      if (!wt.wait(&bars->sfull[b], spar(i))) break;
+      if (!swait(&bars->sfull[b], spar(i))) break;
+      __syncwarp();
       tc_after();
-      const uint32_t sb = lane_base + kTmemS + b * kN;
-      uint32_t r[kN];
-#pragma unroll
-      for (int c = 0; c < kN / 16; ++c) TC_LD16(sb + 16 * c, (r + 16 * c));
+      uint32_t r[24];
+      TC_LD16L_X4(tl + kTmemS + b * kN, r);
+      TC_LD16L_X2(tl + kTmemS + b * kN + 32, (r + 16));
       tc_wait_ld();
       tc_before();
       __syncwarp();
       if (lane == 0) bar_arrive(&bars->sfree[b]);
       const int xb = xsel(i);
-      if (!wt.wait(&bars->xempty[xb], xpar(i))) break;   // phase 0: the peer's query staging is done
-      const uint32_t xd = xd0 + xb * C::kXStride, xf = xf0 + xb * 8u;
-      uint32_t w[C::kXRows * 4];
+      if (!swait(&bars->xempty[xb], xpar(i))) break;   // phase 0: the peer's query staging is done
+      const uint32_t xd = xd0 + xb * C::kXStride, xe = xe0 + xb * C::kXStride, xf = xf0 + xb * 8u;
+      uint32_t w[18];
 #pragma unroll
-      for (int g = 0; g < kN / 4; ++g)
+      for (int g = 0; g < 6; ++g)
         pack24(r[4 * g], r[4 * g + 1], r[4 * g + 2], r[4 * g + 3], w[3 * g], w[3 * g + 1], w[3 * g + 2]);
       // the peer's phase completes on one arrival carrying the tile's bytes
       // and on those bytes landing, in either order
-      if (hl == 0) bar_arrive_expect_tx_remote(xf, C::kXBytes);
+      if (quad == 0 && lane == 0) bar_arrive_expect_tx_remote(xf, C::kXBytes);
 #pragma unroll
-      for (int q = 0; q < C::kXRows; ++q)
-        st_async_v4(xd + 16 * 64 * q, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3], xf);
+      for (int q = 0; q < 4; ++q) st_async_v4(xd + 512 * q, w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3], xf);
+      st_async_v2(xe, w[16], w[17], xf);
     }
-  } else if (pool && !own_q && slot == 1) {
-    // ------------------------------------------------------------ rescaler
-    // When the peer raises the reference maximum of one of its heads, this
-    // CTA's row of that head in O (its latent half) is scaled by the factor
-    // the peer sent with the tile's P rows, before PV of that tile.  The PV
-    // issuer posts the request once PV of the previous tile is complete.
-    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
-    int handled = 0;
-    for (long it = 0; it < wt.lim; ++it) {
-      if (bars->abort) break;
-      int req;
-      asm volatile("ld.acquire.cta.shared.b32 %0, [%1];" : "=r"(req) : "r"(sa((const void*)&bars->resc_req)) : "memory");
-      if (req > handled) {
-        const int i = req - 1;
-        tc_after();
-        const float alpha = *reinterpret_cast<const float*>(pbuf(psel(i)) + swz_chunk(hq, 6));
-        // tensor-memory loads and stores are warp-collective: the whole warp
-        // takes the branch when any of its rows needs scaling (factor 1 for
-        // the others)
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
-            uint32_t r[16], q[16];
-            TC_LD16(lane_base + kTmemO + 32 * c, r);
-            TC_LD16(lane_base + kTmemO + 32 * c + 16, q);
-            tc_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-              q[k] = __float_as_uint(__uint_as_float(q[k]) * alpha);
-            }
-            TC_ST16(lane_base + kTmemO + 32 * c, r);
-            TC_ST16(lane_base + kTmemO + 32 * c + 16, q);
-          }
-          tc_wait_st();
-        }
-        tc_before();
-        __syncwarp();
-        if (lane == 0)
-          asm volatile("red.release.cta.shared.add.s32 [%0], 1;" ::"r"(sa(&bars->resc_done)) : "memory");
-        handled = req;
+    // serve the remaining requests until the PV issuer is done
+    for (long it = 0; it < wt.lim && !bars->abort; ++it) {
+      if (serve()) {
         it = 0;
       } else if (bars->resc_stop) {
-        break;
+        if (!serve()) break;
       }
     }
-  } else if (pool && own_q) {
+  } else if (pool && slot == 0) {
     // ------------------------------------------------------------ softmax
-    // Three threads per head h (TMEM lane h, one of this CTA's 64 heads),
-    // thread `slot` taking the tile's positions [16 slot, 16 slot + 16).  The
-    // three agree on each tile's maximum through shared memory and a 96-thread
-    // barrier, so they take the same rescale decisions.  P is written into
-    // this CTA's buffer and, by asynchronous remote stores, into the peer's.
-    const int h = hq, hl = h & 63, s16 = 16 * slot;
-    const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16);
+    // One warp per quadrant runs the online softmax of the CTA's 16 heads of
+    // that quadrant over all kN positions of a tile: thread t holds heads
+    // hA = base + t/4 and hB = hA + 8 at positions 8k + 2 (t%4) and
+    // 8k + 2 (t%4) + 1 (k = 0..5), 12 per head; the four threads of a head
+    // agree on its tile maximum by shuffles.  P is written into this CTA's
+    // buffer (4-byte pieces, then read back as 16-byte chunks) and, by
+    // asynchronous remote stores of those chunks, into the peer's.
+    const int hA = own_base + fl, hB = hA + 8;
+    const uint32_t tl = tmem + ((uint32_t)own_base << 16);
     const float sl2 = p.scale_log2;
     const bool pos_scale = sl2 > 0.f;
     const float ps = pos_scale ? sl2 : 1.f;   // the factor still to apply to sc in P
-    float m_ref = -INFINITY, l = 0.f;
+    float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
     bool ok = true;
-    // loop-invariant addresses: this thread's two P chunks, the rescale
-    // factor and flag slots, the peer's P buffer 0 and rpfull[0], and the
-    // peer's xempty[0] (buffer b of each is a fixed stride further)
-    const uint32_t off_p0 = swz_chunk(h, 2 * slot), off_p1 = swz_chunk(h, 2 * slot + 1);
-    const uint32_t off_a = swz_chunk(h, 6), off_f = swz_chunk(h, 7);
+    // loop-invariant addresses: this thread's exchange rows, the peer's P
+    // buffer 0, rpfull[0] and xempty[0] (buffer b of each is a fixed stride
+    // further), the three 16-byte P chunks this thread forwards (chunk
+    // c = fc + 4 j of its head pair: hA's chunks 0-5, then hB's)
     const uint32_t rp0 = mapa(pbuf(0), peer), rbar0 = mapa(&bars->rpfull[0], peer);
     const uint32_t rxe0 = mapa(&bars->xempty[0], peer);
-    if (app && slot > 0) {   // idle until the first scores: write the new row first
-      append_row(p.ap, u.b, u.t1 - 1, 64 * (slot - 1) + 32 * (quad & 1) + lane);
-      fence_async_global();
-      __syncwarp();
-      if (lane == 0) bar_arrive(&bars->appended);
+    uint32_t fwd[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int c = fc + 4 * j;
+      fwd[j] = swz_chunk(c < 6 ? hA : hB, c < 6 ? c : c - 6);
     }
+    const uint32_t off_aA = swz_chunk(hA, 6), off_aB = swz_chunk(hB, 6), off_f = swz_chunk(own_base, 7);
     for (int i = 0; i < ntiles; ++i) {
       const int j = i % C::kStages, sb_i = ssel(i), b = psel(i);
       const uint32_t par = ppar(i);
-      float sc[16];
+      float sc[24];
       ok = ok && wt.wait(&bars->sfull[sb_i], spar(i));
       {
         tc_after();
-        uint32_t r[16];
-        TC_LD16(lane_base + kTmemS + sb_i * kN + s16, r);
+        uint32_t r[24];
+        TC_LD16L_X4(tl + kTmemS + sb_i * kN, r);
+        TC_LD16L_X2(tl + kTmemS + sb_i * kN + 32, (r + 16));
         tc_wait_ld();
 #pragma unroll
-        for (int k = 0; k < 16; ++k) sc[k] = __uint_as_float(r[k]);
+        for (int k = 0; k < 24; ++k) sc[k] = __uint_as_float(r[k]);
         tc_before();
         __syncwarp();
         if (lane == 0) bar_arrive(&bars->sfree[sb_i]);   // QK of tile i + kSBufs may overwrite
       }
-      // + the peer's partial (rounded to 24 bits): positions s16 .. s16 + 15
-      // are code words 12 slot .. 12 slot + 11, rows 3 slot .. 3 slot + 2
+      // + the peer's partial (rounded to 24 bits), sent by the peer's sender
+      // thread that holds the same fragment
       const int xb = xsel(i);
       ok = ok && wt.wait(&bars->xfull[xb], xpar(i));
       {
-        const uint4* xr = reinterpret_cast<const uint4*>(xbuf(xb)) + hl;
-        uint32_t w[12];
+        const uint8_t* xr = xbuf(xb) + quad * C::kXQuad;
+        uint32_t w[18];
 #pragma unroll
-        for (int q = 0; q < 3; ++q) {
-          const uint4 v = xr[64 * (3 * slot + q)];
+        for (int q = 0; q < 4; ++q) {
+          const uint4 v = *reinterpret_cast<const uint4*>(xr + 512 * q + 16 * lane);
           w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
         }
+        const uint2 v2 = *reinterpret_cast<const uint2*>(xr + 2048 + 8 * lane);
+        w[16] = v2.x; w[17] = v2.y;
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 6; ++k) {
           const float4 v = unpack24(w[3 * k], w[3 * k + 1], w[3 * k + 2]);
           const float2 a = __fadd2_rn(make_float2(sc[4 * k], sc[4 * k + 1]), make_float2(v.x, v.y));
           const float2 c2 = __fadd2_rn(make_float2(sc[4 * k + 2], sc[4 * k + 3]), make_float2(v.z, v.w));
@@ -832,7 +878,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         // registers, so no release ordering is needed
         if (lane == 0) bar_arrive_remote_relaxed(rxe0 + xb * 8u);
       }
-      // masked scores and the tile maximum of the head.  With a positive
+      // masked scores and the tile maxima of the two heads.  With a positive
       // scale the scores stay unscaled here: round-to-nearest is monotone, so
       // the maximum of the scaled scores is the scaled maximum, and P below
       // takes scale and reference in one fused multiply-add.  (A scale <= 0
@@ -840,90 +886,92 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       const int valid = min(kN, u.t1 - (u.t0 + i * kN));
       if (!pos_scale) {
 #pragma unroll
-        for (int k = 0; k < 16; ++k) sc[k] *= sl2;
+        for (int k = 0; k < 24; ++k) sc[k] *= sl2;
       }
       if (valid < kN) {   // the unit's last tile
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-          if (s16 + k >= valid) sc[k] = -INFINITY;
+        for (int k = 0; k < 24; ++k)
+          if (8 * (k >> 2) + 2 * fc + (k & 1) >= valid) sc[k] = -INFINITY;
       }
-      float mx[4] = {sc[0], sc[1], sc[2], sc[3]};
+      float xa = fmaxf(sc[0], sc[1]), xbm = fmaxf(sc[2], sc[3]);
 #pragma unroll
-      for (int k = 4; k < 16; ++k) mx[k & 3] = fmaxf(mx[k & 3], sc[k]);
-      const float mloc = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-      bars->pm[i & 1][slot][hl] = pos_scale ? mloc * sl2 : mloc;
-      quad_sync(quad);
-      const float mt = fmaxf(fmaxf(bars->pm[i & 1][0][hl], bars->pm[i & 1][1][hl]), bars->pm[i & 1][2][hl]);
-      // lazy rescale of the running reference max
-      const bool need = ok && mt > m_ref + kRescaleThreshold;
-      float alpha = 1.f;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? mt : m_ref;
-        alpha = exp2f(m_ref - m_new);   // 0 when m_ref = -inf
+      for (int k = 1; k < 6; ++k) {
+        xa = fmaxf(xa, fmaxf(sc[4 * k], sc[4 * k + 1]));
+        xbm = fmaxf(xbm, fmaxf(sc[4 * k + 2], sc[4 * k + 3]));
+      }
+      xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 1));
+      xbm = fmaxf(xbm, __shfl_xor_sync(0xffffffffu, xbm, 1));
+      xa = fmaxf(xa, __shfl_xor_sync(0xffffffffu, xa, 2));
+      xbm = fmaxf(xbm, __shfl_xor_sync(0xffffffffu, xbm, 2));
+      const float mtA = pos_scale ? xa * sl2 : xa, mtB = pos_scale ? xbm * sl2 : xbm;
+      // lazy rescale of the running reference maxima
+      const bool needA = ok && mtA > mA + kRescaleThreshold, needB = ok && mtB > mB + kRescaleThreshold;
+      float alA = 1.f, alB = 1.f;
+      if (__any_sync(0xffffffffu, needA || needB)) {
+        const float nA = needA ? mtA : mA, nB = needB ? mtB : mB;
+        alA = exp2f(mA - nA);   // 0 when the reference was -inf
+        alB = exp2f(mB - nB);
         if (i > 0) {
           // O holds tiles < i: wait for PV of tile i-1 (its P buffer's release;
           // the previous use of that buffer is known complete, so the parity
-          // wait cannot be fooled by a phase two steps back), then scale this
-          // thread's blocks of the lane's row (3, 3 and 2 of the 8)
+          // wait cannot be fooled by a phase two steps back), then scale the
+          // rows of this thread's two heads (the 16-lane access leaves the
+          // peer's rows of the quadrant to the rescaler)
           ok = ok && wt.wait(&bars->pfree[psel(i - 1)], ppar(i - 1));
+          __syncwarp();
           tc_after();
-#pragma unroll 1
-          for (int c = 3 * slot; c < 3 * slot + 3 && c < 8; ++c) {
-            uint32_t r[16], q[16];
-            TC_LD16(lane_base + kTmemO + 32 * c, r);
-            TC_LD16(lane_base + kTmemO + 32 * c + 16, q);
-            tc_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-              q[k] = __float_as_uint(__uint_as_float(q[k]) * alpha);
-            }
-            TC_ST16(lane_base + kTmemO + 32 * c, r);
-            TC_ST16(lane_base + kTmemO + 32 * c + 16, q);
-          }
-          tc_wait_st();
+          scale_rows16(tl, alA, alB);
         }
-        l *= alpha;
-        m_ref = m_new;
+        lA *= alA;
+        lB *= alB;
+        mA = nA;
+        mB = nB;
       }
-      // this thread's 16 positions of head h's P row (bf16): chunks 2 slot
-      // and 2 slot + 1, here and in the peer's buffer; l sums the fp32 values
-      // before their rounding.  Thread slot 0 also sends the head's rescale
-      // factor (chunk 6) and lane 0 the quadrant's "some head rescaled" flag
-      // (chunk 7 of the quadrant's first row).
+      // P of the two heads (bf16): the pair of positions of chunk k is 4 bytes
+      // at offset 4 fc of the chunk; l sums the fp32 values before rounding
       ok = ok && wt.wait(&bars->pfree[b], par ^ 1);
       uint8_t* prow = pbuf(b);
-      const uint32_t rp = rp0 + b * C::kPBytes, rbar = rbar0 + b * 8u;
-      if (slot == 0 && hl == 0) bar_arrive_expect_tx_remote(rbar, C::kPMsgBytes);
-      float2 ls = make_float2(0.f, 0.f);
-      const float2 ps2 = make_float2(ps, ps), nm2 = make_float2(-m_ref, -m_ref);
+      const float2 ps2 = make_float2(ps, ps), nA2 = make_float2(-mA, -mA), nB2 = make_float2(-mB, -mB);
+      float2 sA = make_float2(0.f, 0.f), sB = sA;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pk[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 t = __ffma2_rn(make_float2(sc[8 * c + 2 * k], sc[8 * c + 2 * k + 1]), ps2, nm2);
-          const float2 e = make_float2(ex2_approx(t.x), ex2_approx(t.y));
-          const __nv_bfloat162 two = __float22bfloat162_rn(e);
-          ls = __fadd2_rn(ls, e);
-          pk[k] = *reinterpret_cast<const uint32_t*>(&two);
-        }
-        const uint32_t off = c == 0 ? off_p0 : off_p1;
-        *reinterpret_cast<uint4*>(prow + off) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-        st_async_v4(rp + off, pk[0], pk[1], pk[2], pk[3], rbar);
+      for (int k = 0; k < 6; ++k) {
+        const float2 tA = __ffma2_rn(make_float2(sc[4 * k], sc[4 * k + 1]), ps2, nA2);
+        const float2 tB = __ffma2_rn(make_float2(sc[4 * k + 2], sc[4 * k + 3]), ps2, nB2);
+        const float2 eA = make_float2(ex2_approx(tA.x), ex2_approx(tA.y));
+        const float2 eB = make_float2(ex2_approx(tB.x), ex2_approx(tB.y));
+        sA = __fadd2_rn(sA, eA);
+        sB = __fadd2_rn(sB, eB);
+        const __nv_bfloat162 pa = __float22bfloat162_rn(eA), pb = __float22bfloat162_rn(eB);
+        *reinterpret_cast<__nv_bfloat162*>(prow + swz_chunk(hA, k) + 4 * fc) = pa;
+        *reinterpret_cast<__nv_bfloat162*>(prow + swz_chunk(hB, k) + 4 * fc) = pb;
       }
-      if (slot == 0) {
-        // (tile 0 sets the first reference: O holds nothing yet)
-        const bool any = __any_sync(0xffffffffu, i > 0 && alpha != 1.f);
-        st_async_b32(rp + off_a, __float_as_uint(alpha), rbar);
+      lA += sA.x + sA.y;
+      lB += sB.x + sB.y;
+      __syncwarp();
+      // forward whole 16-byte chunks (written by the four threads of a head
+      // pair) to the peer's buffer, with the heads' rescale factors and the
+      // quadrant's "some head rescaled" flag
+      {
+        const uint32_t rp = rp0 + b * C::kPBytes, rbar = rbar0 + b * 8u;
+        if (quad == 0 && lane == 0) bar_arrive_expect_tx_remote(rbar, C::kPMsgBytes);
+#pragma unroll
+        for (int jj = 0; jj < 3; ++jj) {
+          const uint4 v = *reinterpret_cast<const uint4*>(prow + fwd[jj]);
+          st_async_v4(rp + fwd[jj], v.x, v.y, v.z, v.w, rbar);
+        }
+        // (tile 0 sets the first references: O holds nothing yet)
+        const bool any = __any_sync(0xffffffffu, i > 0 && (alA != 1.f || alB != 1.f));
+        if (fc == 0) {
+          st_async_b32(rp + off_aA, __float_as_uint(alA), rbar);
+          st_async_b32(rp + off_aB, __float_as_uint(alB), rbar);
+        }
         if (lane == 0) st_async_b32(rp + off_f, any ? 1u : 0u, rbar);
       }
-      l += ls.x + ls.y;
       if (!C::kConv && valid < kN) {
         // dense bf16 tail: rows past the unit hold whatever the cache holds
         // there; zero them so P = 0 never meets a non-finite value
         uint8_t* v = opl(j);
-        for (int idx = slot * 64 + hl; idx < (kN - valid) * 32; idx += 64 * 3) {
+        for (int idx = 32 * quad + lane; idx < (kN - valid) * 32; idx += 128) {
           const int row = valid + idx / 32, blk = (idx / 8) & 3, ch = idx & 7;
           *reinterpret_cast<uint4*>(v + blk * kBlkBytes + swz_chunk(row, ch)) = make_uint4(0, 0, 0, 0);
         }
@@ -933,11 +981,30 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       __syncwarp();
       if (lane == 0) bar_arrive(&bars->pfull[b]);
     }
-    // the row sum and log-sum-exp of the head are formed after the pool
-    // barrier below
-    bars->l_part[slot][hl] = l;
-    if (slot == 0) bars->m_fin[hl] = m_ref;
-    (void)ok;
+    // the heads' row sums (the four threads' parts), log-sum-exps, and the
+    // row sums sent to the peer for its normalisation of these rows
+    lA += __shfl_xor_sync(0xffffffffu, lA, 1);
+    lB += __shfl_xor_sync(0xffffffffu, lB, 1);
+    lA += __shfl_xor_sync(0xffffffffu, lA, 2);
+    lB += __shfl_xor_sync(0xffffffffu, lB, 2);
+    if (live && fc == 0) {
+      bars->l_own[hA] = lA;
+      bars->l_own[hB] = lB;
+      const uint32_t lbar = mapa(&bars->lpeer, peer);
+      if (quad == 0 && lane == 0) bar_arrive_expect_tx_remote(lbar, 64 * 4);
+      st_async_b32(mapa(&bars->l_peer[hA], peer), __float_as_uint(lA), lbar);
+      st_async_b32(mapa(&bars->l_peer[hB], peer), __float_as_uint(lB), lbar);
+      const bool fin = ok && !bars->abort;
+      const float lseA = (fin && lA > 0.f) ? (mA + log2f(lA)) * 0.69314718055994531f : -INFINITY;
+      const float lseB = (fin && lB > 0.f) ? (mB + log2f(lB)) * 0.69314718055994531f : -INFINITY;
+      if (!(u.flags & kUnitDirect)) {
+        p.ws.part_lse[(size_t)unit_id * p.H + hA] = lseA;
+        p.ws.part_lse[(size_t)unit_id * p.H + hB] = lseB;
+      } else if (p.lse) {
+        p.lse[(size_t)u.b * p.H + hA] = lseA;
+        p.lse[(size_t)u.b * p.H + hB] = lseB;
+      }
+    }
   } else if (C::kConv && conv_id >= 0) {
     // ------------------------------------------------------------ converter
     // raw slot r of tile i -> operand stage j, once the rows have landed and
@@ -996,43 +1063,28 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   }
 
   // -------------------------------------------------------------- epilogue
-  // Every pool warp meets here once its role is done.  The softmax threads
-  // have stored their row sums; the owner of each head (slot 0) forms its l
-  // and log-sum-exp and sends l to the peer.  Pool slots 0 and 1 of every
-  // quadrant (8 warps) then stage the O half (128 heads x 256 fp32), each
-  // row normalised by its head's l -- this CTA's heads from its own sums,
-  // the peer's heads from the peer's -- in four rounds of one 32-column block
-  // per thread: the TMA stores of the blocks a round completes leave while
-  // the next round is staged.  With the last PV complete in both CTAs, every
-  // stage, P and exchange buffer is idle, so the half is staged from offset 0.
-  // A sequence's only unit writes the final bf16 output (4 blocks of 64
-  // columns: two 32-column chunks each, complete after rounds 1 and 3) and
-  // log-sum-exp itself.
+  // Every pool warp meets here once its role is done; the softmax warps have
+  // stored their heads' row sums (and sent them to the peer).  The softmax
+  // and sender warps of every quadrant (8 warps) then stage the O half (128
+  // heads x 256 fp32), each row normalised by its head's l -- this CTA's
+  // heads from its own sums, the peer's heads from the peer's -- in four
+  // rounds of one 32-column block per thread: the TMA stores of the blocks a
+  // round completes leave while the next round is staged.  With the last PV
+  // complete in both CTAs, every stage, P and exchange buffer is idle, so the
+  // half is staged from offset 0.  A sequence's only unit writes the final
+  // bf16 output (4 blocks of 64 columns: two 32-column chunks each, complete
+  // after rounds 1 and 3) itself.
   if (live && pool) {
     pool_sync();
-    const int hl = hq & 63;
-    if (own_q && slot == 0) {
-      const float lt = bars->l_part[0][hl] + bars->l_part[1][hl] + bars->l_part[2][hl];
-      const float m = bars->m_fin[hl];
-      const uint32_t lbar = mapa(&bars->lpeer, peer);
-      if (hl == 0) bar_arrive_expect_tx_remote(lbar, 64 * 4);
-      st_async_b32(mapa(&bars->l_peer[hl], peer), __float_as_uint(lt), lbar);
-      const bool finite = !bars->abort && lt > 0.f;
-      const float lse = finite ? (m + log2f(lt)) * 0.69314718055994531f : -INFINITY;
-      if (!(u.flags & kUnitDirect))
-        p.ws.part_lse[(size_t)unit_id * p.H + hq] = lse;
-      else if (p.lse)
-        p.lse[(size_t)u.b * p.H + hq] = lse;
-    }
     if (slot < 2) {
       bool ok = true;
       if (ntiles > 0) ok = wt.wait(&bars->pfree[psel(ntiles - 1)], ppar(ntiles - 1));
       float lt;
-      if (own_q) {
-        lt = bars->l_part[0][hl] + bars->l_part[1][hl] + bars->l_part[2][hl];
+      if (own_lane) {
+        lt = bars->l_own[hq];
       } else {
         ok = wt.wait(&bars->lpeer, 0) && ok;
-        lt = bars->l_peer[hl];
+        lt = bars->l_peer[hq];
       }
       __syncwarp();   // the tensor-memory loads below are warp-collective
       tc_after();

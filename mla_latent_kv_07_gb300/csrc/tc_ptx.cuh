@@ -46,6 +46,14 @@ __device__ __forceinline__ void st_async_v4(uint32_t remote_addr, uint32_t a, ui
                "r"(a), "r"(b), "r"(c), "r"(d), "r"(remote_bar)
                : "memory");
 }
+// 8 bytes into a peer CTA's shared memory, counted on the peer's barrier when
+// they land
+__device__ __forceinline__ void st_async_v2(uint32_t remote_addr, uint32_t a, uint32_t b, uint32_t remote_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(
+                   remote_addr),
+               "r"(a), "r"(b), "r"(remote_bar)
+               : "memory");
+}
 // 4 bytes into a peer CTA's shared memory, counted on the peer's barrier when
 // they land
 __device__ __forceinline__ void st_async_b32(uint32_t remote_addr, uint32_t v, uint32_t remote_bar) {
@@ -174,6 +182,29 @@ __device__ __forceinline__ void mma_commit_mc(uint64_t* b, uint16_t mask) {
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),    \
                  "=r"(r[6]), "=r"(r[7])                                                    \
                : "r"(taddr))
+// 16 lanes (the lane field of taddr onwards) x 32 / 16 fp32 columns: thread
+// t holds lanes t/4 and t/4 + 8 at columns 8k + 2 (t%4) and 8k + 2 (t%4) + 1,
+// r[4k .. 4k+3] = (lane t/4: both columns, then lane t/4 + 8: both columns)
+#define TC_LD16L_X4(taddr, r)                                                                    \
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12," \
+               "%13,%14,%15}, [%16];"                                                            \
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),         \
+                 "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]),       \
+                 "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])                              \
+               : "r"(taddr))
+#define TC_LD16L_X2(taddr, r)                                                                  \
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"       \
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),       \
+                 "=r"(r[6]), "=r"(r[7])                                                        \
+               : "r"(taddr))
+// the store counterpart of TC_LD16L_X4 (same thread / register layout)
+#define TC_ST16L_X4(taddr, r)                                                                          \
+  asm volatile("tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13," \
+               "%14,%15,%16};" ::"r"(taddr),                                                           \
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),  \
+               "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),       \
+               "r"(r[15])                                                                              \
+               : "memory")
 #define TC_ST16(taddr, r)                                                                     \
   asm volatile(                                                                               \
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12," \
