@@ -1030,8 +1030,13 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
             dequant16(v, sc, lo, hi);
           }
           const int blk = q >> 2, ch = (q & 3) * 2;
-          *reinterpret_cast<uint4*>(dst + blk * kBlkBytes + swz_chunk(row, ch)) = lo;
-          *reinterpret_cast<uint4*>(dst + blk * kBlkBytes + swz_chunk(row, ch + 1)) = hi;
+          // odd blocks store their odd chunk first: a quarter-warp (two blocks
+          // of one row) then covers all eight chunk positions of the
+          // 128-byte swizzle row per store, free of bank conflicts
+          const bool flip = blk & 1;
+          const uint4 v1 = flip ? hi : lo, v2 = flip ? lo : hi;
+          *reinterpret_cast<uint4*>(dst + blk * kBlkBytes + swz_chunk(row, ch + (flip ? 1 : 0))) = v1;
+          *reinterpret_cast<uint4*>(dst + blk * kBlkBytes + swz_chunk(row, ch + (flip ? 0 : 1))) = v2;
         }
       } else {
         // gathered bf16 rows: 48 rows x 32 chunks of 8 values
