@@ -35,7 +35,7 @@
 // Tensor memory (512 columns): O half [0,256) fp32; Q half [256,400) bf16 (2
 // per column); S double buffer [400,448) and [448,496) fp32.
 //
-// Warp roles (512 threads; 544 with a converter):
+// Warp roles (512 threads; 544 for dense FP8 tiles):
 //   warp 0  producer: TMA tiles (dense) or four-row TMA gathers (gather)
 //   warp 1  QK issuer (one thread) and tensor-memory owner
 //   warp 2  PV issuer (one thread); in a dense bf16 call it first works out
@@ -51,7 +51,7 @@
 //                 row (the cache-write step)
 //           12-15 converter (if any)
 //           Slots 4-11 stage the output half in the epilogue.
-//   warps 3, 16 and 12-15  converter (FP8 caches and gathers): raw rows ->
+//   warps 3, 12-15 and (dense FP8) 16  converter (FP8 caches and gathers): raw rows ->
 //           bf16 operand tile bf16(fp32(e4m3 * scale)) in the 128-byte
 //           swizzled layout
 // Distributed shared memory moves ~20-35 GB/s per SM with ~0.3 us latency on
@@ -87,7 +87,6 @@ constexpr int kPeHalf = kDr / 2;           // 32 rotary columns per CTA
 constexpr float kRescaleThreshold = 16.0f;
 constexpr uint32_t kTmemO = 0, kTmemQ = 256, kTmemS = 400;
 constexpr long kSpinLimit = 1L << 26;   // polls (~seconds) before giving up
-constexpr int kConvWarps = 6;             // converter: warps 3, 16 and the pool's four slot-2 warps
 
 // Shared-memory plan per variant.  Tiles are 48 positions (MMA N for QK, K
 // for PV), with two S, P and exchange buffers.  An operand stage holds the
@@ -112,9 +111,14 @@ struct Cfg {
   // schedule first), 3 converter; 4-15 the head pool, three warps per TMEM
   // lane quadrant (quadrant = warp & 3, slot = (warp - 4) >> 2: softmax,
   // sender/rescaler, converter); 16 converter.  Variants without a converter
-  // stop at warp 15 (warp 3 and the pool's third slot idle).
+  // stop at warp 15 (warp 3 and the pool's third slot idle), and so do the
+  // gather variants: with five converter warps they run at 128 registers a
+  // thread (sixteen warps; seventeen are allocated as twenty, 96 registers),
+  // which measured faster for gathers (workload 5 kernel 39.8 -> 37.7 us) and
+  // slower for dense FP8 tiles (workload 4 203 -> 208 us).
   static constexpr int kSmWarps = 4;   // softmax warps: one per TMEM lane quadrant
-  static constexpr int kThreads = 32 * (kConv ? 17 : 16);
+  static constexpr int kConvWarps = kSparse ? 5 : 6;   // warp 3, the pool's four slot-2 warps, warp 16
+  static constexpr int kThreads = 32 * (kConv && !kSparse ? 17 : 16);
   // QK may be issued at most this many tiles past the last issued PV: enough
   // run-ahead to keep the tensor pipe busy through the exchange and softmax
   // of a tile, no more -- the pipe runs its queue in order, so each queued QK
@@ -395,8 +399,9 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   // 16-lane fragments (TC_LD16L_*): this thread holds heads base + fl and
   // base + fl + 8 at the column pairs 8k + 2 fc, 8k + 2 fc + 1
   const int fl = lane >> 2, fc = lane & 3;
-  // converter warps: 3, 16 and the pool's third slot (one per quadrant)
-  const int conv_id = warp == 3 ? 0 : warp == 16 ? 1 : (pool && slot == 2) ? 2 + quad : -1;
+  // converter warps: 3, 16 (dense FP8) and the pool's third slot (one per
+  // quadrant)
+  const int conv_id = warp == 3 ? 0 : warp == 16 ? 1 : (pool && slot == 2) ? C::kConvWarps - 4 + quad : -1;
 
   auto opl = [&](int j) { return sm + j * C::kStage; };               // operand stage j
   auto ope = [&](int j) { return sm + j * C::kStage + kOplBytes; };
@@ -418,10 +423,10 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int j = 0; j < C::kStages; ++j) {
       bar_init(&bars->full[j], 1);
-      bar_init(&bars->deq[j], kConvWarps);
+      bar_init(&bars->deq[j], C::kConvWarps);
       bar_init(&bars->empty[j], 1);
     }
-    for (int r = 0; r < C::kRawSlots; ++r) bar_init(&bars->rfree[r], kConvWarps);
+    for (int r = 0; r < C::kRawSlots; ++r) bar_init(&bars->rfree[r], C::kConvWarps);
     for (int b = 0; b < C::kPBufs; ++b) {
       bar_init(&bars->pfull[b], C::kSmWarps);
       bar_init(&bars->pfree[b], 2);    // both CTAs' PV commits
@@ -1008,7 +1013,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   } else if (C::kConv && conv_id >= 0) {
     // ------------------------------------------------------------ converter
     // raw slot r of tile i -> operand stage j, once the rows have landed and
-    // PV of the stage's previous tile is done; kConvWarps warps share a tile
+    // PV of the stage's previous tile is done; C::kConvWarps warps share a tile
     const int t = 32 * conv_id + lane;
     for (int i = 0; i < ntiles; ++i) {
       const int r = i % C::kRawRing, j = i % C::kStages;
@@ -1020,7 +1025,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       uint8_t* dst = opl(j);
       if (kFmt == 1) {
         // 48 rows x 16 chunks of 16 codes -> 2 swizzled 16-byte chunks each
-        for (int idx = t; idx < kN * 16; idx += 32 * kConvWarps) {
+        for (int idx = t; idx < kN * 16; idx += 32 * C::kConvWarps) {
           const int row = idx >> 4, q = idx & 15;  // codes [16q, 16q + 16) of the half row
           uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
           if (row < valid) {
@@ -1040,7 +1045,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         }
       } else {
         // gathered bf16 rows: 48 rows x 32 chunks of 8 values
-        for (int idx = t; idx < kN * 32; idx += 32 * kConvWarps) {
+        for (int idx = t; idx < kN * 32; idx += 32 * C::kConvWarps) {
           const int row = idx >> 5, q = idx & 31;
           uint4 v = make_uint4(0, 0, 0, 0);
           if (row < valid) v = *reinterpret_cast<const uint4*>(raw(r) + row * C::kRawRow + q * 16);
@@ -1052,7 +1057,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       // ones its QK reads)
       constexpr int kPeChunks = C::kRawPe / 16;
       const int pe_chunk0 = kPeChunks == 8 ? 0 : 4 * (int)rank;
-      for (int idx = t; idx < kN * kPeChunks; idx += 32 * kConvWarps) {
+      for (int idx = t; idx < kN * kPeChunks; idx += 32 * C::kConvWarps) {
         const int row = idx / kPeChunks, q = idx % kPeChunks;
         uint4 v = make_uint4(0, 0, 0, 0);
         if (row < valid) v = *reinterpret_cast<const uint4*>(rpe(r) + row * C::kRawPe + q * 16);
