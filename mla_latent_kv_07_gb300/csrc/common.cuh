@@ -124,6 +124,10 @@ struct DenseSchedule {
   int max_end_pos, B, target, granule, mtp_s;
   int direct;           // a sequence with a single unit is finished by the decode
   int append;           // the call writes row end_pos - 1 (the last unit does)
+  // a sparse call: the lengths are the gather counts and the status bits the
+  // per-sequence flags, both written by the gather-list prep (end_pos unused)
+  const int* lengths = nullptr;
+  const uint32_t* seq_flags = nullptr;
 };
 
 // Parameters of the decode kernels.

@@ -467,12 +467,12 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   pdl_wait();
   pdl_trigger();
   const Unit u = [&]() -> Unit {
-    // only the dense bf16 variant computes its schedule (the FP8 variant
-    // keeps the schedule kernel; see the host launcher)
-    if constexpr (kSparse || kFmt != 0) {
+    // the dense bf16 and the gather variants compute their schedule (the
+    // dense FP8 variant keeps the schedule kernel; see the host launcher)
+    if constexpr (!kSparse && kFmt != 0) {
       return p.ws.units[unit_id];
     } else {
-      if (p.sched.end_pos == nullptr) return p.ws.units[unit_id];
+      if (p.sched.end_pos == nullptr && p.sched.lengths == nullptr) return p.ws.units[unit_id];
       // warp 2 works out the schedule and this pair's unit (the first pair's
       // rank-0 CTA also writes the combine's per-sequence table, the unit
       // count and the call's status word, afresh)

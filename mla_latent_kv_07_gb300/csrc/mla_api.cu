@@ -181,13 +181,15 @@ mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cuda
   const int target =
       tc ? mla::decode_tc_units(mla::decode_fmt(a.cache->fmt), K > 0, sms) : mla::target_units_mma(a.H, sms);
   const int granule = tc ? mla::decode_tc_granule(mla::decode_fmt(a.cache->fmt), K > 0) : mla::decode_mma_granule();
-  // dense bf16 calls of up to kWarpScheduleMaxB sequences on the
-  // tensor-memory kernel: every CTA pair works out its own unit, so no
-  // schedule kernel sits between the call's start and its first loads.  (The
-  // FP8 variant runs at its register limit, where the added code cost more
-  // than it saved; long calls -- prefill chunks -- keep the schedule kernel.)
+  // dense bf16 and sparse calls of up to kWarpScheduleMaxB sequences on the
+  // tensor-memory kernel: every CTA pair works out its own unit (a sparse
+  // call from the gather counts the prep kernel wrote), so no schedule kernel
+  // sits between the call's start (or its prep) and the first loads.  (The
+  // dense FP8 variant runs at its register limit, where the added code cost
+  // more than it saved; long calls -- prefill chunks -- keep the schedule
+  // kernel.)
   const bool fused_schedule =
-      tc && K == 0 && mla::decode_fmt(a.cache->fmt) == 0 && a.B <= mla::kWarpScheduleMaxB;
+      tc && a.B <= mla::kWarpScheduleMaxB && (K > 0 || mla::decode_fmt(a.cache->fmt) == 0);
   if (!fused_schedule) {
     e = mla::launch_schedule(K ? nullptr : a.end_pos, a.max_end_pos, ws, a.B, target, granule, tc, a.mtp_s,
                              ap != nullptr, s);
@@ -199,8 +201,10 @@ mla_status run_decode(const DecodeArgs& a, const mla::Workspace& ws, int K, cuda
   p.spin_limit = spin_limit;
   p.withhold_tile = withhold_tile;
   if (ap && tc) p.ap = *ap;
-  if (fused_schedule)
+  if (fused_schedule && K == 0)
     p.sched = mla::DenseSchedule{a.end_pos, a.max_end_pos, a.B, target, granule, a.mtp_s, 1, ap != nullptr ? 1 : 0};
+  else if (fused_schedule)
+    p.sched = mla::DenseSchedule{nullptr, a.max_end_pos, a.B, target, granule, 1, 1, 0, ws.lengths, ws.seq_flags};
   e = tc ? mla::launch_decode_tc(p, s) : mla::launch_decode_mma(p, s);
   trace_stop(s, traced);
   if (e != cudaSuccess) return cuda_fail(e, "decode");

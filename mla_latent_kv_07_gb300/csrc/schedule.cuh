@@ -1,7 +1,8 @@
-// schedule.cuh -- the split schedule of a dense call computed by one warp,
-// for the tensor-memory decode kernel: every CTA finds its own unit from
-// end_pos, so no schedule kernel (and no unit table round trip) sits between
-// the call's start and its first cache load.  The rule is schedule_kernel's
+// schedule.cuh -- the split schedule of a call computed by one warp, for the
+// tensor-memory decode kernel: every CTA finds its own unit from end_pos (a
+// dense call) or from the gather counts the list prep wrote (a sparse call),
+// so no schedule kernel (and no unit table round trip) sits between the
+// call's start, or the prep, and the first cache load.  The rule is schedule_kernel's
 // (aux_kernels.cu): lengths cut into units of `chunk` positions, chunk the
 // smallest granule multiple with sum_b ceil(len_b / chunk) <= target, capped
 // at the longest length.
@@ -45,8 +46,13 @@ __device__ Unit warp_schedule(const DenseSchedule& s, int want, uint32_t* flags_
     if (r < nblk) {
       const int b = lane + 32 * r;
       if (b < s.B) {
-        len[r] = dense_len(s, b, &flags);
-        if (s.append && s.mtp_s == 1 && !append_row_valid(s.end_pos[b], s.max_end_pos)) flags |= kDevAppendSkipped;
+        if (s.lengths) {
+          len[r] = s.lengths[b];
+          flags |= s.seq_flags[b];
+        } else {
+          len[r] = dense_len(s, b, &flags);
+          if (s.append && s.mtp_s == 1 && !append_row_valid(s.end_pos[b], s.max_end_pos)) flags |= kDevAppendSkipped;
+        }
       }
       hi += len[r] >> 7;
       lo += len[r] & 127;
