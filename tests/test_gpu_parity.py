@@ -402,6 +402,29 @@ def test_sparse_small_lists_and_outputs():
     check_close(f64(lse).reshape(-1), ref_lse, "lse")
 
 
+def test_sparse_empty_split_and_single_unit_sequences():
+    # one sequence with nothing to gather (every entry -1 or out of range), one
+    # long list split over several units (combined inside the decode kernel),
+    # one short list (a single unit); every output and log-sum-exp checked
+    B, S, H, K = 3, 4096, 128, 1024
+    oc = oracle_cache(_rand_bf16((B, S, 512), 61), _rand_bf16((B, S, 64), 62), 1)
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((B, H, 512), 63), _rand_bf16((B, H, 64), 64)
+    ends = np.array([4096, 4096, 4096], np.int32)
+    rng = np.random.default_rng(65)
+    topk = np.full((B, K), -1, np.int32)
+    topk[0, :5] = [4096, 5000, -3, 4097, 9999]          # all out of range: nothing gathered
+    topk[1] = rng.permutation(4096)[:K]
+    topk[2, :7] = [3, 900, 17, 4095, 2048, 17, 0]
+    out, lse = mla.decode_sparse(dc, ql.cuda(), qp.cuda(), torch.from_numpy(ends).cuda(), S, 0.15,
+                                 torch.from_numpy(topk).cuda())
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), ends, 0.15, topk=topk)
+    got = f64(out).reshape(B, H, 512)
+    assert np.all(got[0] == 0.0) and np.all(np.isneginf(f64(lse).reshape(B, H)[0]))
+    check_close(got[1:].reshape(-1, 512), ref.reshape(B, H, 512)[1:].reshape(-1, 512), "out")
+    check_close(f64(lse).reshape(B, H)[1:].reshape(-1), ref_lse.reshape(B, H)[1:].reshape(-1), "lse")
+
+
 @pytest.mark.parametrize("fmt", [1, 2])
 def test_sparse_fused_append_sees_the_new_row(fmt):
     B, S, H, K = 3, 128, 128, 64
