@@ -290,6 +290,52 @@ def test_kernel_schedule_matches_schedule_kernel(ends, max_end, S, s):
     assert (seq[:, 1] >= -1).all() and hdr[0][1] >= int((seq[:, 1] != 0).sum())
 
 
+def test_sparse_kernel_schedule_matches_schedule_kernel():
+    # sparse calls of up to 128 sequences compute the split schedule inside the
+    # decode kernel from the gather counts; a dense FP8 call with end_pos equal
+    # to those counts runs the schedule kernel on the same lengths, so the
+    # status word, unit count and per-sequence table must agree byte for byte
+    counts = [0, 1, 47, 48, 49, 700, 2048, 95, 96, 1500, 3, 333, 2047, 1024, 511, 5, 0, 1999]
+    B, H, S, K = len(counts), 128, 4096, 2048
+    rng = np.random.default_rng(157)
+    topk = np.full((B, K), -1, np.int32)
+    for b, c in enumerate(counts):
+        topk[b, :c] = rng.permutation(S)[:c]
+    ql, qp = _rand_bf16((B, H, 512), 158).cuda(), _rand_bf16((B, H, 64), 159).cuda()
+    tables = []
+    ws = mla.alloc_workspace(B, H, S, K)
+    mla.decode_sparse(mla.Cache(B, S, 1), ql, qp, torch.full((B,), S, dtype=torch.int32).cuda(), S, 0.1,
+                      torch.from_numpy(topk).cuda(), workspace=ws)
+    torch.cuda.synchronize()
+    tables.append(ws[:256 + 8 * B].cpu().numpy())
+    ws = mla.alloc_workspace(B, H, S)
+    mla.decode(mla.Cache(B, S, 1), ql, qp, torch.tensor(counts, dtype=torch.int32).cuda(), S, 0.1, workspace=ws)
+    torch.cuda.synchronize()
+    tables.append(ws[:256 + 8 * B].cpu().numpy())
+    hdr = [tb[:8].view(np.int32) for tb in tables]
+    assert hdr[0][0] == hdr[1][0] and hdr[0][1] == hdr[1][1], hdr
+    assert np.array_equal(tables[0][256:], tables[1][256:])
+
+
+def test_sparse_more_sequences_than_the_in_kernel_schedule_takes():
+    # 130 sequences: the sparse call runs the schedule kernel (the in-kernel
+    # schedule holds at most 128 lengths); sampled outputs against the oracle
+    B, S, H, K = 130, 512, 128, 64
+    oc = oracle_cache(_rand_bf16((B, S, 512), 161), _rand_bf16((B, S, 64), 162), 1)
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((B, H, 512), 163), _rand_bf16((B, H, 64), 164)
+    rng = np.random.default_rng(165)
+    ends = rng.integers(1, S + 1, B).astype(np.int32)
+    topk = rng.integers(-1, S, (B, K)).astype(np.int32)
+    out, lse = mla.decode_sparse(dc, ql.cuda(), qp.cuda(), torch.from_numpy(ends).cuda(), S, 0.13,
+                                 torch.from_numpy(topk).cuda())
+    pairs = sample_pairs(B, H, 2, seed=166)
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), ends, 0.13, pairs=pairs, topk=topk)
+    got = f64(out).reshape(B, H, 512)[pairs[:, 0], pairs[:, 1]]
+    check_close(got, ref, "out")
+    check_close(f64(lse).reshape(B, H)[pairs[:, 0], pairs[:, 1]], ref_lse, "lse")
+
+
 @pytest.mark.parametrize("fmt", [0, 1])
 def test_bounded_wait_runs_out_and_reports(fmt):
     # the self-test withholds the first unit's first tile: its waits run out
