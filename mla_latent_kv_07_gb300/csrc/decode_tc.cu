@@ -22,8 +22,9 @@
 //     its top 24 bits; asynchronous remote stores, counted on the receiver's
 //     barrier), where they are added to the peer's own fp32 partial.
 //   * softmax: each CTA runs the online softmax of its own 64 heads only and
-//     writes their bf16 P rows into its own P buffer and, by asynchronous
-//     remote stores, into the peer's, with each head's rescale factor.
+//     writes their bf16 P rows into its own P buffer and into the peer's
+//     (bulk copies of whole rows, or remote stores of 16-byte chunks for
+//     dense bf16), with each head's rescale factor.
 //   * PV: each CTA multiplies P of all 128 heads (shared memory) by its latent
 //     half V (the same shared-memory tile, read as an MN-major operand) into
 //     its own O half.  When the owner of a head raised the head's reference
@@ -55,7 +56,7 @@
 //           bf16 operand tile bf16(fp32(e4m3 * scale)) in the 128-byte
 //           swizzled layout
 // Distributed shared memory moves ~20-35 GB/s per SM with ~0.3 us latency on
-// this part, so each tile sends 9 KB of partial scores and 6.3 KB of P rows
+// this part, so each tile sends 9 KB of partial scores and 6-8 KB of P rows
 // per direction.
 //
 // Every wait is bounded; on expiry the kernel raises a status bit, stops
@@ -96,7 +97,11 @@ constexpr long kSpinLimit = 1L << 26;   // polls (~seconds) before giving up
 // stored -- FP8 codes or gathered bf16 half rows, the 4 FP8 scales of each
 // row, the 64 rotary values -- into a separate ring of raw slots, which the
 // converter frees as soon as it has read them.  So a load never waits for a
-// PV, and the HBM latency stays out of the operand stages' cycle.
+// PV, and the HBM latency stays out of the operand stages' cycle.  The dense
+// FP8 variant fills 227 KB exactly: four operand stages (the rotary operand
+// only the CTA's 32 columns), four raw slots (the ring's cycle -- a load's
+// latency plus the conversion -- bounds the tile period with three), two P
+// and two exchange buffers.
 template <int kFmt, bool kSparse>
 struct Cfg {
   static constexpr bool kConv = kFmt == 1 || kSparse;       // converter warps present
@@ -127,7 +132,11 @@ struct Cfg {
   static constexpr int kQkAhead = 4;
   static constexpr int kBlkBytes = kN * 128;       // one 64-column swizzled block of a tile
   static constexpr int kOplBytes = 4 * kBlkBytes;  // latent half operand
-  static constexpr int kOpeBytes = kBlkBytes;      // rotary operand (full 64 columns)
+  // rotary operand: dense bf16 tiles land the full 64 columns (128-byte
+  // swizzle, as stored); the converter variants write only the CTA's 32
+  // columns (the ones its QK reads) as 8-row x 16-byte core matrices without
+  // swizzle: core (row group g, chunk c) at 512 g + 128 c
+  static constexpr int kOpeBytes = kConv ? kN * 64 : kBlkBytes;
   // P: 128 heads x kN bf16, swizzled (rows of 64 positions: chunks 6 and 7 of
   // a row are padding, which carries the peer's rescale factors and flags)
   static constexpr int kPBytes = ((kN + 63) / 64) * kSwBlk;
@@ -144,9 +153,12 @@ struct Cfg {
   static constexpr int kXQuad = 32 * 72;
   static constexpr int kXBytes = 4 * kXQuad;
   static constexpr int kXStride = kFmt == 1 ? kXBytes : 2 * kXBytes;
-  // bytes of one tile's message of P rows to the peer: 64 rows x kN bf16,
-  // one rescale factor per row, one flag word per quadrant
-  static constexpr uint32_t kPMsgBytes = 64 * kN * 2 + 64 * 4 + 4 * 4;
+  // bytes of one tile's message of P rows to the peer: variants with a
+  // converter send one block of 16 whole rows (128 bytes, padding included)
+  // from each quadrant's softmax warp by bulk copy; dense bf16 sends the 64
+  // rows' kN positions by remote stores of 16-byte chunks, one rescale factor
+  // per row and one flag word per quadrant (measured faster there)
+  static constexpr uint32_t kPMsgBytes = kConv ? 4 * 16 * 128 : 64 * kN * 2 + 64 * 4 + 4 * 4;
   static constexpr int kStage = kOplBytes + kOpeBytes;
   static constexpr int kStages = kConv ? (kFmt == 1 ? 4 : 2) : 4;
   static constexpr int kRawRow = kFmt == 1 ? kHalf : kHalf * 2;  // bytes of a raw latent half row
@@ -158,7 +170,7 @@ struct Cfg {
   // 32 its QK reads); gathers land whole 128-byte rows
   static constexpr int kRawPe = (kFmt == 1 && !kSparse) ? kPeHalf * 2 : 128;
   static constexpr int kRaw = kConv ? kN * kRawRow + kScBytes + kN * kRawPe : 0;
-  static constexpr int kRawSlots = kConv ? (kFmt == 1 && !kSparse ? 3 : 2) : 0;
+  static constexpr int kRawSlots = kConv ? (kFmt == 1 ? (kSparse ? 3 : 4) : 2) : 0;
   // the converter's ring length in index arithmetic (never zero, so the
   // converter code of the variants without one compiles cleanly)
   static constexpr int kRawRing = kRawSlots > 0 ? kRawSlots : 1;
@@ -237,7 +249,7 @@ struct Bars {
   uint64_t full[4];    // tile landed: stage (dense bf16) or raw slot
   uint64_t deq[4];     // operand stage converted
   uint64_t empty[4];   // PV done: operand stage free
-  uint64_t rfree[3];   // raw slot read by the converter
+  uint64_t rfree[4];   // raw slot read by the converter
   uint64_t sfull[2], sfree[2];
   uint64_t pfull[3];   // P rows of this CTA's heads written (its softmax warps)
   uint64_t pfree[3];   // PV of the buffer's tile done in both CTAs (one multicast commit from each)
@@ -703,14 +715,15 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
         tc_after();
         const uint32_t sd = tmem + kTmemS + b * kN;
         const uint64_t kd = sdesc_at(d_k0, j * C::kStage);
-        const uint64_t ped = sdesc_at(kd, kOplBytes + rank * (kPeHalf * 2));
+        const uint64_t ped = C::kConv ? sdesc_plain(sa(ope(j)), 128, 512) : sdesc_at(kd, kOplBytes + rank * (kPeHalf * 2));
+        constexpr uint32_t kPeStep = C::kConv ? 256 : 32;   // bytes per 16 columns
         mma_ts_c<false>(sd, t_q, kd, id_qk);
 #pragma unroll
         for (int kk = 1; kk < kHalf / 16; ++kk)
           mma_ts_c<true>(sd, t_q + 8 * kk, sdesc_at(kd, (kk >> 2) * kBlkBytes + (kk & 3) * 32), id_qk);
 #pragma unroll
         for (int kk = 0; kk < kPeHalf / 16; ++kk)
-          mma_ts_c<true>(sd, t_q + kHalf / 2 + 8 * kk, sdesc_at(ped, 32 * kk), id_qk);
+          mma_ts_c<true>(sd, t_q + kHalf / 2 + 8 * kk, sdesc_at(ped, kPeStep * kk), id_qk);
         mma_commit(&bars->sfull[b]);
       }
       mma_commit(&bars->drain);
@@ -818,8 +831,12 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     // hA = base + t/4 and hB = hA + 8 at positions 8k + 2 (t%4) and
     // 8k + 2 (t%4) + 1 (k = 0..5), 12 per head; the four threads of a head
     // agree on its tile maximum by shuffles.  P is written into this CTA's
-    // buffer (4-byte pieces, then read back as 16-byte chunks) and, by
-    // asynchronous remote stores of those chunks, into the peer's.
+    // buffer (4-byte pieces) and sent to the peer's: with a converter, the
+    // warp's 16 rows by one bulk copy (shared memory to shared memory,
+    // counted on the peer's barrier), the rows' padding carrying the rescale
+    // factors and the quadrant's flag; dense bf16, as 16-byte chunks read
+    // back and sent by remote stores, the factors and flag stored beside
+    // them.
     const int hA = own_base + fl, hB = hA + 8;
     const uint32_t tl = tmem + ((uint32_t)own_base << 16);
     const float sl2 = p.scale_log2;
@@ -827,10 +844,10 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     const float ps = pos_scale ? sl2 : 1.f;   // the factor still to apply to sc in P
     float mA = -INFINITY, mB = -INFINITY, lA = 0.f, lB = 0.f;
     bool ok = true;
-    // loop-invariant addresses: this thread's exchange rows, the peer's P
-    // buffer 0, rpfull[0] and xempty[0] (buffer b of each is a fixed stride
-    // further), the three 16-byte P chunks this thread forwards (chunk
-    // c = fc + 4 j of its head pair: hA's chunks 0-5, then hB's)
+    // loop-invariant addresses: the peer's P buffer 0, rpfull[0] and
+    // xempty[0] (buffer b of each is a fixed stride further), and (dense
+    // bf16) the three 16-byte P chunks this thread forwards (chunk c = fc +
+    // 4 j of its head pair: hA's chunks 0-5, then hB's)
     const uint32_t rp0 = mapa(pbuf(0), peer), rbar0 = mapa(&bars->rpfull[0], peer);
     const uint32_t rxe0 = mapa(&bars->xempty[0], peer);
     uint32_t fwd[3];
@@ -953,24 +970,38 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       lA += sA.x + sA.y;
       lB += sB.x + sB.y;
       __syncwarp();
-      // forward whole 16-byte chunks (written by the four threads of a head
-      // pair) to the peer's buffer, with the heads' rescale factors and the
-      // quadrant's "some head rescaled" flag
+      // the P rows (written by all the warp's threads) to the peer's buffer,
+      // with the heads' rescale factors and the quadrant's "some head
+      // rescaled" flag
       {
         const uint32_t rp = rp0 + b * C::kPBytes, rbar = rbar0 + b * 8u;
-        if (quad == 0 && lane == 0) bar_arrive_expect_tx_remote(rbar, C::kPMsgBytes);
-#pragma unroll
-        for (int jj = 0; jj < 3; ++jj) {
-          const uint4 v = *reinterpret_cast<const uint4*>(prow + fwd[jj]);
-          st_async_v4(rp + fwd[jj], v.x, v.y, v.z, v.w, rbar);
-        }
         // (tile 0 sets the first references: O holds nothing yet)
         const bool any = __any_sync(0xffffffffu, i > 0 && (alA != 1.f || alB != 1.f));
-        if (fc == 0) {
-          st_async_b32(rp + off_aA, __float_as_uint(alA), rbar);
-          st_async_b32(rp + off_aB, __float_as_uint(alB), rbar);
+        if constexpr (C::kConv) {
+          if (fc == 0) {
+            *reinterpret_cast<float*>(prow + off_aA) = alA;
+            *reinterpret_cast<float*>(prow + off_aB) = alB;
+          }
+          if (lane == 0) *reinterpret_cast<uint32_t*>(prow + off_f) = any ? 1u : 0u;
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            if (quad == 0) bar_arrive_expect_tx_remote(rbar, C::kPMsgBytes);
+            bulk_s2c(rp + own_base * 128, prow + own_base * 128, 16 * 128, rbar);
+          }
+        } else {
+          if (quad == 0 && lane == 0) bar_arrive_expect_tx_remote(rbar, C::kPMsgBytes);
+#pragma unroll
+          for (int jj = 0; jj < 3; ++jj) {
+            const uint4 v = *reinterpret_cast<const uint4*>(prow + fwd[jj]);
+            st_async_v4(rp + fwd[jj], v.x, v.y, v.z, v.w, rbar);
+          }
+          if (fc == 0) {
+            st_async_b32(rp + off_aA, __float_as_uint(alA), rbar);
+            st_async_b32(rp + off_aB, __float_as_uint(alB), rbar);
+          }
+          if (lane == 0) st_async_b32(rp + off_f, any ? 1u : 0u, rbar);
         }
-        if (lane == 0) st_async_b32(rp + off_f, any ? 1u : 0u, rbar);
       }
       if (!C::kConv && valid < kN) {
         // dense bf16 tail: rows past the unit hold whatever the cache holds
@@ -1052,16 +1083,15 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           *reinterpret_cast<uint4*>(dst + (q >> 3) * kBlkBytes + swz_chunk(row, q & 7)) = v;
         }
       }
-      // rotary rows -> swizzled operand (with half rows, the CTA's 16-byte
-      // chunks 4 rank .. 4 rank + 3 of the 64-column operand row, the only
-      // ones its QK reads)
-      constexpr int kPeChunks = C::kRawPe / 16;
-      const int pe_chunk0 = kPeChunks == 8 ? 0 : 4 * (int)rank;
-      for (int idx = t; idx < kN * kPeChunks; idx += 32 * C::kConvWarps) {
-        const int row = idx / kPeChunks, q = idx % kPeChunks;
+      // rotary rows -> the CTA's 32 columns (the only ones its QK reads) as
+      // unswizzled core matrices; gathered rows are whole, so their 16-byte
+      // chunks 4 rank .. 4 rank + 3
+      const int pe_chunk0 = C::kRawPe == 128 ? 4 * (int)rank : 0;
+      for (int idx = t; idx < kN * 4; idx += 32 * C::kConvWarps) {
+        const int row = idx >> 2, q = idx & 3;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < valid) v = *reinterpret_cast<const uint4*>(rpe(r) + row * C::kRawPe + q * 16);
-        *reinterpret_cast<uint4*>(ope(j) + swz_chunk(row, pe_chunk0 + q)) = v;
+        if (row < valid) v = *reinterpret_cast<const uint4*>(rpe(r) + row * C::kRawPe + (pe_chunk0 + q) * 16);
+        *reinterpret_cast<uint4*>(ope(j) + (row >> 3) * 512 + q * 128 + (row & 7) * 16) = v;
       }
       fence_async_smem();
       __syncwarp();

@@ -113,6 +113,12 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
   return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46) | (2ull << 61);
 }
+// smem matrix descriptor without swizzle (8-row x 16-byte core matrices):
+// lbo = bytes between core matrices along K, sbo = along M/N; version 1
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr & 0x3FFFF) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | (1ull << 46);
+}
 // instruction descriptor, kind::f16: bf16 x bf16 -> fp32
 __host__ __device__ constexpr uint32_t idesc(int M, int N, bool b_mn_major, bool a_mn_major = false) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) |
@@ -246,6 +252,12 @@ __device__ __forceinline__ void bulk_store(void* gdst, const void* src, uint32_t
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
                "r"(sa(src)), "r"(bytes)
                : "memory");
+}
+// shared::cta -> a cluster peer's shared memory, completing bytes on the
+// peer's mbarrier (remote addresses from mapa)
+__device__ __forceinline__ void bulk_s2c(uint32_t remote_dst, const void* src, uint32_t bytes, uint32_t remote_bar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(remote_dst), "r"(sa(src)), "r"(bytes), "r"(remote_bar) : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the bulk stores of this thread have read their shared-memory sources (their
