@@ -51,7 +51,7 @@ struct AbsorbParams {
 
 __device__ bool wait_bounded(uint64_t* b, uint32_t parity) {
   for (long it = 0; it < kSpin; ++it)
-    if (bar_try(b, parity)) return true;
+    if (bar_try_local(b, parity)) return true;
   return false;
 }
 
@@ -118,7 +118,7 @@ __global__ void __launch_bounds__(128) absorb_kernel(const __grid_constant__ Abs
       }
     } else {
       // the loads issued above still land in this CTA's shared memory
-      for (long it = 0; it < kSpin && !bar_try(&full, 0); ++it) {}
+      for (long it = 0; it < kSpin && !bar_try_local(&full, 0); ++it) {}
     }
     s_ok = landed;
     mma_commit(&done);   // arrives once the MMAs (if any) are complete

@@ -288,6 +288,15 @@ struct Waiter {
     atomicOr(status, kDevTimeout);
     return false;
   }
+  __device__ __forceinline__ bool wait_local(uint64_t* b, uint32_t parity) {
+    for (long it = 0; it < lim; ++it) {
+      if (bar_try_local(b, parity)) return true;
+      if (bars->abort) return false;
+    }
+    bars->abort = 1;
+    atomicOr(status, kDevTimeout);
+    return false;
+  }
   // teardown variant: ignores the abort flag (the awaited operation was
   // issued by this thread and completes on its own), still bounded
   __device__ __forceinline__ void drain(uint64_t* b, uint32_t parity) {
@@ -566,7 +575,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     for (int i = 0; i < ntiles && !bars->abort; ++i) {
       const int j = i % kSlots;
       const uint32_t use = i / kSlots;
-      if (!wt.wait(C::kConv ? &bars->rfree[j] : &bars->empty[j], (use & 1) ^ 1)) break;
+      if (!wt.wait_local(C::kConv ? &bars->rfree[j] : &bars->empty[j], (use & 1) ^ 1)) break;
       const int e0 = u.t0 + i * kN;
       const int slot = u.b / p.mtp_s;   // cache slot of the sequence (several per slot: multi-token)
       if (unit_id == 0 && i == p.withhold_tile) {
@@ -576,7 +585,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       }
       // the tile that holds the new row: its writers fenced their stores
       // for the tensor copies before arriving
-      if (app && i == ntiles - 1 && !wt.wait(&bars->appended, 0)) break;
+      if (app && i == ntiles - 1 && !wt.wait_local(&bars->appended, 0)) break;
       if (!kSparse) {
         if (lane == 0) {
           if (kFmt == 0) {
@@ -638,7 +647,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       int nreq = 0;
       for (int i = 0; i < ntiles; ++i) {
         const int j = i % C::kStages, b = psel(i);
-        if (!wt.wait(&bars->pfull[b], ppar(i))) break;
+        if (!wt.wait_local(&bars->pfull[b], ppar(i))) break;
         if (!wt.wait(&bars->rpfull[b], ppar(i))) break;
         // the peer's rows were written by another CTA's asynchronous stores:
         // order them before the tensor core reads the buffer
@@ -694,7 +703,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       constexpr uint32_t id_qk = idesc(128, kN, false);
       const uint64_t d_k0 = sdesc(sa(opl(0)), 16, 1024);
       const uint32_t t_q = tmem + kTmemQ;
-      if (live && wt.wait(&bars->qready, 0)) tc_after();
+      if (live && wt.wait_local(&bars->qready, 0)) tc_after();
       for (int k = 0; k < ntiles && !bars->abort; ++k) {
         const int j = k % C::kStages, b = ssel(k);
         bool paced = false;
@@ -710,8 +719,8 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           }
           break;
         }
-        if (!wt.wait(C::kConv ? &bars->deq[j] : &bars->full[j], (k / C::kStages) & 1)) break;
-        if (!wt.wait(&bars->sfree[b], spar(k) ^ 1)) break;
+        if (!wt.wait_local(C::kConv ? &bars->deq[j] : &bars->full[j], (k / C::kStages) & 1)) break;
+        if (!wt.wait_local(&bars->sfree[b], spar(k) ^ 1)) break;
         tc_after();
         const uint32_t sd = tmem + kTmemS + b * kN;
         const uint64_t kd = sdesc_at(d_k0, j * C::kStage);
@@ -772,6 +781,18 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       return true;
     };
     // a bounded wait that serves rescale requests while it polls
+    auto swait_local = [&](uint64_t* bar, uint32_t parity) -> bool {
+      for (long it = 0; it < wt.lim; ++it) {
+        if (bar_try_local(bar, parity)) return true;
+        if (bars->abort) return false;
+        if (serve()) it = 0;
+      }
+      if (!bars->abort) {
+        bars->abort = 1;
+        atomicOr(p.ws.status, kDevTimeout);
+      }
+      return false;
+    };
     auto swait = [&](uint64_t* bar, uint32_t parity) -> bool {
       for (long it = 0; it < wt.lim; ++it) {
         if (bar_try(bar, parity)) return true;
@@ -792,7 +813,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     const uint32_t xf0 = mapa(&bars->xfull[0], peer);
     for (int i = 0; i < ntiles; ++i) {
       const int b = ssel(i);
-      if (!swait(&bars->sfull[b], spar(i))) break;
+      if (!swait_local(&bars->sfull[b], spar(i))) break;
       __syncwarp();
       tc_after();
       uint32_t r[24];
@@ -861,7 +882,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
       const int j = i % C::kStages, sb_i = ssel(i), b = psel(i);
       const uint32_t par = ppar(i);
       float sc[24];
-      ok = ok && wt.wait(&bars->sfull[sb_i], spar(i));
+      ok = ok && wt.wait_local(&bars->sfull[sb_i], spar(i));
       {
         tc_after();
         uint32_t r[24];
@@ -1049,9 +1070,9 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
     for (int i = 0; i < ntiles; ++i) {
       const int r = i % C::kRawRing, j = i % C::kStages;
       // FP8: stages 1-3 hold the staged query until it is in tensor memory
-      if (kFmt == 1 && i == 1 && !wt.wait(&bars->qready, 0)) break;
-      if (!wt.wait(&bars->full[r], (i / C::kRawRing) & 1)) break;
-      if (!wt.wait(&bars->empty[j], ((i / C::kStages) & 1) ^ 1)) break;
+      if (kFmt == 1 && i == 1 && !wt.wait_local(&bars->qready, 0)) break;
+      if (!wt.wait_local(&bars->full[r], (i / C::kRawRing) & 1)) break;
+      if (!wt.wait_local(&bars->empty[j], ((i / C::kStages) & 1) ^ 1)) break;
       const int valid = min(kN, u.t1 - (u.t0 + i * kN));
       uint8_t* dst = opl(j);
       if (kFmt == 1) {

@@ -74,11 +74,25 @@ __device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes) {
 // Non-suspending probe of a barrier phase.  (A suspending try_wait was seen to
 // return up to microseconds after phases completed by tcgen05.commit or by
 // remote arrivals, which serialised the pipeline; a polling test_wait notices
-// them at once.)
+// them at once.)  Cluster-scope acquire: for barriers that the peer CTA's
+// stores, copies or commits complete.
 __device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{ .reg .pred p; mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
+      "selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(sa(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// The same probe with CTA-scope acquire, for barriers that only this CTA's
+// threads, tensor-core commits and tensor copies complete.  It is measurably
+// cheaper inside the decode kernel's per-tile hand-offs.
+__device__ __forceinline__ bool bar_try_local(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2; "
       "selp.u32 %0, 1, 0, p; }"
       : "=r"(ok)
       : "r"(sa(b)), "r"(parity)
