@@ -37,7 +37,8 @@
 // per column); S double buffer [400,448) and [448,496) fp32.
 //
 // Warp roles (512 threads; 544 for dense FP8 tiles):
-//   warp 0  producer: TMA tiles (dense) or four-row TMA gathers (gather)
+//   warp 0  producer: TMA tiles (dense), or four-row TMA gathers of the
+//           latent halves and 16-byte copies of the small per-row pieces (gather)
 //   warp 1  QK issuer (one thread) and tensor-memory owner
 //   warp 2  PV issuer (one thread); in a dense bf16 call it first works out
 //           the split schedule and the pair's unit (schedule.cuh)
@@ -162,13 +163,10 @@ struct Cfg {
   static constexpr int kStage = kOplBytes + kOpeBytes;
   static constexpr int kStages = kConv ? (kFmt == 1 ? 4 : 2) : 4;
   static constexpr int kRawRow = kFmt == 1 ? kHalf : kHalf * 2;  // bytes of a raw latent half row
-  // FP8 scales, 16 B per row: dense tiles land as 48 consecutive rows; a
-  // gather lands 4 rows per 128-byte slot (a tensor copy's shared-memory
-  // destination is 128-byte aligned)
-  static constexpr int kScBytes = kFmt == 1 ? (kSparse ? 2048 : 1024) : 0;
-  // rotary bytes per raw row: dense FP8 loads only the CTA's 32 columns (the
-  // 32 its QK reads); gathers land whole 128-byte rows
-  static constexpr int kRawPe = (kFmt == 1 && !kSparse) ? kPeHalf * 2 : 128;
+  // FP8 scales, 16 B per row, 48 consecutive rows
+  static constexpr int kScBytes = kFmt == 1 ? 1024 : 0;
+  // rotary bytes per raw row: only the CTA's 32 columns (the 32 its QK reads)
+  static constexpr int kRawPe = kPeHalf * 2;
   static constexpr int kRaw = kConv ? kN * kRawRow + kScBytes + kN * kRawPe : 0;
   static constexpr int kRawSlots = kConv ? (kFmt == 1 ? (kSparse ? 3 : 4) : 2) : 0;
   // the converter's ring length in index arithmetic (never zero, so the
@@ -197,8 +195,8 @@ struct Cfg {
 struct TcParams {
   DecodeParams p;
   CUtensorMap m_kv;   // bf16: latent (box 64 x N), FP8: codes (box 256 x N)
-  CUtensorMap m_pe;   // rotary (box 64 x N, 128-byte swizzle)
-  CUtensorMap m_sc;   // FP8 scales (box 4 x N)
+  CUtensorMap m_pe;   // rotary (dense tiles; box 64 or 32 x N)
+  CUtensorMap m_sc;   // FP8 scales (dense tiles; box 4 x N)
   CUtensorMap m_ql;   // q_latent [B][128][512] (box 64 x 128, 128-byte swizzle)
   CUtensorMap m_qp;   // q_pe [B][128][64] (box 64 x 128, 128-byte swizzle)
   CUtensorMap m_po;   // partial outputs [units][128][512] fp32 (box 32 x 128, 128-byte swizzle)
@@ -443,7 +441,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
   // ---------------------------------------------------------------- set-up
   if (threadIdx.x == 0) {
     for (int j = 0; j < C::kStages; ++j) {
-      bar_init(&bars->full[j], 1);
+      bar_init(&bars->full[j], kSparse ? 33 : 1);   // gathers: + the producer's 32 lanes' copies
       bar_init(&bars->deq[j], C::kConvWarps);
       bar_init(&bars->empty[j], 1);
     }
@@ -601,28 +599,43 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           }
         }
       } else {
-        // gathered rows, four per TMA instruction (tile::gather4 on row-high
-        // boxes): lane g takes rows 4g..4g+3 of the tile -- its latent half,
-        // the FP8 scales, the rotary row -- each landing 128-byte aligned.  A
-        // short last group repeats its last row; the converter ignores rows
-        // past the unit.
+        // gathered rows: the latent halves four per TMA instruction
+        // (tile::gather4 on row-high boxes, lane g rows 4g..4g+3; a short
+        // last group repeats its last row), the small per-row pieces -- the
+        // FP8 scales, the CTA's 32 rotary columns -- by 16-byte asynchronous
+        // copies from every lane, which keeps them off the copy engine whose
+        // issue rate bounds the gather.  The converter ignores rows past the
+        // unit.
         const int v = min(kN, u.t1 - e0);
         const int groups = (v + 3) / 4;
-        constexpr uint32_t kGroupBytes = 4 * (C::kRawRow + (kFmt == 1 ? 16 : 0) + 128);
-        if (lane == 0) bar_expect_tx(&bars->full[j], (uint32_t)groups * kGroupBytes);
+        // the tile's rows: lane l reads list positions l and l + 32 (one
+        // round of index loads), shared by shuffles
+        const int* gl = p.ws.gidx + (size_t)u.b * p.K + e0;
+        const int base = u.b * p.max_seq_len;
+        const int g0 = base + gl[min(lane, v - 1)], g1 = base + gl[min(lane + 32, v - 1)];
+        if (lane == 0) bar_expect_tx(&bars->full[j], (uint32_t)groups * 4 * C::kRawRow);
         __syncwarp();
-        if (lane < groups) {
-          const int* gl = p.ws.gidx + (size_t)u.b * p.K + e0;
-          const int base = u.b * p.max_seq_len, c = 4 * lane;
-          int r[4];
+        int r[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) r[k] = base + gl[min(c + k, v - 1)];
-          tma_gather4(raw(j) + c * C::kRawRow, &tp.m_kv, rank * kHalf, r[0], r[1], r[2], r[3],
-                      &bars->full[j]);
-          if (kFmt == 1)
-            tma_gather4(rsc(j) + lane * 128, &tp.m_sc, 0, r[0], r[1], r[2], r[3], &bars->full[j]);
-          tma_gather4(rpe(j) + c * 128, &tp.m_pe, 0, r[0], r[1], r[2], r[3], &bars->full[j]);
+        for (int k = 0; k < 4; ++k) {
+          const int t = min(4 * lane + k, v - 1);
+          const int a0 = __shfl_sync(0xffffffffu, g0, t & 31), a1 = __shfl_sync(0xffffffffu, g1, t & 31);
+          r[k] = t < 32 ? a0 : a1;
         }
+        if (lane < groups)
+          tma_gather4(raw(j) + 4 * lane * C::kRawRow, &tp.m_kv, rank * kHalf, r[0], r[1], r[2], r[3],
+                      &bars->full[j]);
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          const int t = lane + 32 * h2;
+          if (t >= v) break;
+          const size_t row = (size_t)(h2 ? g1 : g0);
+          if (kFmt == 1) cp_async16(rsc(j) + t * 16, p.kv_scale + row * kNblk);
+          const uint8_t* pe = static_cast<const uint8_t*>(p.pe) + row * (kDr * 2) + rank * (kPeHalf * 2);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) cp_async16(rpe(j) + t * C::kRawPe + q * 16, pe + q * 16);
+        }
+        cp_async_arrive(&bars->full[j]);   // every lane, once per tile
       }
       issued = i + 1;
     }
@@ -1082,7 +1095,7 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
           if (row < valid) {
             const uint4 v = *reinterpret_cast<const uint4*>(raw(r) + row * kHalf + q * 16);
-            const uint8_t* srow = rsc(r) + (kSparse ? (row >> 2) * 128 + (row & 3) * 16 : row * 16);
+            const uint8_t* srow = rsc(r) + row * 16;
             const float sc = reinterpret_cast<const float*>(srow)[rank * 2 + (q >> 3)];
             dequant16(v, sc, lo, hi);
           }
@@ -1104,14 +1117,12 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           *reinterpret_cast<uint4*>(dst + (q >> 3) * kBlkBytes + swz_chunk(row, q & 7)) = v;
         }
       }
-      // rotary rows -> the CTA's 32 columns (the only ones its QK reads) as
-      // unswizzled core matrices; gathered rows are whole, so their 16-byte
-      // chunks 4 rank .. 4 rank + 3
-      const int pe_chunk0 = C::kRawPe == 128 ? 4 * (int)rank : 0;
+      // the CTA's 32 rotary columns (the only ones its QK reads) -> unswizzled
+      // core matrices
       for (int idx = t; idx < kN * 4; idx += 32 * C::kConvWarps) {
         const int row = idx >> 2, q = idx & 3;
         uint4 v = make_uint4(0, 0, 0, 0);
-        if (row < valid) v = *reinterpret_cast<const uint4*>(rpe(r) + row * C::kRawPe + (pe_chunk0 + q) * 16);
+        if (row < valid) v = *reinterpret_cast<const uint4*>(rpe(r) + row * C::kRawPe + q * 16);
         *reinterpret_cast<uint4*>(ope(j) + (row >> 3) * 512 + q * 128 + (row & 7) * 16) = v;
       }
       fence_async_smem();
@@ -1329,13 +1340,11 @@ cudaError_t launch_decode_tc(const DecodeParams& p, cudaStream_t s) {
   const uint32_t n = (uint32_t)decode_tc_granule(p.fmt, p.K > 0);   // tile rows
   bool ok = true;
   if (p.K) {
-    // gathers: 2D maps over all rows [B * S], one row high, for tile::gather4
+    // gathers: a 2D map of the latent rows [B * S], one row high, for
+    // tile::gather4 (scales and rotary columns go by 16-byte copies)
     const uint64_t rows = B * S;
     ok = encode2_rows(&tp.m_kv, p.fmt == 0 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
-                      p.fmt == 0 ? 2 : 1, p.kv, kDc, rows, kHalf) &&
-         encode2_rows(&tp.m_pe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.pe, kDr, rows, kDr) &&
-         (p.fmt == 0 || encode2_rows(&tp.m_sc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, p.kv_scale, kNblk,
-                                     rows, kNblk));
+                      p.fmt == 0 ? 2 : 1, p.kv, kDc, rows, kHalf);
   } else {
     if (p.fmt == 0) {
       ok = encode3(&tp.m_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p.kv, kDc, S, slots, 64, n,

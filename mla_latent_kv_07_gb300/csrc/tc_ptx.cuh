@@ -99,6 +99,15 @@ __device__ __forceinline__ bool bar_try_local(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// 16-byte asynchronous copy, global -> this CTA's shared memory (through L2)
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa(dst)), "l"(src) : "memory");
+}
+// one arrival on b once the thread's earlier cp.async copies have landed
+// (counted in the barrier's expected arrivals)
+__device__ __forceinline__ void cp_async_arrive(uint64_t* b) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(sa(b)) : "memory");
+}
 __device__ __forceinline__ uint32_t mapa(const void* p, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(sa(p)), "r"(rank));
