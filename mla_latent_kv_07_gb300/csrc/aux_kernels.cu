@@ -80,7 +80,8 @@ __device__ int block_exclusive_scan(int v, int* smem /* >= 33 ints */, int* tota
 }
 
 // ------------------------------------------------------------ sparse prep
-// One CTA per sequence.  The positions [0, T) are taken in windows of
+// One CTA per sequence (and, with new rows to write, one more per sequence
+// for its row, so the list work does not wait for it).  The positions [0, T) are taken in windows of
 // kPrepWindow: every valid list entry in the window sets its bit in a shared
 // bitmap (repeats set it once), then each thread counts the set bits of its
 // run of words, a block scan turns the counts into output offsets, and the
@@ -92,22 +93,22 @@ __global__ void __launch_bounds__(1024) sparse_prep_kernel(const int* __restrict
                                                           const int* __restrict__ end_pos,
                                                           int max_end_pos, Workspace ws,
                                                           int* gidx_out, int* gcount_out,
-                                                          const AppendRows ap) {
+                                                          const AppendRows ap, int B) {
   __shared__ uint32_t bm[kPrepWindow / 32];
   __shared__ int scan_smem[33];
   pdl_wait();   // the previous call's kernels may still read the workspace and the cache
   pdl_trigger();
+  // the fused append: CTA B + b writes sequence b's new row, position
+  // end_pos[b] - 1 (warps 0-3), beside the list CTAs
+  if ((int)blockIdx.x >= B) {
+    const int b = blockIdx.x - B, row = end_pos[b] - 1;
+    if (row >= 0 && row < ap.max_seq_len && threadIdx.x < 128) append_row(ap, b, row, threadIdx.x);
+    return;
+  }
   const int b = blockIdx.x;
   const int end = end_pos[b];
   uint32_t flags = 0;
-  // the fused append: the new row is position end_pos[b] - 1 (warps 0-3)
-  if (ap.kv_new) {
-    const int row = end - 1;
-    if (row < 0 || row >= ap.max_seq_len)
-      flags |= kDevAppendSkipped;
-    else if (threadIdx.x < 128)
-      append_row(ap, b, row, threadIdx.x);
-  }
+  if (ap.kv_new && (end - 1 < 0 || end - 1 >= ap.max_seq_len)) flags |= kDevAppendSkipped;
   int T = end;
   if (T < 0 || T > max_end_pos) {
     flags |= kDevEndPosClamped;
@@ -608,8 +609,8 @@ cudaError_t launch_append_host_pos(const AppendParams& p, cudaStream_t s) {
 cudaError_t launch_sparse_prep(const int* topk, int K, const int* end_pos, int max_end_pos,
                                const Workspace& ws, int B, int* gidx_out, int* gcount_out,
                                const AppendRows& ap, cudaStream_t s) {
-  return launch_pdl(sparse_prep_kernel, dim3(B), dim3(1024), 0, s, topk, K, end_pos, max_end_pos, ws,
-                    gidx_out, gcount_out, ap);
+  return launch_pdl(sparse_prep_kernel, dim3(ap.kv_new ? 2 * B : B), dim3(1024), 0, s, topk, K, end_pos,
+                    max_end_pos, ws, gidx_out, gcount_out, ap, B);
 }
 
 cudaError_t launch_schedule(const int* end_pos, int max_end_pos, const Workspace& ws, int B,
