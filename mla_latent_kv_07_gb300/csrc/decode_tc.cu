@@ -1046,7 +1046,9 @@ __global__ void __launch_bounds__(Cfg<kFmt, kSparse>::kThreads, 1)
           *reinterpret_cast<uint4*>(v + blk * kBlkBytes + swz_chunk(row, ch)) = make_uint4(0, 0, 0, 0);
         }
       }
-      fence_async_smem();
+      // (converter variants: the fence before the bulk copy already ordered
+      // every generic write of this tile's P for the tensor core)
+      if constexpr (!C::kConv) fence_async_smem();
       tc_before();
       __syncwarp();
       if (lane == 0) bar_arrive(&bars->pfull[b]);
