@@ -18,6 +18,9 @@
 // W_UK's [n][c] layout as an MN-major A operand; W_UV and the activations are
 // K-major.  All tiles arrive by TMA in the 128-byte swizzled layout.
 //
+// The weights are constant, so their loads are issued before the wait on the
+// previous kernel (programmatic dependent launch): they stream in while it
+// finishes; the activations follow the wait.
 // Warps: thread 0 issues the loads and the MMAs; all four warps move the
 // result from tensor memory (lane = c or v) to global memory (a warp writes
 // 32 consecutive bf16 of one sequence).  Waits are bounded; on expiry a
@@ -89,15 +92,19 @@ __global__ void __launch_bounds__(128) absorb_kernel(const __grid_constant__ Abs
   __syncthreads();
   tc_after();
   const uint32_t tmem = tslot;
-  pdl_wait();   // the inputs may come from the previous kernel
-  pdl_trigger();
-
-  __shared__ int s_ok;
+  // the weights are constant: their loads go out before the wait on the
+  // previous kernel, so they stream in while it finishes
   if (threadIdx.x == 0) {
     bar_expect_tx(&full, kWBlocks * kSwBlk + kXBlocks * kXBlk);
     const int row0 = kQ ? 0 : 128;     // W_UK or W_UV rows of head h
     for (int cb = 0; cb < kWBlocks; ++cb)
       tma3(wsm + cb * kSwBlk, &ap.m_w, 64 * (cb + 2 * mb), row0, h, &full);
+  }
+  pdl_wait();   // the activations may come from the previous kernel
+  pdl_trigger();
+
+  __shared__ int s_ok;
+  if (threadIdx.x == 0) {
     for (int k = 0; k < kXBlocks; ++k) tma3(xsm + k * kXBlk, &ap.m_x, 64 * k, h, b0, &full);
     const bool landed = wait_bounded(&full, 0);
     if (landed) {
