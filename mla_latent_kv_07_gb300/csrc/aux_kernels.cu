@@ -81,12 +81,12 @@ __device__ int block_exclusive_scan(int v, int* smem /* >= 33 ints */, int* tota
 
 // ------------------------------------------------------------ sparse prep
 // One CTA per sequence (and, with new rows to write, one more per sequence
-// for its row, so the list work does not wait for it).  The positions [0, T) are taken in windows of
-// kPrepWindow: every valid list entry in the window sets its bit in a shared
-// bitmap (repeats set it once), then each thread counts the set bits of its
-// run of words, a block scan turns the counts into output offsets, and the
-// set positions are written in increasing order.  Invalid entries set
-// nothing; the list's tail is -1.
+// for its row, so the list work does not wait for it).  The positions
+// [0, T) are taken in windows of kPrepWindow: every valid list entry in the
+// window sets its bit in a shared bitmap (repeats set it once), then each
+// thread counts the set bits of its run of words, a block scan turns the
+// counts into output offsets, and the set positions are written in
+// increasing order.  Invalid entries set nothing; the list's tail is -1.
 constexpr int kPrepWindow = 1 << 18;   // positions per pass: a 32 KB bitmap
 
 __global__ void __launch_bounds__(1024) sparse_prep_kernel(const int* __restrict__ topk, int K,
