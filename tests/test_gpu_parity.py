@@ -491,6 +491,36 @@ def test_sparse_fused_append_sees_the_new_row(fmt):
     check_close(f64(lse).reshape(-1), ref_lse, "lse")
 
 
+@pytest.mark.parametrize("H", [128, 64])
+def test_sparse_bf16_cache_lists_and_fused_append(H):
+    # the gather variants on a bf16 cache (the tensor-memory kernel at
+    # H = 128, the warp-MMA kernel below): split and single-unit sequences,
+    # last tiles of fewer than 32 and of 32-47 rows, repeats and invalid
+    # entries, a one-position sequence, with the step's new rows written by
+    # the list prep; every output, log-sum-exp and cache byte checked
+    B, S, K = 4, 600, 320
+    oc = oracle_cache(_rand_bf16((B, S, 512), 171), _rand_bf16((B, S, 64), 172), 0)
+    dc = device_cache(oc)
+    ql, qp = _rand_bf16((B, H, 512), 173), _rand_bf16((B, H, 64), 174)
+    ends = np.array([600, 45, 230, 1], np.int32)
+    rng = np.random.default_rng(175)
+    topk = np.full((B, K), -1, np.int32)
+    topk[0] = rng.permutation(600)[:K]                 # 320 rows: 6 full tiles + 32
+    topk[1, :50] = rng.permutation(50)                 # 45 valid rows (44 is the new row)
+    topk[2] = rng.integers(-3, 260, K)                 # repeats, some past end_pos
+    topk[3, :3] = [0, 0, 5]                            # only the new row
+    kv_new, pe_new = _rand_bf16((B, 512), 176), _rand_bf16((B, 64), 177)
+    out, lse = mla.decode_sparse(dc, ql.cuda(), qp.cuda(), torch.from_numpy(ends).cuda(), S, 0.17,
+                                 torch.from_numpy(topk).cuda(), kv_new=kv_new.cuda(), pe_new=pe_new.cuda())
+    orc.cache_append(oc, bits(kv_new), bits(pe_new), ends - 1)
+    torch.cuda.synchronize()
+    assert np.array_equal(bits(dc.kv.cpu()), oc["kv"])
+    assert np.array_equal(bits(dc.pe.cpu()), oc["pe"])
+    ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), ends, 0.17, topk=topk)
+    check_close(f64(out).reshape(-1, 512), ref, "out")
+    check_close(f64(lse).reshape(-1), ref_lse, "lse")
+
+
 def test_sparse_gather_lists_span_bitmap_windows():
     # positions past 2^18 and 2^19: the list prep takes the sequence in
     # windows of 2^18 positions; entries on both sides of each window edge,
