@@ -491,15 +491,16 @@ def test_sparse_fused_append_sees_the_new_row(fmt):
     check_close(f64(lse).reshape(-1), ref_lse, "lse")
 
 
-@pytest.mark.parametrize("H", [128, 64])
-def test_sparse_bf16_cache_lists_and_fused_append(H):
+@pytest.mark.parametrize("fmt,H", [(0, 128), (0, 64), (1, 64)])
+def test_sparse_gather_variants_lists_and_fused_append(fmt, H):
     # the gather variants on a bf16 cache (the tensor-memory kernel at
-    # H = 128, the warp-MMA kernel below): split and single-unit sequences,
-    # last tiles of fewer than 32 and of 32-47 rows, repeats and invalid
-    # entries, a one-position sequence, with the step's new rows written by
-    # the list prep; every output, log-sum-exp and cache byte checked
+    # H = 128, the warp-MMA kernel below) and on an FP8 cache at H = 64:
+    # split and single-unit sequences, last tiles of fewer than 32 and of
+    # 32-47 rows, repeats and invalid entries, a one-position sequence, with
+    # the step's new rows written by the list prep; every output, log-sum-exp
+    # and cache byte checked
     B, S, K = 4, 600, 320
-    oc = oracle_cache(_rand_bf16((B, S, 512), 171), _rand_bf16((B, S, 64), 172), 0)
+    oc = oracle_cache(_rand_bf16((B, S, 512), 171), _rand_bf16((B, S, 64), 172), fmt)
     dc = device_cache(oc)
     ql, qp = _rand_bf16((B, H, 512), 173), _rand_bf16((B, H, 64), 174)
     ends = np.array([600, 45, 230, 1], np.int32)
@@ -514,7 +515,11 @@ def test_sparse_bf16_cache_lists_and_fused_append(H):
                                  torch.from_numpy(topk).cuda(), kv_new=kv_new.cuda(), pe_new=pe_new.cuda())
     orc.cache_append(oc, bits(kv_new), bits(pe_new), ends - 1)
     torch.cuda.synchronize()
-    assert np.array_equal(bits(dc.kv.cpu()), oc["kv"])
+    if fmt == 0:
+        assert np.array_equal(bits(dc.kv.cpu()), oc["kv"])
+    else:
+        assert np.array_equal(dc.kv.cpu().numpy(), oc["kv"])
+        assert np.array_equal(dc.kv_scale.cpu().numpy().view(np.uint32), oc["kv_scale"].view(np.uint32))
     assert np.array_equal(bits(dc.pe.cpu()), oc["pe"])
     ref, ref_lse = orc.decode_absorbed(oc, bits(ql), bits(qp), ends, 0.17, topk=topk)
     check_close(f64(out).reshape(-1, 512), ref, "out")
